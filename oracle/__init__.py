@@ -1,0 +1,169 @@
+"""fp64 CPU oracle of the selective SSM scan and its single-token state update.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline leg are the only callers. The product path (the CUDA library and its
+Python binding) never imports this package, and this package imports nothing
+from the product package.
+
+The arithmetic lives in ``scan_oracle.c`` (plain C, double precision, one row
+at a time, sequential in time). This module only builds that file with gcc,
+widens the caller's inputs exactly to float64, gathers the requested rows and
+calls it through ctypes.
+
+Every function here follows the definition on the pages:
+  * "Mamba 论文精读" (youngju.dev) §2.2 (ZOH: A_bar = exp(Delta A); recurrence
+    h_t = A_bar h_{t-1} + B_bar x_t, y_t = C h_t), §3.1 (Delta = softplus(...)),
+    §3.3 (simplified scan: B_bar = Delta B, h starts at zero), §3.4 (gate
+    y * silu(z));
+  * "Mamba的基础知识" (weblog-19d), 状态空间模型 section (skip term D u);
+  * "mamba->jamba" (blog.csdn.net) §2.2 (constant-time recurrent inference).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "scan_oracle.c")
+LIBRARY = os.path.join(_HERE, "liboracle.so")
+
+_P = ctypes.POINTER(ctypes.c_double)
+_PI = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(source: str = SOURCE, output: str = LIBRARY, extra_flags: Sequence[str] = ()) -> str:
+    """Compile the C oracle with gcc (-O2, strict IEEE: no fast-math, no FMA contraction)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+           *extra_flags, source, "-o", output, "-lm"]
+    subprocess.run(cmd, check=True)
+    return output
+
+
+class Oracle:
+    """ctypes handle on one build of the C oracle (the default one, or a test's variant)."""
+
+    def __init__(self, library: Optional[str] = None):
+        path = library or LIBRARY
+        if library is None and (not os.path.exists(path)
+                                or os.path.getmtime(path) < os.path.getmtime(SOURCE)):
+            build()
+        self.lib = ctypes.CDLL(path)
+        self.lib.oracle_scan.restype = ctypes.c_int
+        self.lib.oracle_scan.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _PI,
+                                         ctypes.c_int, _P, _P]
+        self.lib.oracle_state_update.restype = ctypes.c_int
+        self.lib.oracle_state_update.argtypes = [ctypes.c_int64, ctypes.c_int64, _P,
+                                                 _P, _P, _P, _P, _P, _P, _P, _P, _PI,
+                                                 ctypes.c_int, _P]
+
+    # -- scan ---------------------------------------------------------------
+    def scan(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+             rows=None, return_state=True):
+        """Selective scan of the rows ``rows`` (flat indices b*dim + d; all rows if None).
+
+        u, delta, z : (batch, dim, L);  B, C : (batch, N, L);  A : (dim, N);
+        D, delta_bias : (dim,). Any float dtype (bf16 torch tensors included) is
+        widened exactly to float64 first.
+        Returns y of shape (len(rows), L) and, if asked, the final state
+        (len(rows), N), both float64.
+        """
+        u = _f64(u)
+        batch, dim, L = u.shape
+        N = _f64(A).shape[1]
+        rows = np.arange(batch * dim, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+        b_idx = np.ascontiguousarray(rows // dim)
+        d_idx = rows % dim
+        ur = np.ascontiguousarray(u.reshape(batch * dim, L)[rows])
+        dr = np.ascontiguousarray(_f64(delta).reshape(batch * dim, L)[rows])
+        zr = None if z is None else np.ascontiguousarray(_f64(z).reshape(batch * dim, L)[rows])
+        Ar = np.ascontiguousarray(_f64(A)[d_idx])
+        Dr = None if D is None else np.ascontiguousarray(_f64(D)[d_idx])
+        br = None if delta_bias is None else np.ascontiguousarray(_f64(delta_bias)[d_idx])
+        Bf = np.ascontiguousarray(_f64(B))
+        Cf = np.ascontiguousarray(_f64(C))
+        assert Bf.shape == (batch, N, L) and Cf.shape == (batch, N, L)
+        y = np.empty((len(rows), L), np.float64)
+        h = np.empty((len(rows), N), np.float64) if return_state else None
+        rc = self.lib.oracle_scan(len(rows), L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar),
+                                  _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf), _iptr(b_idx),
+                                  int(bool(softplus)), _ptr(y), _ptr(h))
+        if rc != 0:
+            raise ValueError(f"oracle_scan rejected dstate={N}")
+        return (y, h) if return_state else y
+
+    # -- state update ---------------------------------------------------------
+    def state_update(self, state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                     softplus=False, rows=None):
+        """One decode step of the rows ``rows`` (flat b*dim + d; all rows if None).
+
+        state : (batch, dim, N);  u, delta, z : (batch, dim);  B, C : (batch, N);
+        A : (dim, N); D, delta_bias : (dim,).
+        Returns (y (len(rows),), new_state (len(rows), N)), float64; the input
+        state is not modified.
+        """
+        s = _f64(state)
+        batch, dim, N = s.shape
+        rows = np.arange(batch * dim, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+        b_idx = np.ascontiguousarray(rows // dim)
+        d_idx = rows % dim
+        sr = np.ascontiguousarray(s.reshape(batch * dim, N)[rows]).copy()
+        ur = np.ascontiguousarray(_f64(u).reshape(batch * dim)[rows])
+        dr = np.ascontiguousarray(_f64(delta).reshape(batch * dim)[rows])
+        zr = None if z is None else np.ascontiguousarray(_f64(z).reshape(batch * dim)[rows])
+        Ar = np.ascontiguousarray(_f64(A)[d_idx])
+        Dr = None if D is None else np.ascontiguousarray(_f64(D)[d_idx])
+        br = None if delta_bias is None else np.ascontiguousarray(_f64(delta_bias)[d_idx])
+        Bf = np.ascontiguousarray(_f64(B))
+        Cf = np.ascontiguousarray(_f64(C))
+        assert Bf.shape == (batch, N) and Cf.shape == (batch, N)
+        y = np.empty(len(rows), np.float64)
+        rc = self.lib.oracle_state_update(len(rows), N, _ptr(sr), _ptr(ur), _ptr(dr), _ptr(zr),
+                                          _ptr(Ar), _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf),
+                                          _iptr(b_idx), int(bool(softplus)), _ptr(y))
+        if rc != 0:
+            raise ValueError(f"oracle_state_update rejected dstate={N}")
+        return y, sr
+
+
+def _f64(x):
+    """Exact widening of a numpy array or (CPU) torch tensor of any float dtype to float64."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor; bf16 -> f32 -> f64 is exact
+        import torch
+        t = x.detach().to("cpu")
+        if t.dtype in (torch.bfloat16, torch.float16):
+            t = t.float()
+        return t.double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_P)
+
+
+def _iptr(a):
+    return a.ctypes.data_as(_PI)
+
+
+_default: Optional[Oracle] = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def scan(*args, **kwargs):
+    return default().scan(*args, **kwargs)
+
+
+def state_update(*args, **kwargs):
+    return default().state_update(*args, **kwargs)

@@ -1,0 +1,131 @@
+/*
+ * Selective state-space scan: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline use it. It shares no code, header or constant with the CUDA path.
+ *
+ * It evaluates the selective SSM (S6) exactly as the pages define it, one
+ * (batch, channel) row at a time, sequentially in time, in double precision,
+ * with the C library's exp/log1p, no vectorisation and no reassociation:
+ *
+ *   dt      = delta[l] (+ bias)                 -- bias of the dt projection
+ *   dt      = softplus(dt)   if softplus_flag   -- "Mamba 论文精读" (youngju.dev) §3.1,
+ *                                                  Delta_t = softplus(Linear_Delta(x_t))
+ *   dA[n]   = exp(dt * A[n])                     -- same page §2.2 (ZOH: A_bar = exp(Delta A))
+ *   dBu[n]  = dt * B[l][n] * u[l]                -- same page §3.3 simplified scan: B_bar = Delta * B
+ *   h[n]    = dA[n] * h[n] + dBu[n],  h = 0 before the first step
+ *                                                -- same page §2.2 recurrence h_t = A_bar h_{t-1} + B_bar x_t
+ *   y[l]    = sum_n C[l][n] * h[n]               -- same page §2.2, y_t = C h_t (read after the update)
+ *   y[l]   += D * u[l]        if D given         -- "Mamba的基础知识" (weblog-19d), 状态空间模型 section:
+ *                                                  the D term is a skip connection
+ *   y[l]   *= silu(z[l])      if z given         -- "Mamba 论文精读" §3.4 block: y = y * silu(z)
+ *
+ * The state update for decoding is one iteration of the same loop body applied
+ * to a given state ("mamba->jamba" (blog.csdn.net) §2.2: constant-time recurrent
+ * inference; "Mamba 论文精读" §6: O(1) per token, fixed state). Both entry points
+ * call the same step function, so L successive updates from h = 0 reproduce the
+ * scan bit for bit.
+ *
+ * softplus is written as max(x,0) + log1p(exp(-|x|)), which is the same
+ * function as log(1 + exp(x)) for every x but does not overflow for large x.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+static double softplus_ref(double x)
+{
+    double ax = x < 0.0 ? -x : x;
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-ax));
+}
+
+static double silu_ref(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* One time step of the selective SSM for one row.
+ * h[dstate] in/out; A_row[dstate]; Bt, Ct: the step's B and C, read with
+ * stride bc_stride (seqlen for the scan layout (batch, dstate, seqlen), 1 for
+ * the decode layout (batch, dstate)). Returns y for the step. */
+static double ssm_step(double* h, int64_t dstate, const double* A_row,
+                       const double* Bt, const double* Ct, int64_t bc_stride,
+                       double u, double delta, const double* zp,
+                       const double* Dp, const double* biasp, int softplus_flag)
+{
+    double dt = delta;
+    if (biasp) dt += *biasp;
+    if (softplus_flag) dt = softplus_ref(dt);
+    double y = 0.0;
+    for (int64_t n = 0; n < dstate; ++n) {
+        double dA = exp(dt * A_row[n]);
+        double dBu = dt * Bt[n * bc_stride] * u;
+        h[n] = dA * h[n] + dBu;
+        y += Ct[n * bc_stride] * h[n];
+    }
+    if (Dp) y += (*Dp) * u;
+    if (zp) y *= silu_ref(*zp);
+    return y;
+}
+
+/*
+ * Scan of nrows independent rows over seqlen steps.
+ *   u, delta, z : (nrows, seqlen)        z may be NULL
+ *   A           : (nrows, dstate)        the A row of each row's channel
+ *   Dskip, bias : (nrows)                either may be NULL
+ *   B, C        : (nbatch, dstate, seqlen), row r uses batch bidx[r]
+ *   y           : (nrows, seqlen) out
+ *   hlast       : (nrows, dstate) out, may be NULL: state after the last step
+ * Returns 0, or -1 if dstate is out of range.
+ */
+int oracle_scan(int64_t nrows, int64_t seqlen, int64_t dstate,
+                const double* u, const double* delta, const double* z,
+                const double* A, const double* Dskip, const double* bias,
+                const double* B, const double* C, const int64_t* bidx,
+                int softplus_flag, double* y, double* hlast)
+{
+    double h[1024];
+    if (dstate < 1 || dstate > 1024) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double* Bb = B + bidx[r] * dstate * seqlen;
+        const double* Cb = C + bidx[r] * dstate * seqlen;
+        for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0;
+        for (int64_t l = 0; l < seqlen; ++l) {
+            int64_t i = r * seqlen + l;
+            y[i] = ssm_step(h, dstate, A + r * dstate, Bb + l, Cb + l, seqlen,
+                            u[i], delta[i], z ? z + i : NULL,
+                            Dskip ? Dskip + r : NULL, bias ? bias + r : NULL,
+                            softplus_flag);
+        }
+        if (hlast)
+            for (int64_t n = 0; n < dstate; ++n) hlast[r * dstate + n] = h[n];
+    }
+    return 0;
+}
+
+/*
+ * Single-token state update of nrows rows.
+ *   state       : (nrows, dstate) in/out
+ *   u, delta, z : (nrows)                z may be NULL
+ *   A           : (nrows, dstate)
+ *   Dskip, bias : (nrows)                either may be NULL
+ *   B, C        : (nbatch, dstate), row r uses batch bidx[r]
+ *   y           : (nrows) out
+ */
+int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
+                        const double* u, const double* delta, const double* z,
+                        const double* A, const double* Dskip, const double* bias,
+                        const double* B, const double* C, const int64_t* bidx,
+                        int softplus_flag, double* y)
+{
+    if (dstate < 1 || dstate > 1024) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        y[r] = ssm_step(state + r * dstate, dstate, A + r * dstate,
+                        B + bidx[r] * dstate, C + bidx[r] * dstate, 1,
+                        u[r], delta[r], z ? z + r : NULL,
+                        Dskip ? Dskip + r : NULL, bias ? bias + r : NULL,
+                        softplus_flag);
+    }
+    return 0;
+}
