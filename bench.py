@@ -1,0 +1,332 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan hot path on B300.
+
+A step is one selective-scan call (the whole hot path: dt prep, discretisation,
+recurrence, contraction, skip term, gate) over one batch of the 8 x 2048-channel
+x 4096-step bf16 workload, inputs resident in HBM. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the fp64 CPU oracle (single thread, host cores) on a
+bounded sample of the same workload; it is a deliberately slow baseline.
+Under torchrun each rank runs its own independent problem (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan elems/s (B·L·D·N) & achieved HBM GB/s vs roofline, 1×B300"
+UNIT = "elem/s"
+DEFAULT_WORKLOAD = "scan_b8_d2048_l4096_bf16"
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ["selective_state_space_133_b300/csrc/scan_fwd.cuh",
+                  "selective_state_space_133_b300/csrc/common.cuh",
+                  "selective_state_space_133_b300/csrc/mamba_scan.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_fwd_traffic.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch():
+    """DRAM bytes per launch from the committed ncu capture, if the kernel is unchanged since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("kernel_hash") == kernel_hash():
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons in the background."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows), "samples": len(rows), "reasons": sorted(reasons),
+                "window": "1 s soak of the same kernel immediately before the timed region, plus the timed region"}
+
+
+def dist_setup(want_nccl: bool):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if want_nccl else "gloo")
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_rate(x, w, budget_s: float):
+    """Time the fp64 oracle (1 thread) on whole channels of the workload for ~budget_s; elem/s."""
+    import numpy as np
+    import oracle
+    orc = oracle.default()
+    n_rows = w.batch * w.dim
+    rows_done, elapsed, r0 = 0, 0.0, 0
+    probe = 4
+    while elapsed < budget_s and r0 < n_rows:
+        n = min(probe, n_rows - r0)
+        rows = np.arange(r0, r0 + n, dtype=np.int64)
+        t0 = time.perf_counter()
+        orc.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], x["softplus"],
+                 rows=rows, return_state=False)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        rows_done += n
+        r0 += n
+        probe = max(1, min(512, int(n * max(0.05, (budget_s - elapsed)) / max(dt, 1e-6))))
+    elems = rows_done * w.seqlen * 16
+    return elems / elapsed, elems, rows_done, elapsed
+
+
+def run_reference(args, w):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    from selective_state_space_133_b300 import synthetic as syn
+    x = syn.workload_inputs(w)
+    per_step_budget = float(os.environ.get("BENCH_REF_STEP_S", "2.0"))
+    for _ in range(args.warmup):
+        oracle_rate(x, w, per_step_budget / 4)
+    tot_elems, tot_time, rows = 0, 0.0, 0
+    for _ in range(args.steps):
+        _, e, r, t = oracle_rate(x, w, per_step_budget)
+        tot_elems += e
+        tot_time += t
+        rows += r
+    value = tot_elems / tot_time
+    sample = (f"each step: whole channels (all {w.seqlen} steps x 16 states) of the workload, about "
+              f"{per_step_budget:.1f} s of single-thread fp64 oracle work; {rows} channels over {args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_time / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
+                       "io_dtype": "bf16" if "bf16" in w.name else "fp32"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    from selective_state_space_133_b300 import ops
+    from selective_state_space_133_b300 import synthetic as syn
+
+    ws, rank, local = dist_setup(want_nccl=True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    # each rank: its own independent problem of the workload's shape (weak scaling)
+    x = syn.scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed + 7919 * rank, with_D=w.with_D,
+                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y = torch.empty_like(d["u"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                           d["softplus"], y=y, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ops.check_device_error(stream)
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_index = vis.split(",")[local] if vis else str(local)
+    sampler = ClockSampler(gpu_index) if rank == 0 else None
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:   # bring clocks to steady state under this kernel
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ops.check_device_error(stream)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    ms_per_step = total_ms / K
+    value = ws * w.elements * K / (total_ms * 1e-3)
+    kernel_ms = statistics.mean(launch_ms)
+
+    # e2e: pinned host inputs -> device, scan, y -> pinned host, every step
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = y_host.numel() * y_host.element_size()
+    K2 = max(3, min(K, 20))
+
+    def e2e_step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                d[k].copy_(v, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+    e2e_value = ws * w.elements * K2 / (e2e_ms * 1e-3)
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = hbm_peak()
+    achieved = w.io_bytes / (kernel_ms * 1e-3) / 1e9
+    traffic = traffic_per_launch()
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = clocks["sm_mhz"] if clocks else None
+    alu = None
+    if sm_mhz:
+        per_clk_sm = w.elements / (kernel_ms * 1e-3) / (sm_mhz * 1e6) / props.multi_processor_count
+        alu = {"bound": "alu", "achieved": per_clk_sm, "peak": 32.0, "unit": "elem/clk/SM",
+               "frac": per_clk_sm / 32.0,
+               "note": "one MUFU ex2 per element; measured ex2 rate 32/clk/SM; FP32 pipe also 4 lane-ops/element"}
+    budget = float(os.environ.get("BENCH_CPU_BASELINE_S", "10"))
+    cpu_v, cpu_e, cpu_rows, cpu_t = oracle_rate(x, w, budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
+                   "z_gate": w.with_z, "skip_D": w.with_D, "softplus_in_kernel": w.softplus_in_kernel,
+                   "state_dtype": "fp32", "parallelism": f"replicas x{ws}",
+                   "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB > 126 MB L2"},
+        "gpu_launches": K,
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": w.io_bytes, "kernel_ms": kernel_ms},
+        "alu_roofline": alu,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": K2},
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{cpu_rows} whole channels (x {w.seqlen} steps x 16 states = {cpu_e} elements) "
+                                   f"of the workload, single-thread fp64, {cpu_t:.1f} s"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    args = ap.parse_args()
+    from selective_state_space_133_b300 import synthetic as syn
+    w = syn.SCAN_WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,128 @@
+/*
+ * mamba_scan.h -- C ABI of the B300 (sm_103a) selective state-space scan library
+ * (libmambascan.so).
+ *
+ * What is computed (per batch b, channel d, state n, time l):
+ *
+ *   dt        = delta[b,d,l] + delta_bias[d]            (bias optional, 0 if NULL)
+ *   dt        = softplus(dt)            if softplus_flag  ("Mamba 论文精读", youngju.dev,
+ *                                                          §3.1: Delta_t = softplus(Linear_Delta(x_t)))
+ *   dA        = exp(dt * A[d,n])                          (same page §2.2, ZOH: A_bar = exp(Delta A))
+ *   dBu       = dt * B[b,n,l] * u[b,d,l]                   (same page §3.3 simplified scan: B_bar = Delta B)
+ *   h[n]      = dA * h[n] + dBu,  h = 0 before l = 0       (same page §2.2 recurrence; §3.3 starts h at zero)
+ *   y[b,d,l]  = sum_n C[b,n,l] * h[n]  (+ D[d] * u[b,d,l]) (§2.2 y_t = C h_t; the D skip term is the
+ *                                                          output term of "Mamba的基础知识", weblog-19d,
+ *                                                          状态空间模型 section)
+ *   y        *= silu(z[b,d,l])          if z != NULL      ("Mamba 论文精读" §3.4 block gate)
+ *
+ * "mamba->jamba" (blog.csdn.net) §2.3 states the fused-kernel requirement this
+ * library meets: only delta, A, B, C (and u, z) are read from HBM, discretisation,
+ * scan and the contraction with C happen on chip, and only y (batch, D, L) is
+ * written; no (batch, L, D, N) intermediate ever reaches device memory.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *     nothing, keeps no state between calls (apart from one device error word,
+ *     see mamba_check_device_error) and never frees anything.
+ *   - All tensors are dense, row-major, contiguous:
+ *       u, delta, z, y : (batch, dim, seqlen)
+ *       B, C           : (batch, dstate, seqlen)   -- one group, shared by all channels
+ *       A              : (dim, dstate)             fp32, expected < 0 (not checked)
+ *       D, delta_bias  : (dim)                     fp32
+ *       state          : (batch, dim, dstate)      fp32
+ *     For the state update, u/delta/z/y are (batch, dim) and B/C are (batch, dstate).
+ *   - u, delta, z, B, C and y share io_dtype (fp32 or bf16). A, D, delta_bias and
+ *     the state are always fp32; the recurrence and all accumulation are fp32.
+ *   - dstate must be 16.
+ *   - Base pointers of u, delta, z, y, B, C, A and state/final_state must be
+ *     16-byte aligned; D and delta_bias 4-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and launch on the current CUDA device.
+ *   - Every argument check happens on the host before any launch; on an error
+ *     nothing is launched and nothing is written.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAMBA_F32 = 0,
+    MAMBA_BF16 = 1
+} mamba_dtype;
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_ERR_NULL = -1,            /* a required pointer is NULL */
+    MAMBA_ERR_SHAPE = -2,           /* negative size, unsupported dstate, or a size too large */
+    MAMBA_ERR_DTYPE = -3,           /* io_dtype is not a mamba_dtype */
+    MAMBA_ERR_ALIGN = -4,           /* a base pointer violates the alignment above */
+    MAMBA_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed (launch or tensor map) */
+    MAMBA_ERR_DEVICE_TIMEOUT = -6   /* a kernel gave up waiting on its own copies (see below) */
+} mamba_status;
+
+/*
+ * Selective scan (prefill / training forward).
+ *   u, delta, z : (batch, dim, seqlen) io_dtype; z may be NULL (no gate)
+ *   A           : (dim, dstate) fp32
+ *   B, C        : (batch, dstate, seqlen) io_dtype
+ *   D           : (dim) fp32 or NULL (no skip term)
+ *   delta_bias  : (dim) fp32 or NULL (zero bias)
+ *   softplus_flag : nonzero -> dt = softplus(delta + bias), else dt = delta + bias
+ *   y           : (batch, dim, seqlen) io_dtype, written (bf16 by round-to-nearest-even)
+ *   final_state : (batch, dim, dstate) fp32 or NULL; receives h after the last step
+ *                 (zeros when seqlen == 0)
+ * Any of batch, dim, seqlen may be 0 (nothing to compute; final_state, if given,
+ * is zero-filled). When seqlen == 0, u, delta, B, C, z and y may be NULL (an
+ * empty tensor's data pointer). y must not alias an input.
+ * Returns MAMBA_OK or a negative mamba_status.
+ */
+int mamba_scan_fwd(const void* u, const void* delta, const float* A,
+                   const void* B, const void* C,
+                   const float* D, const void* z,
+                   const float* delta_bias, int softplus_flag,
+                   void* y, float* final_state,
+                   int batch, int dim, int seqlen, int dstate,
+                   int io_dtype, void* stream);
+
+/*
+ * Single-token recurrent state update (decode): one step of the recurrence above
+ * applied in place to `state` ("mamba->jamba" §2.2: constant-time recurrent
+ * inference; "Mamba 论文精读" §6: O(1) work and a fixed-size state per token).
+ *   state       : (batch, dim, dstate) fp32, read and overwritten
+ *   u, delta, z : (batch, dim) io_dtype; z may be NULL
+ *   A           : (dim, dstate) fp32
+ *   B, C        : (batch, dstate) io_dtype
+ *   D           : (dim) fp32 or NULL;  delta_bias : (dim) fp32 or NULL
+ *   y           : (batch, dim) io_dtype, written
+ * Returns MAMBA_OK or a negative mamba_status.
+ */
+int mamba_state_update(float* state, const void* u, const void* delta, const float* A,
+                       const void* B, const void* C,
+                       const float* D, const void* z,
+                       const float* delta_bias, int softplus_flag,
+                       void* y, int batch, int dim, int dstate,
+                       int io_dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error word.
+ * Kernels that wait on their own asynchronous copies give up after a bounded
+ * number of polls (far beyond any normal copy time), set this word and return
+ * early instead of hanging. Returns MAMBA_OK, MAMBA_ERR_DEVICE_TIMEOUT, or
+ * MAMBA_ERR_CUDA if the synchronisation itself failed.
+ */
+int mamba_check_device_error(void* stream);
+
+/* Human-readable name of a mamba_status value (static string, never NULL). */
+const char* mamba_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int mamba_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SCAN_H */

@@ -72,15 +72,14 @@ class Oracle:
         Returns y of shape (len(rows), L) and, if asked, the final state
         (len(rows), N), both float64.
         """
-        u = _f64(u)
         batch, dim, L = u.shape
         N = _f64(A).shape[1]
         rows = np.arange(batch * dim, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
         b_idx = np.ascontiguousarray(rows // dim)
         d_idx = rows % dim
-        ur = np.ascontiguousarray(u.reshape(batch * dim, L)[rows])
-        dr = np.ascontiguousarray(_f64(delta).reshape(batch * dim, L)[rows])
-        zr = None if z is None else np.ascontiguousarray(_f64(z).reshape(batch * dim, L)[rows])
+        ur = _gather_rows(u, rows, batch * dim, L)
+        dr = _gather_rows(delta, rows, batch * dim, L)
+        zr = None if z is None else _gather_rows(z, rows, batch * dim, L)
         Ar = np.ascontiguousarray(_f64(A)[d_idx])
         Dr = None if D is None else np.ascontiguousarray(_f64(D)[d_idx])
         br = None if delta_bias is None else np.ascontiguousarray(_f64(delta_bias)[d_idx])
@@ -98,20 +97,25 @@ class Oracle:
 
     # -- state update ---------------------------------------------------------
     def state_update(self, state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     softplus=False, rows=None):
+                     softplus=False, rows=None, compact_state=False):
         """One decode step of the rows ``rows`` (flat b*dim + d; all rows if None).
 
-        state : (batch, dim, N);  u, delta, z : (batch, dim);  B, C : (batch, N);
-        A : (dim, N); D, delta_bias : (dim,).
+        state : (batch, dim, N), or (len(rows), N) with compact_state=True;
+        u, delta, z : (batch, dim);  B, C : (batch, N);  A : (dim, N);
+        D, delta_bias : (dim,).
         Returns (y (len(rows),), new_state (len(rows), N)), float64; the input
         state is not modified.
         """
-        s = _f64(state)
-        batch, dim, N = s.shape
+        batch, dim = u.shape
+        N = _f64(A).shape[1]
         rows = np.arange(batch * dim, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
         b_idx = np.ascontiguousarray(rows // dim)
         d_idx = rows % dim
-        sr = np.ascontiguousarray(s.reshape(batch * dim, N)[rows]).copy()
+        s = _f64(state)
+        if compact_state:
+            sr = np.ascontiguousarray(s.reshape(len(rows), N)).copy()
+        else:
+            sr = np.ascontiguousarray(s.reshape(batch * dim, N)[rows]).copy()
         ur = np.ascontiguousarray(_f64(u).reshape(batch * dim)[rows])
         dr = np.ascontiguousarray(_f64(delta).reshape(batch * dim)[rows])
         zr = None if z is None else np.ascontiguousarray(_f64(z).reshape(batch * dim)[rows])
@@ -141,6 +145,15 @@ def _f64(x):
             t = t.float()
         return t.double().numpy()
     return np.asarray(x, dtype=np.float64)
+
+
+def _gather_rows(x, rows, n_rows, L):
+    """Rows ``rows`` of x viewed as (n_rows, L), widened exactly to float64 (gather first, then widen)."""
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach().reshape(n_rows, L)[torch.as_tensor(rows, device=x.device)]
+        return np.ascontiguousarray(_f64(t))
+    return np.ascontiguousarray(np.asarray(x).reshape(n_rows, L)[rows], dtype=np.float64)
 
 
 def _ptr(a):

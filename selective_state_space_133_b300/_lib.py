@@ -1,0 +1,55 @@
+"""ctypes handle on libmambascan.so (the C ABI in include/mamba_scan.h).
+
+There is no fallback: if the library is missing the import of an op raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIBRARY
+
+MAMBA_F32 = 0
+MAMBA_BF16 = 1
+STATUS = {0: "MAMBA_OK", -1: "MAMBA_ERR_NULL", -2: "MAMBA_ERR_SHAPE", -3: "MAMBA_ERR_DTYPE",
+          -4: "MAMBA_ERR_ALIGN", -5: "MAMBA_ERR_CUDA", -6: "MAMBA_ERR_DEVICE_TIMEOUT"}
+
+# (name, restype, argtypes) of every symbol the header declares.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "mamba_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "mamba_state_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
+    "mamba_check_device_error": (_I, [_P]),
+    "mamba_status_string": (ctypes.c_char_p, [_I]),
+    "mamba_version": (_I, []),
+}
+
+_lib = None
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(f"{LIBRARY} is missing: build it with "
+                               "selective_state_space_133_b300.build.build_library()")
+        handle = ctypes.CDLL(LIBRARY)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def check(status: int, where: str) -> None:
+    if status != 0:
+        raise MambaError(status, where)

@@ -1,0 +1,48 @@
+"""Runs N launches of the scan (or of the decode step) on a named workload and exits.
+
+A plain driver for profilers: inputs are generated, moved to the GPU once,
+and the op is launched ``--launches`` times back to back, nothing else.
+
+    python -m selective_state_space_133_b300.launch --workload scan_b8_d2048_l4096_bf16 --launches 3
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import ops
+from . import synthetic as syn
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="scan_b8_d2048_l4096_bf16")
+    ap.add_argument("--launches", type=int, default=3)
+    args = ap.parse_args()
+    dev = torch.device("cuda", 0)
+    if args.workload in syn.SCAN_WORKLOADS:
+        w = syn.SCAN_WORKLOADS[args.workload]
+        x = syn.workload_inputs(w)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+        y = torch.empty_like(d["u"])
+        fs = torch.empty(w.batch, w.dim, syn.DSTATE, device=dev) if w.final_state else None
+        for _ in range(args.launches):
+            ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                               d["softplus"], y=y, final_state=fs)
+    else:
+        w = syn.DECODE_WORKLOADS[args.workload]
+        st = {k: v.to(dev) for k, v in syn.decode_static(w).items()}
+        x = {k: v.to(dev) for k, v in syn.decode_step(w, 0).items()}
+        y = torch.empty_like(x["u"])
+        for _ in range(args.launches):
+            ops.mamba_state_update(st["state"], x["u"], x["delta"], st["A"], x["B"], x["C"], st["D"], x["z"],
+                                   st["delta_bias"], True, y=y)
+    ops.check_device_error()
+    torch.cuda.synchronize()
+    print(f"{args.launches} launches of {args.workload}: ok")
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

@@ -1,0 +1,123 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every step of the scan and of the state update runs in the CUDA kernels of
+libmambascan.so; these wrappers only check that the torch tensors they are
+given are dense CUDA tensors of the right dtype, allocate outputs the caller
+did not supply (device memory through torch), and pass raw pointers and sizes
+to the library on the given (or current) stream. Nothing here copies,
+converts or computes on tensor data.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+_IO = {torch.float32: _lib.MAMBA_F32, torch.bfloat16: _lib.MAMBA_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, dtype, shape, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+                   y=None, final_state=None, stream=None):
+    """Selective scan (see include/mamba_scan.h, mamba_scan_fwd).
+
+    u, delta, z: (batch, dim, L); B, C: (batch, 16, L), all fp32 or all bf16;
+    A: (dim, 16) fp32; D, delta_bias: (dim,) fp32. ``final_state`` may be a
+    preallocated (batch, dim, 16) fp32 tensor, or True to allocate one.
+    Returns y, or (y, final_state) when a final state was requested.
+    """
+    if u.dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {u.dtype}")
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_scan_fwd runs on CUDA tensors only")
+    batch, dim, L = u.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    _need(u, "u", u.dtype, (batch, dim, L), dev)
+    _need(delta, "delta", u.dtype, (batch, dim, L), dev)
+    _need(z, "z", u.dtype, (batch, dim, L), dev)
+    _need(B, "B", u.dtype, (batch, N, L), dev)
+    _need(C, "C", u.dtype, (batch, N, L), dev)
+    _need(A, "A", torch.float32, (dim, N), dev)
+    _need(D, "D", torch.float32, (dim,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (dim,), dev)
+    if y is None:
+        y = torch.empty_like(u)
+    _need(y, "y", u.dtype, (batch, dim, L), dev)
+    want_state = final_state is not None and final_state is not False
+    if final_state is True:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    st = _lib.lib().mamba_scan_fwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(y), _ptr(final_state), batch, dim, L, N, _IO[u.dtype],
+        _stream_handle(stream, dev))
+    _lib.check(st, "mamba_scan_fwd")
+    return (y, final_state) if want_state else y
+
+
+def mamba_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                       softplus=False, y=None, stream=None):
+    """One decode step in place on ``state`` (see include/mamba_scan.h, mamba_state_update).
+
+    state: (batch, dim, 16) fp32; u, delta, z: (batch, dim); B, C: (batch, 16),
+    all fp32 or all bf16; A: (dim, 16) fp32; D, delta_bias: (dim,) fp32.
+    Returns y (batch, dim).
+    """
+    if u.dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {u.dtype}")
+    dev = state.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_state_update runs on CUDA tensors only")
+    batch, dim, N = state.shape
+    _need(state, "state", torch.float32, (batch, dim, N), dev)
+    for name, t in (("u", u), ("delta", delta), ("z", z)):
+        _need(t, name, u.dtype, (batch, dim), dev)
+    _need(B, "B", u.dtype, (batch, N), dev)
+    _need(C, "C", u.dtype, (batch, N), dev)
+    _need(A, "A", torch.float32, (dim, N), dev)
+    _need(D, "D", torch.float32, (dim,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (dim,), dev)
+    if y is None:
+        y = torch.empty_like(u)
+    _need(y, "y", u.dtype, (batch, dim), dev)
+    st = _lib.lib().mamba_state_update(
+        _ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(softplus)), _ptr(y), batch, dim, N, _IO[u.dtype],
+        _stream_handle(stream, dev))
+    _lib.check(st, "mamba_state_update")
+    return y
+
+
+def check_device_error(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a bounded-wait timeout."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _lib.check(_lib.lib().mamba_check_device_error(_stream_handle(stream, dev)),
+               "mamba_check_device_error")

@@ -1,0 +1,99 @@
+"""The C-ABI library on the host: it loads, exports what the header declares, and
+rejects bad arguments before touching the GPU (no compute call is made here)."""
+import os
+import re
+
+import pytest
+
+from selective_state_space_133_b300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mamba_scan.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build_library()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_api():
+    assert declared_functions() == sorted(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(0, -7, -1):
+        s = L.mamba_status_string(code).decode()
+        assert s.startswith(_lib.STATUS[code])
+    assert L.mamba_status_string(42).decode() == "unknown mamba_status"
+    assert L.mamba_version() == 100
+
+
+# Fake, never-dereferenced addresses: validation fails before any CUDA call.
+P = 0x10000  # 16-byte aligned
+
+
+def scan(L, **kw):
+    args = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, sp=1, y=P, fs=None,
+                batch=2, dim=32, seqlen=64, dstate=16, dtype=0, stream=None)
+    args.update(kw)
+    return L.mamba_scan_fwd(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["z"],
+                            args["bias"], args["sp"], args["y"], args["fs"], args["batch"], args["dim"],
+                            args["seqlen"], args["dstate"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), -3), (dict(dtype=-1), -3),
+    (dict(dstate=8), -2), (dict(dstate=32), -2), (dict(batch=-1), -2), (dict(dim=-5), -2),
+    (dict(seqlen=-1), -2), (dict(batch=70000), -2),
+    (dict(dim=1 << 20, seqlen=1 << 20), -2),
+    (dict(u=None), -1), (dict(delta=None), -1), (dict(A=None), -1), (dict(B=None), -1),
+    (dict(C=None), -1), (dict(y=None), -1),
+    (dict(u=P + 8), -4), (dict(y=P + 4), -4), (dict(B=P + 2), -4), (dict(z=P + 8), -4),
+    (dict(fs=P + 4), -4), (dict(A=P + 4), -4), (dict(D=P + 2), -4), (dict(bias=P + 1), -4),
+])
+def test_scan_rejects(L, kw, code):
+    assert scan(L, **kw) == code
+
+
+def test_scan_empty_length_allows_null_io(L):
+    # seqlen == 0 with a null A is still rejected before any launch
+    assert scan(L, seqlen=0, u=None, delta=None, B=None, C=None, y=None, A=None) == -1
+
+
+def test_scan_empty_is_noop(L):
+    # batch or dim of 0: nothing to do, nothing launched, even with null pointers
+    assert scan(L, batch=0, u=None, y=None) == 0
+    assert scan(L, dim=0, u=None, y=None) == 0
+
+
+def update(L, **kw):
+    args = dict(state=P, u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, sp=1, y=P,
+                batch=4, dim=8, dstate=16, dtype=1, stream=None)
+    args.update(kw)
+    return L.mamba_state_update(args["state"], args["u"], args["delta"], args["A"], args["B"], args["C"],
+                                args["D"], args["z"], args["bias"], args["sp"], args["y"], args["batch"],
+                                args["dim"], args["dstate"], args["dtype"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), -3), (dict(dstate=4), -2), (dict(batch=-2), -2),
+    (dict(state=None), -1), (dict(u=None), -1), (dict(y=None), -1), (dict(A=None), -1),
+    (dict(state=P + 4), -4), (dict(A=P + 8), -4), (dict(B=P + 2), -4), (dict(u=P + 1), -4),
+])
+def test_update_rejects(L, kw, code):
+    assert update(L, **kw) == code
+
+
+def test_update_empty_is_noop(L):
+    assert update(L, batch=0, state=None) == 0
