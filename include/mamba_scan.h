@@ -21,9 +21,11 @@
  * written; no (batch, L, D, N) intermediate ever reaches device memory.
  *
  * Conventions shared by every entry point
- *   - Pointers are DEVICE pointers owned by the caller; the library allocates
- *     nothing, keeps no state between calls (apart from one device error word,
- *     see mamba_check_device_error) and never frees anything.
+ *   - Pointers are DEVICE pointers owned by the caller. The library keeps no
+ *     state between calls (apart from one device error word, see
+ *     mamba_check_device_error). Only mamba_scan_fwd allocates: a stream-ordered
+ *     workspace (cudaMallocAsync / cudaFreeAsync on `stream`); callers that
+ *     manage memory themselves pass the workspace to mamba_scan_fwd_ws.
  *   - All tensors are dense, row-major, contiguous:
  *       u, delta, z, y : (batch, dim, seqlen)
  *       B, C           : (batch, dstate, seqlen)   -- one group, shared by all channels
@@ -44,6 +46,8 @@
 #ifndef MAMBA_SCAN_H
 #define MAMBA_SCAN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -60,7 +64,8 @@ typedef enum {
     MAMBA_ERR_DTYPE = -3,           /* io_dtype is not a mamba_dtype */
     MAMBA_ERR_ALIGN = -4,           /* a base pointer violates the alignment above */
     MAMBA_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed (launch or tensor map) */
-    MAMBA_ERR_DEVICE_TIMEOUT = -6   /* a kernel gave up waiting on its own copies (see below) */
+    MAMBA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up waiting on its own copies (see below) */
+    MAMBA_ERR_WORKSPACE = -7        /* workspace_bytes < mamba_scan_workspace_size(...) */
 } mamba_status;
 
 /*
@@ -77,6 +82,9 @@ typedef enum {
  * Any of batch, dim, seqlen may be 0 (nothing to compute; final_state, if given,
  * is zero-filled). When seqlen == 0, u, delta, B, C, z and y may be NULL (an
  * empty tensor's data pointer). y must not alias an input.
+ * The call launches one small kernel that packs B and C into a device workspace
+ * (fp32, one 128-byte row of B then C per step) and then the scan kernel; the
+ * workspace is allocated and freed stream-ordered on `stream`.
  * Returns MAMBA_OK or a negative mamba_status.
  */
 int mamba_scan_fwd(const void* u, const void* delta, const float* A,
@@ -86,6 +94,35 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A,
                    void* y, float* final_state,
                    int batch, int dim, int seqlen, int dstate,
                    int io_dtype, void* stream);
+
+/*
+ * Bytes of device workspace mamba_scan_fwd_ws needs for these sizes (0 when
+ * there is nothing to compute or an argument is out of range): the packed
+ * fp32 B/C rows, batch * roundup(seqlen, 16) * 128 bytes, plus, only when
+ * seqlen * sizeof(io type) is not a multiple of 16 bytes, copies of u, delta
+ * and z at a row pitch that is.
+ */
+size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype);
+
+/*
+ * mamba_scan_fwd with a caller-provided workspace: same arguments, semantics
+ * and checks, plus
+ *   workspace       : device buffer, 256-byte aligned, owned by the caller, of
+ *                     at least mamba_scan_workspace_size(...) bytes (may be NULL
+ *                     when that size is 0); its contents are scratch, needed
+ *                     only until the call's kernels on `stream` have finished
+ *   workspace_bytes : its size
+ * Allocates nothing. Returns MAMBA_ERR_WORKSPACE if the buffer is too small,
+ * MAMBA_ERR_NULL if it is NULL while needed, MAMBA_ERR_ALIGN if misaligned.
+ */
+int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
+                      const void* B, const void* C,
+                      const float* D, const void* z,
+                      const float* delta_bias, int softplus_flag,
+                      void* y, float* final_state,
+                      int batch, int dim, int seqlen, int dstate,
+                      int io_dtype, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /*
  * Single-token recurrent state update (decode): one step of the recurrence above

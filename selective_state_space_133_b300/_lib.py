@@ -12,13 +12,17 @@ from .build import LIBRARY
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
 STATUS = {0: "MAMBA_OK", -1: "MAMBA_ERR_NULL", -2: "MAMBA_ERR_SHAPE", -3: "MAMBA_ERR_DTYPE",
-          -4: "MAMBA_ERR_ALIGN", -5: "MAMBA_ERR_CUDA", -6: "MAMBA_ERR_DEVICE_TIMEOUT"}
+          -4: "MAMBA_ERR_ALIGN", -5: "MAMBA_ERR_CUDA", -6: "MAMBA_ERR_DEVICE_TIMEOUT",
+          -7: "MAMBA_ERR_WORKSPACE"}
 
 # (name, restype, argtypes) of every symbol the header declares.
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+_Z = ctypes.c_size_t
 SIGNATURES = {
     "mamba_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "mamba_scan_fwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "mamba_scan_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mamba_state_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
     "mamba_check_device_error": (_I, [_P]),
     "mamba_status_string": (ctypes.c_char_p, [_I]),

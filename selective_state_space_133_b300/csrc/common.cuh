@@ -49,6 +49,19 @@ __device__ __forceinline__ float log1p_unit(float v) {
     return v * q;
 }
 
+// q(v) of log1p_unit for two values at once, on the packed FP32 pipe.
+__device__ __forceinline__ float2 log1p_unit_q2(float2 v) {
+    float2 q = make_float2(-0.008574675768613815f, -0.008574675768613815f);
+    q = __ffma2_rn(q, v, make_float2(0.044214192777872086f, 0.044214192777872086f));
+    q = __ffma2_rn(q, v, make_float2(-0.10785368084907532f, -0.10785368084907532f));
+    q = __ffma2_rn(q, v, make_float2(0.17757023870944977f, 0.17757023870944977f));
+    q = __ffma2_rn(q, v, make_float2(-0.2449961155653f, -0.2449961155653f));
+    q = __ffma2_rn(q, v, make_float2(0.3327617645263672f, 0.3327617645263672f));
+    q = __ffma2_rn(q, v, make_float2(-0.49997448921203613f, -0.49997448921203613f));
+    q = __ffma2_rn(q, v, make_float2(0.9999998211860657f, 0.9999998211860657f));
+    return q;
+}
+
 // softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^{-|x|}); accurate in relative
 // terms for small results (x << 0), where log2-based forms are not.
 __device__ __forceinline__ float softplus_f(float x) {
@@ -104,6 +117,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Plain arrival (count 1) on `bar`, release semantics at CTA scope.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -116,6 +134,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed may
+// sleep (up to `ns` nanoseconds) until it does, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -124,12 +156,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Waits for phase `parity` of `bar` to complete. Gives up after about one second
 // of wall time (a TMA load normally lands in microseconds) and returns false.
+// The common case, a phase that completes within the first sleep, costs one
+// try_wait and no timer read.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     const uint64_t start = global_timer_ns();
     for (uint32_t i = 1; i < (1u << 30); ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && global_timer_ns() - start > 1000000000ull) return false;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (global_timer_ns() - start > 1000000000ull) return false;
     }
     return false;
 }

@@ -2,7 +2,9 @@
 //
 // Declared in include/mamba_scan.h. Every check runs on the host before any
 // launch; a rejected call launches nothing and writes nothing. The library
-// allocates no device memory and keeps no state besides the device error word.
+// keeps no state besides the device error word; mamba_scan_fwd allocates its
+// workspace stream-ordered, mamba_scan_fwd_ws takes it from the caller.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -13,14 +15,6 @@
 namespace {
 
 using mscan::kDState;
-
-constexpr int kRows = 16;    // channels per CTA (one warp, two lanes per channel)
-constexpr int kTL = 16;      // steps per chunk
-
-// TMA ring depth: two chunks of look-ahead on top of the three chunks a CTA
-// works on (bf16: 27 KB of shared memory per CTA, 7 CTAs per SM).
-template <typename T> constexpr int kStages = 5;
-template <> constexpr int kStages<float> = 4;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -42,13 +36,16 @@ EncodeTiledFn get_encode_fn() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// 3-D map over a (d2, d1, d0) row-major tensor (d0 innermost) with box (b0, b1, 1).
-bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t d0, uint64_t d1,
-                 uint64_t d2, uint32_t b0, uint32_t b1) {
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 3-D map over a tensor with extents (e0, e1, e2), e0 innermost, row pitch
+// `pitch0` elements (>= e0) and plane pitch pitch0 * e1; box (b0, b1, 1).
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0, uint64_t e1,
+                 uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+    const cuuint64_t dims[3] = {e0, e1, e2};
+    const cuuint64_t strides[2] = {pitch0 * es, pitch0 * e1 * es};
     const cuuint32_t box[3] = {b0, b1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -56,31 +53,77 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Workspace of one scan call: the packed fp32 B/C rows and, when a row of
+// u/delta/z is not a whole number of 16-byte units (TMA strides must be), copies
+// of those tensors at a padded row pitch.
+struct ScanWorkspace {
+    int Lp;          // sequence length rounded up to whole chunks (rows of the B/C buffer)
+    int pitch;       // row pitch (elements) the tensor maps of u/delta/z use
+    bool copy_rows;  // u/delta/z are copied to `pitch` first
+    size_t bc, u, dl, z, total;  // byte offsets of the parts, and the total
+};
+
+ScanWorkspace scan_workspace(long long batch, long long dim, long long L, size_t es) {
+    ScanWorkspace w;
+    w.Lp = static_cast<int>(round_up(static_cast<size_t>(L), mscan::kTL));
+    w.copy_rows = (static_cast<size_t>(L) * es) % 16 != 0;
+    w.pitch = w.copy_rows ? static_cast<int>(round_up(static_cast<size_t>(L), 16 / es)) : static_cast<int>(L);
+    w.bc = 0;
+    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * mscan::kBCW * sizeof(float), 256);
+    const size_t rows = w.copy_rows ? round_up(static_cast<size_t>(batch) * dim * w.pitch * es, 256) : 0;
+    w.u = off; off += rows;
+    w.dl = off; off += rows;
+    w.z = off; off += rows;
+    w.total = L > 0 ? off : 0;
+    return w;
+}
+
 template <typename T>
-int launch_scan(const mscan::ScanArgs& a, cudaStream_t stream) {
+int launch_scan(const mscan::ScanArgs& a, const void* u, const void* delta, const void* z, const void* B,
+                const void* C, int softplus, char* ws, cudaStream_t stream) {
     constexpr size_t es = sizeof(T);
-    CUtensorMap tm_u, tm_dl, tm_z, tm_B, tm_C;
-    memset(&tm_u, 0, sizeof(tm_u)); memset(&tm_dl, 0, sizeof(tm_dl)); memset(&tm_z, 0, sizeof(tm_z));
-    memset(&tm_B, 0, sizeof(tm_B)); memset(&tm_C, 0, sizeof(tm_C));
-    mscan::ScanArgs args = a;
-    args.use_tma = (static_cast<uint64_t>(a.seqlen) * es) % 16 == 0 && a.seqlen > 0;
-    if (args.use_tma) {
+    const ScanWorkspace w = scan_workspace(a.batch, a.dim, a.seqlen, es);
+    CUtensorMap tm_u, tm_dl, tm_z, tm_bc;
+    memset(&tm_u, 0, sizeof(tm_u)); memset(&tm_dl, 0, sizeof(tm_dl));
+    memset(&tm_z, 0, sizeof(tm_z)); memset(&tm_bc, 0, sizeof(tm_bc));
+    if (a.seqlen > 0) {
+        float* bc = reinterpret_cast<float*>(ws + w.bc);
+        const long long pack_threads = static_cast<long long>(a.batch) * w.Lp;
+        mscan::bc_pack_kernel<T><<<static_cast<unsigned>((pack_threads + 255) / 256), 256, 0, stream>>>(
+            static_cast<const T*>(B), static_cast<const T*>(C), bc, a.batch, a.seqlen, w.Lp);
+        if (w.copy_rows) {
+            const long long rows = static_cast<long long>(a.batch) * a.dim;
+            const unsigned blocks = static_cast<unsigned>(
+                std::min<long long>((rows * a.seqlen + 255) / 256, 148ll * 16));
+            const void* src[3] = {u, delta, z};
+            const size_t dst[3] = {w.u, w.dl, w.z};
+            for (int i = 0; i < 3; ++i) {
+                if (!src[i]) continue;
+                mscan::row_pitch_kernel<T><<<blocks, 256, 0, stream>>>(static_cast<const T*>(src[i]),
+                                                                     reinterpret_cast<T*>(ws + dst[i]), rows,
+                                                                     a.seqlen, w.pitch);
+            }
+            u = ws + w.u;
+            delta = ws + w.dl;
+            if (z) z = ws + w.z;
+        }
         const auto ty = mscan::Io<T>::kTmaType;
-        bool ok = make_map_3d(&tm_u, ty, es, a.u, a.seqlen, a.dim, a.batch, kTL, kRows) &&
-                  make_map_3d(&tm_dl, ty, es, a.delta, a.seqlen, a.dim, a.batch, kTL, kRows) &&
-                  make_map_3d(&tm_B, ty, es, a.B, a.seqlen, kDState, a.batch, kTL, kDState) &&
-                  make_map_3d(&tm_C, ty, es, a.C, a.seqlen, kDState, a.batch, kTL, kDState);
-        if (ok && a.z) ok = make_map_3d(&tm_z, ty, es, a.z, a.seqlen, a.dim, a.batch, kTL, kRows);
+        const uint32_t bl = mscan::kTL, bd = mscan::kCtaCh;
+        bool ok = make_map_3d(&tm_u, ty, es, u, a.seqlen, a.dim, a.batch, w.pitch, bl, bd) &&
+                  make_map_3d(&tm_dl, ty, es, delta, a.seqlen, a.dim, a.batch, w.pitch, bl, bd) &&
+                  make_map_3d(&tm_bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), bc, mscan::kBCW, w.Lp,
+                              a.batch, mscan::kBCW, mscan::kBCW, bl);
+        if (ok && z) ok = make_map_3d(&tm_z, ty, es, z, a.seqlen, a.dim, a.batch, w.pitch, bl, bd);
         if (!ok) return MAMBA_ERR_CUDA;
     }
-    const dim3 grid((a.dim + kRows - 1) / kRows, a.batch);
-    constexpr int S = kStages<T>;
-    if (a.softplus) {
-        if (a.z) mscan::scan_fwd_kernel<T, kRows, kTL, S, true, true><<<grid, 32, 0, stream>>>(args, tm_u, tm_dl, tm_z, tm_B, tm_C);
-        else     mscan::scan_fwd_kernel<T, kRows, kTL, S, true, false><<<grid, 32, 0, stream>>>(args, tm_u, tm_dl, tm_z, tm_B, tm_C);
+    const dim3 grid((a.dim + mscan::kCtaCh - 1) / mscan::kCtaCh, a.batch);
+    const int threads = mscan::kScanThreads;
+    if (softplus) {
+        if (z) mscan::scan_fwd_kernel<T, true, true><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
+        else   mscan::scan_fwd_kernel<T, true, false><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
     } else {
-        if (a.z) mscan::scan_fwd_kernel<T, kRows, kTL, S, false, true><<<grid, 32, 0, stream>>>(args, tm_u, tm_dl, tm_z, tm_B, tm_C);
-        else     mscan::scan_fwd_kernel<T, kRows, kTL, S, false, false><<<grid, 32, 0, stream>>>(args, tm_u, tm_dl, tm_z, tm_B, tm_C);
+        if (z) mscan::scan_fwd_kernel<T, false, true><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
+        else   mscan::scan_fwd_kernel<T, false, false><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
@@ -100,9 +143,10 @@ size_t dtype_size(int io_dtype) { return io_dtype == MAMBA_BF16 ? 2 : 4; }
 
 extern "C" {
 
-int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-                   const void* z, const float* delta_bias, int softplus_flag, void* y, float* final_state,
-                   int batch, int dim, int seqlen, int dstate, int io_dtype, void* stream) {
+// Argument checks shared by the scan entry points (MAMBA_OK or the error code).
+static int check_scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* delta_bias, const void* y,
+                           const float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate != kDState) return MAMBA_ERR_SHAPE;
     if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
@@ -110,7 +154,9 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void*
     // every flat index must fit in 63 bits of bytes, and TMA strides in 40 bits
     const unsigned long long elems = static_cast<unsigned long long>(batch) * dim * seqlen;
     if (dim > 0 && seqlen > 0 && elems / dim / seqlen != static_cast<unsigned long long>(batch)) return MAMBA_ERR_SHAPE;
-    if (static_cast<unsigned long long>(seqlen) * dim * es >= (1ull << 40)) return MAMBA_ERR_SHAPE;
+    if ((static_cast<unsigned long long>(seqlen) + 16) * dim * es >= (1ull << 40)) return MAMBA_ERR_SHAPE;
+    if ((static_cast<unsigned long long>(seqlen) + 16) * mscan::kBCW * sizeof(float) >= (1ull << 40))
+        return MAMBA_ERR_SHAPE;
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!A) return MAMBA_ERR_NULL;
     if (seqlen > 0 && (!u || !delta || !B || !C || !y)) return MAMBA_ERR_NULL;
@@ -118,13 +164,59 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void*
     for (const void* p : p16)
         if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
     if ((D && !aligned(D, 4)) || (delta_bias && !aligned(delta_bias, 4))) return MAMBA_ERR_ALIGN;
+    return MAMBA_OK;
+}
 
+static int scan_with_workspace(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                               const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
+                               float* final_state, int batch, int dim, int seqlen, int io_dtype, void* workspace,
+                               cudaStream_t s) {
     mscan::ScanArgs a;
-    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C; a.A = A; a.D = D; a.bias = delta_bias;
-    a.y = y; a.final_state = final_state;
-    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = softplus_flag != 0; a.use_tma = 0;
+    a.A = A; a.D = D; a.bias = delta_bias; a.y = y; a.final_state = final_state;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen;
+    char* ws = static_cast<char*>(workspace);
+    const int sp = softplus_flag != 0;
+    return io_dtype == MAMBA_BF16 ? launch_scan<__nv_bfloat16>(a, u, delta, z, B, C, sp, ws, s)
+                                  : launch_scan<float>(a, u, delta, z, B, C, sp, ws, s);
+}
+
+size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype) {
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate != kDState) return 0;
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return 0;
+    return scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+}
+
+int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                      const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
+                      float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+                             io_dtype);
+    if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
+    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    if (need > 0) {
+        if (!workspace) return MAMBA_ERR_NULL;
+        if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
+    }
+    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
+                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                   const void* z, const float* delta_bias, int softplus_flag, void* y, float* final_state,
+                   int batch, int dim, int seqlen, int dstate, int io_dtype, void* stream) {
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+                             io_dtype);
+    if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return io_dtype == MAMBA_BF16 ? launch_scan<__nv_bfloat16>(a, s) : launch_scan<float>(a, s);
+    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    void* ws = nullptr;
+    if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return MAMBA_ERR_CUDA;
+    st = scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
+                             seqlen, io_dtype, ws, s);
+    if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == MAMBA_OK) st = MAMBA_ERR_CUDA;
+    return st;
 }
 
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A, const void* B, const void* C,
@@ -175,10 +267,11 @@ const char* mamba_status_string(int status) {
         case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a base pointer is not aligned as required";
         case MAMBA_ERR_CUDA: return "MAMBA_ERR_CUDA: a CUDA call failed";
         case MAMBA_ERR_DEVICE_TIMEOUT: return "MAMBA_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
+        case MAMBA_ERR_WORKSPACE: return "MAMBA_ERR_WORKSPACE: the workspace is smaller than mamba_scan_workspace_size";
         default: return "unknown mamba_status";
     }
 }
 
-int mamba_version(void) { return 100; }
+int mamba_version(void) { return 200; }
 
 }  // extern "C"

@@ -11,105 +11,91 @@
 // §2.3: discretise, scan and contract on chip; HBM traffic O(BLD + BLN)).
 //
 // Design (B300-first, not the pages' kernel):
-//  * The path is bound by the SM's issue slots, the FP32 pipe and the MUFU exp
-//    (one exp per (b,l,d,n) element), not by HBM. Each thread therefore walks
-//    the WHOLE sequence for its rows sequentially: no warp-level scan, no carry
-//    fix-ups; the recurrence costs 4 FP32 lane-ops + 1 exp per element, issued
-//    as packed FFMA2/FMUL2 on pairs of states.
-//  * CTA = one warp = ROWS channels of one batch, two lanes per channel, each
-//    lane holding 8 of the 16 states. One-warp CTAs keep the grid balanced over
-//    148 SMs (7 resident per SM).
-//  * The sequence is cut into TL-step chunks. Lane 0 issues 3-D TMA loads of a
-//    chunk's u/delta/z (ROWS x TL) and B/C (16 x TL) tiles into a STAGES-deep
-//    ring (one mbarrier per slot, bounded waits).
-//  * Per chunk there are three phases: the pre-pass (dt and dt*u once per
-//    (row, step); B/C transposed into per-step fp32 pairs), the recurrence, and
-//    the epilogue (two half-state partial sums + D*u, times silu(z), stored as
-//    16-byte vectors). They are software-pipelined: iteration c runs the
-//    recurrence of chunk c, the pre-pass of chunk c+1 and the epilogue of chunk
-//    c-1 as one straight-line block, so the three independent instruction
-//    streams hide each other's latencies inside a single warp.
-//  * The last chunk's recurrence runs only its valid steps; padding steps are
-//    never applied, so the final state needs no masking.
+//  * At N = 16 the path is bound by the SM, not by HBM: every (b,l,d,n)
+//    element costs one MUFU ex2 and four FP32 operations (dt*A, dt*u*B, the
+//    recurrence FMA, the C.h FMA), B300 retires about 32 ex2 and 128 FP32
+//    lane-operations per clock per SM, and every element also needs its B and
+//    C values delivered from shared memory (256 bytes per wavefront at best,
+//    one wavefront per clock per SM). Each thread therefore walks the whole
+//    sequence for its states sequentially: no cross-thread scan and no carry
+//    fix-up pass, which would add work per element.
+//  * A CTA is one warp = 16 channels of one batch row with its own copy ring,
+//    so no warp ever waits for another. In the recurrence, lane (h, c) =
+//    (lane >> 4, lane & 15) owns states 8h..8h+7 of channel c: each half-warp
+//    reads one B/C address per step (a 16-byte broadcast load, 2 wavefronts),
+//    and the per-(channel, step) values dt and dt*u are shared by two lanes.
+//  * The sequence is cut into 16-step chunks. Lane 0 issues 3-D TMA loads of
+//    a chunk's u/delta/z tiles (16 channels x 16 steps) and of the chunk's
+//    packed B/C rows (fp32, [step][B0..15 C0..15], written once per call by
+//    bc_pack_kernel) into a 4-deep ring with one "full" mbarrier per slot (TMA
+//    transaction count); a slot is refilled as soon as the warp is done with
+//    it, and the waits for data are bounded and report a timeout instead of
+//    hanging.
+//  * Per chunk there are three phases, run in order:
+//      pre-pass   once per (channel, step), lane (c, j) = (lane >> 1, lane & 1)
+//                 taking steps 8j..8j+7 of channel c: dt and dt*u, stored as
+//                 float2 pairs that the recurrence uses, each value broadcast
+//                 to both halves, as packed f32x2 operands;
+//      recurrence per lane, 16 steps x 8 states with packed FMUL2/FFMA2 and
+//                 software-pipelined by one step; the step's partial C.h of
+//                 the lane's 8 states goes to shared memory (one 16-byte store
+//                 per 4 steps);
+//      epilogue   once per (channel, step), same lanes as the pre-pass: the two
+//                 partials + D*u, times silu(z), rounded, one 16-byte store.
+//    All shared-memory strides are chosen so that these accesses are free of
+//    bank conflicts.
+//  * Steps past the end of the sequence get dt = 0 (exp(0) = 1, zero input),
+//    so the padded tail leaves the state unchanged and the final state needs
+//    no masking.
 #pragma once
-
-#include <type_traits>
 
 #include "common.cuh"
 
 namespace mscan {
 
+constexpr int kTL = 16;                  // steps per chunk
+constexpr int kCtaCh = 16;               // channels per CTA (one warp)
+constexpr int kBCW = 2 * kDState;        // floats per step in the packed B/C buffer
+constexpr int kWP = kTL + 2;             // W row stride (float2): 16-byte rows, distinct banks
+constexpr int kPJ = kCtaCh * 4 + 8;      // partial sums: stride between 4-step groups (floats)
+constexpr int kPH = (kTL / 4) * kPJ;     // partial sums: stride between state halves (floats)
+constexpr int kStages = 4;               // TMA ring depth
+constexpr int kScanThreads = 32;
+
 struct ScanArgs {
-    const void* u;
-    const void* delta;
-    const void* z;       // may be null
-    const void* B;
-    const void* C;
     const float* A;
     const float* D;      // may be null
     const float* bias;   // may be null
     void* y;
     float* final_state;  // may be null
     int batch, dim, seqlen;
-    int softplus;
-    int use_tma;         // 1: TMA tiles; 0: plain loads (row pitch not 16-byte aligned)
 };
 
-template <typename T, int ROWS, int TL>
-struct RawTiles {
-    alignas(128) T u[ROWS][TL];
-    alignas(128) T dl[ROWS][TL];
-    alignas(128) T z[ROWS][TL];
-    alignas(128) T B[kDState][TL];
-    alignas(128) T C[kDState][TL];
+template <typename T>
+struct ScanStage {
+    alignas(128) T u[kCtaCh][kTL];
+    alignas(128) T dl[kCtaCh][kTL];
+    alignas(128) T z[kCtaCh][kTL];
+    alignas(128) float bc[kTL][kBCW];
 };
 
-template <typename T, int ROWS, int TL, int STAGES>
+template <typename T>
 struct ScanSmem {
-    RawTiles<T, ROWS, TL> raw[STAGES];
-    alignas(16) float2 W[2][ROWS][TL + 1];            // {dt, dt*u}; odd pitch: conflict-free scan reads
-    alignas(16) float4 BC[2][TL][kDState / 2 + 1];    // per step {B_2k, B_2k+1, C_2k, C_2k+1}; +1 pad
-    alignas(16) float Y[2][2][ROWS][TL + 4];          // partial C.h per half of the states
-    alignas(8) uint64_t full[STAGES];
+    ScanStage<T> st[kStages];
+    alignas(16) float2 W[kCtaCh][kWP];   // {dt, dt*u} per (channel, step)
+    alignas(16) float P[2 * kPH];        // [state half][4-step group][channel][4 steps]
+    alignas(8) uint64_t full[kStages];   // TMA transaction barrier per slot
 };
 
-// Plain (non-TMA) fill of one raw slot, zero outside the tensor. Used when the
-// row pitch seqlen*sizeof(T) is not a multiple of 16 bytes, which TMA cannot map.
-template <typename T, int ROWS, int TL>
-__device__ __forceinline__ void fill_raw_plain(RawTiles<T, ROWS, TL>& R, const ScanArgs& a, int b, int d0, int l0,
-                                               int lane) {
-    const T* u = static_cast<const T*>(a.u);
-    const T* dl = static_cast<const T*>(a.delta);
-    const T* z = static_cast<const T*>(a.z);
-    const T* Bm = static_cast<const T*>(a.B);
-    const T* Cm = static_cast<const T*>(a.C);
-    const T zero = Io<T>::from_f(0.f);
-    for (int i = lane; i < ROWS * TL; i += 32) {
-        const int r = i / TL, t = i % TL;
-        const int d = d0 + r, l = l0 + t;
-        const bool ok = d < a.dim && l < a.seqlen;
-        const size_t off = (static_cast<size_t>(b) * a.dim + d) * a.seqlen + l;
-        R.u[r][t] = ok ? u[off] : zero;
-        R.dl[r][t] = ok ? dl[off] : zero;
-        if (z) R.z[r][t] = ok ? z[off] : zero;
-    }
-    for (int i = lane; i < kDState * TL; i += 32) {
-        const int n = i / TL, t = i % TL;
-        const int l = l0 + t;
-        const bool ok = l < a.seqlen;
-        const size_t off = (static_cast<size_t>(b) * kDState + n) * a.seqlen + l;
-        R.B[n][t] = ok ? Bm[off] : zero;
-        R.C[n][t] = ok ? Cm[off] : zero;
-    }
-}
+// ------------------------------------------------------------ helpers ------
 
-// Load 8 consecutive values (16-byte aligned in shared memory) as fp32.
-__device__ __forceinline__ void lds8_f32(const float* p, float (&v)[8]) {
+// Eight consecutive values (16-byte aligned for bf16, 32-byte for fp32) as fp32.
+__device__ __forceinline__ void lds8(const float* p, float (&v)[8]) {
     const float4 a = reinterpret_cast<const float4*>(p)[0];
     const float4 b = reinterpret_cast<const float4*>(p)[1];
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-__device__ __forceinline__ void lds8_f32(const __nv_bfloat16* p, float (&v)[8]) {
+__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float (&v)[8]) {
     const uint4 q = *reinterpret_cast<const uint4*>(p);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -119,256 +105,309 @@ __device__ __forceinline__ void lds8_f32(const __nv_bfloat16* p, float (&v)[8]) 
     }
 }
 
-// Store 8 consecutive outputs (16-byte aligned in global memory).
-__device__ __forceinline__ void stg8(float* p, const float (&v)[8]) {
-    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+// Eight consecutive outputs to global memory; `vec` = all 8 are in range and
+// the address is aligned for vector stores; otherwise the first `valid` go out
+// one by one.
+__device__ __forceinline__ void stg8(float* p, const float (&v)[8], bool vec, int valid) {
+    if (vec) {
+        reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < valid) p[i] = v[i];
+    }
 }
-__device__ __forceinline__ void stg8(__nv_bfloat16* p, const float (&v)[8]) {
-    uint32_t w[4];
+__device__ __forceinline__ void stg8(__nv_bfloat16* p, const float (&v)[8], bool vec, int valid) {
+    __nv_bfloat162 o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 q = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-        w[j] = *reinterpret_cast<const uint32_t*>(&q);
+    for (int j = 0; j < 4; ++j) o[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    if (vec) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(*reinterpret_cast<const uint32_t*>(&o[0]),
+                                                  *reinterpret_cast<const uint32_t*>(&o[1]),
+                                                  *reinterpret_cast<const uint32_t*>(&o[2]),
+                                                  *reinterpret_cast<const uint32_t*>(&o[3]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < valid) p[i] = (i & 1) ? o[i >> 1].y : o[i >> 1].x;
     }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Per-lane state and the three phases of one CTA.
-template <typename T, int ROWS, int TL, int STAGES, bool SOFTPLUS, bool HAS_Z>
-struct ScanCta {
-    using Smem = ScanSmem<T, ROWS, TL, STAGES>;
-    using Raw = RawTiles<T, ROWS, TL>;
-    static_assert(ROWS * 2 == 32, "one warp: two lanes per row");
-    static_assert(TL == 16, "pre-pass/epilogue: 8 steps per lane; transpose: one step per lane pair");
+// softplus on a pair: max(x,0) + log1p(e^{-|x|}), log1p on the FP32 pipe.
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    const float2 v = make_float2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
+    return __fadd2_rn(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), __fmul2_rn(v, log1p_unit_q2(v)));
+}
 
-    Smem& S;
-    const ScanArgs& a;
-    int lane, r, g, b, d0, d;
-    float bias, Dd;
-    float2 a2[4];  // A[d, 8g .. 8g+7] * log2(e), as pairs
-    float2 h[4];   // this lane's 8 states
+// y * silu(z) on a pair: y * z / (1 + e^{-z}).
+__device__ __forceinline__ float2 gate2(float2 y, float2 z) {
+    const float2 e = make_float2(ex2_approx(-z.x * kLog2e), ex2_approx(-z.y * kLog2e));
+    const float2 den = __fadd2_rn(e, make_float2(1.f, 1.f));
+    const float2 r = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+    return __fmul2_rn(__fmul2_rn(y, z), r);
+}
 
-    __device__ __forceinline__ ScanCta(Smem& S_, const ScanArgs& a_) : S(S_), a(a_) {}
+// ------------------------------------------------------------- kernel ------
 
-    // dt and dt*u for steps 8g..8g+7 of row r; B/C of step lane/2 transposed.
-    __device__ __forceinline__ void prepass(const Raw& R, int buf) {
-        const int t0 = 8 * g;
-        float dv[8], uv[8];
-        lds8_f32(&R.dl[r][t0], dv);
-        lds8_f32(&R.u[r][t0], uv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float dt = dv[i] + bias;
-            if (SOFTPLUS) dt = softplus_f(dt);
-            S.W[buf][r][t0 + i] = make_float2(dt, dt * uv[i]);
-        }
-        const int t = lane >> 1;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int q = 2 * j + (lane & 1);
-            S.BC[buf][t][q] = make_float4(Io<T>::to_f(R.B[2 * q][t]), Io<T>::to_f(R.B[2 * q + 1][t]),
-                                          Io<T>::to_f(R.C[2 * q][t]), Io<T>::to_f(R.C[2 * q + 1][t]));
-        }
-    }
-
-    // One step of the recurrence for this lane's 8 states; returns its part of C.h.
-    // The C.h sum runs as two independent FFMA2 chains (states 0-3, 4-7).
-    __device__ __forceinline__ float step(int buf, int t) {
-        const float2 dw = S.W[buf][r][t];
-        const float2 dd = make_float2(dw.x, dw.x);
-        const float2 ww = make_float2(dw.y, dw.y);
-        float2 yp[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 bc = S.BC[buf][t][4 * g + q];
-            const float2 x = __fmul2_rn(dd, a2[q]);
-            float2 e;
-            e.x = ex2_approx(x.x);
-            e.y = ex2_approx(x.y);
-            const float2 pb = __fmul2_rn(ww, make_float2(bc.x, bc.y));
-            h[q] = __ffma2_rn(e, h[q], pb);
-            yp[q >> 1] = __ffma2_rn(make_float2(bc.z, bc.w), h[q], yp[q >> 1]);
-        }
-        const float2 ys = __fadd2_rn(yp[0], yp[1]);
-        return ys.x + ys.y;
-    }
-
-    // All TL steps of a chunk (fully unrolled), partial sums to Y[buf][g][r][:].
-    __device__ __forceinline__ void scan_full(int buf) {
-#pragma unroll
-        for (int t = 0; t < TL; t += 4) {
-            float yv[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) yv[j] = step(buf, t + j);
-            *reinterpret_cast<float4*>(&S.Y[buf][g][r][t]) = make_float4(yv[0], yv[1], yv[2], yv[3]);
-        }
-    }
-
-    // The first `steps` steps of a chunk (the sequence's last, partial chunk).
-    __device__ __forceinline__ void scan_partial(int buf, int steps) {
-#pragma unroll 1
-        for (int t = 0; t < steps; ++t) S.Y[buf][g][r][t] = step(buf, t);
-    }
-
-    // y = (Y0 + Y1 + D*u) * silu(z) for steps 8g..8g+7 of row r, stored to global.
-    // FULL: the chunk lies entirely inside the sequence.
-    template <bool FULL>
-    __device__ __forceinline__ void epilogue(const Raw& R, int buf, int l0) {
-        const int t0 = 8 * g;
-        float uv[8], zv[8], y0[8], y1[8], out[8];
-        lds8_f32(&R.u[r][t0], uv);
-        if (HAS_Z) lds8_f32(&R.z[r][t0], zv);
-        lds8_f32(&S.Y[buf][0][r][t0], y0);
-        lds8_f32(&S.Y[buf][1][r][t0], y1);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float yy = fmaf(Dd, uv[i], y0[i] + y1[i]);
-            if (HAS_Z) yy *= silu_f(zv[i]);
-            out[i] = yy;
-        }
-        if (d < a.dim) {
-            T* yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + d) * a.seqlen;
-            const int lb = l0 + t0;
-            if (a.use_tma && (FULL || lb + 8 <= a.seqlen)) {
-                stg8(yrow + lb, out);  // row pitch is a multiple of 16 bytes on this path
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (FULL || lb + i < a.seqlen) yrow[lb + i] = Io<T>::from_f(out[i]);
-            }
-        }
-    }
-};
-
-template <typename T, int ROWS, int TL, int STAGES, bool SOFTPLUS, bool HAS_Z>
-__global__ void __launch_bounds__(32)
+template <typename T, bool SOFTPLUS, bool HAS_Z>
+__global__ void __launch_bounds__(kScanThreads)
 scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_dl, const __grid_constant__ CUtensorMap tm_z,
-                const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C) {
-    using Cta = ScanCta<T, ROWS, TL, STAGES, SOFTPLUS, HAS_Z>;
-    __shared__ typename Cta::Smem S;
-    Cta k(S, a);
-    k.lane = threadIdx.x;
-    k.b = blockIdx.y;
-    k.d0 = blockIdx.x * ROWS;
-    k.r = k.lane >> 1;
-    k.g = k.lane & 1;
-    k.d = k.d0 + k.r;
-    const int dc = k.d < a.dim ? k.d : a.dim - 1;  // clamped for parameter loads of padding rows
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 av =
-            *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(dc) * kDState + 8 * k.g + 2 * q);
-        k.a2[q] = make_float2(av.x * kLog2e, av.y * kLog2e);
-        k.h[q] = make_float2(0.f, 0.f);
-    }
-    k.bias = a.bias ? a.bias[dc] : 0.f;
-    k.Dd = a.D ? a.D[dc] : 0.f;
+                const __grid_constant__ CUtensorMap tm_bc) {
+    __shared__ ScanSmem<T> sm;
+    const int lane = threadIdx.x;
+    const int b = blockIdx.y;
+    const int d0 = blockIdx.x * kCtaCh;
+    const int L = a.seqlen;
+    const int n = (L + kTL - 1) / kTL;
 
-    const int n = (a.seqlen + TL - 1) / TL;
-    const int lane = k.lane;
-    constexpr uint32_t kTile = ROWS * TL * sizeof(T);
-    constexpr uint32_t kBC = kDState * TL * sizeof(T);
-    constexpr uint32_t kSlotBytes = (HAS_Z ? 3u : 2u) * kTile + 2u * kBC;
-    int issued = 0;
-
-    auto issue = [&](int c) {  // lane 0 only
-        RawTiles<T, ROWS, TL>& R = S.raw[c % STAGES];
-        uint64_t* bar = &S.full[c % STAGES];
-        mbar_arrive_expect_tx(bar, kSlotBytes);
-        const int l0 = c * TL;
-        tma_load_3d(&R.u[0][0], &tm_u, bar, l0, k.d0, k.b);
-        tma_load_3d(&R.dl[0][0], &tm_dl, bar, l0, k.d0, k.b);
-        if (HAS_Z) tma_load_3d(&R.z[0][0], &tm_z, bar, l0, k.d0, k.b);
-        tma_load_3d(&R.B[0][0], &tm_B, bar, l0, 0, k.b);
-        tma_load_3d(&R.C[0][0], &tm_C, bar, l0, 0, k.b);
+    // Chunk k's tiles into slot k % kStages (lane 0 only).
+    auto issue = [&](int k) {
+        constexpr uint32_t kTile = kCtaCh * kTL * sizeof(T);
+        constexpr uint32_t kStageBytes = (HAS_Z ? 3u : 2u) * kTile + kTL * kBCW * 4u;
+        ScanStage<T>& S = sm.st[k % kStages];
+        uint64_t* bar = &sm.full[k % kStages];
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        const int l0 = k * kTL;
+        tma_load_3d(&S.u[0][0], &tm_u, bar, l0, d0, b);
+        tma_load_3d(&S.dl[0][0], &tm_dl, bar, l0, d0, b);
+        if (HAS_Z) tma_load_3d(&S.z[0][0], &tm_z, bar, l0, d0, b);
+        tma_load_3d(&S.bc[0][0], &tm_bc, bar, 0, l0, b);
     };
-    // Makes chunk c's raw tiles available in slot c % STAGES, first refilling the
-    // ring up to chunk c + STAGES - 3: when chunk c is acquired, the epilogue of
-    // chunk c-2 is done, so only chunks c-1 .. c+STAGES-3 hold slots. Returns
-    // false if a TMA wait timed out (after draining what is still in flight).
-    auto acquire = [&](int c) -> bool {
-        if (!a.use_tma) {
-            fill_raw_plain<T, ROWS, TL>(S.raw[c % STAGES], a, k.b, k.d0, c * TL, lane);
-            __syncwarp();
-            return true;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
+        fence_barrier_init();
+        for (int k = 0; k < n && k < kStages; ++k) issue(k);
+    }
+    __syncwarp();
+
+    // Recurrence lanes: channel rc, states 8*rh .. 8*rh+7.
+    const int rc = lane & 15, rh = lane >> 4;
+    // Pre-pass / epilogue lanes: channel ec, steps 8*ej .. 8*ej+7 of each chunk.
+    const int ec = lane >> 1, ej = lane & 1;
+
+    const int rd = d0 + rc < a.dim ? d0 + rc : a.dim - 1;  // clamped for parameter loads
+    float2 A2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * kDState + 8 * rh + 2 * i);
+        A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
+    }
+    float2 h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
+
+    const int ed = d0 + ec;
+    const bool eactive = ed < a.dim;
+    const int edc = eactive ? ed : a.dim - 1;
+    const float bias = a.bias ? a.bias[edc] : 0.f;
+    const float Dd = a.D ? a.D[edc] : 0.f;
+    // this lane's output: steps 8*ej .. 8*ej+7 of every chunk of channel ed
+    T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + 8 * ej;
+    const bool vec_ok = eactive && (L & 7) == 0;
+
+    // Bounded wait for the tiles of chunk k in slot s; warp-uniform verdict. On
+    // a timeout the warp records the error and waits (bounded again) for the
+    // copies that may still be in flight, so that none lands after it exits.
+    auto wait_full = [&](int s, int k) -> bool {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.full[s], (k / kStages) & 1));
+        if (!ok) {
+            report_device_error(-6);
+            for (int j = k + 1; j < n && j < k + kStages; ++j)
+                mbar_wait_bounded(&sm.full[j % kStages], (j / kStages) & 1);
         }
-        const int want = min(n, c + STAGES - 2);
-        if (issued < want) {
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                for (int q = issued; q < want; ++q) issue(q);
+        return ok;
+    };
+
+    // Slot s is free once every lane is done with chunk k: lane 0 refills it
+    // with chunk k + kStages (the proxy fence orders the lanes' generic reads
+    // of the slot before the TMA's writes).
+    auto release = [&](int k) {
+        if (lane == 0 && k + kStages < n) {
+            fence_proxy_async_smem();
+            issue(k + kStages);
+        }
+    };
+
+    // --- the three phases --------------------------------------------------
+    auto prepass = [&](const ScanStage<T>& S, int k) {
+        float uv[8], dv[8];
+        lds8(&S.u[ec][8 * ej], uv);
+        lds8(&S.dl[ec][8 * ej], dv);
+        const float2 bb = make_float2(bias, bias);
+        float4* W = reinterpret_cast<float4*>(&sm.W[ec][8 * ej]);
+        const int lr = k * kTL + 8 * ej;  // first step of this lane's eight
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 x = __fadd2_rn(make_float2(dv[2 * i], dv[2 * i + 1]), bb);
+            if (SOFTPLUS) x = softplus2(x);
+            float2 w = __fmul2_rn(x, make_float2(uv[2 * i], uv[2 * i + 1]));
+            if (lr + 8 > L) {  // sequence tail: padding steps leave the state unchanged
+                if (lr + 2 * i >= L) { x.x = 0.f; w.x = 0.f; }
+                if (lr + 2 * i + 1 >= L) { x.y = 0.f; w.y = 0.f; }
             }
-            issued = want;
+            W[i] = make_float4(x.x, w.x, x.y, w.y);
         }
-        if (mbar_wait_bounded(&S.full[c % STAGES], (c / STAGES) & 1)) return true;
-        report_device_error(-6);
-        for (int q = c + 1; q < issued; ++q) mbar_wait_bounded(&S.full[q % STAGES], (q / STAGES) & 1);
-        return false;
     };
 
-    if (a.use_tma) {
-        if (lane == 0) {
+    // The recurrence is software-pipelined by one step: the loads, the ex2 of
+    // dt*A and dt*u*B of step t+1 are issued before the state update of step t,
+    // so their latencies overlap the dependent FMA chain of the previous step.
+    auto recurrence = [&](const ScanStage<T>& S) {
+        const float2* W = &sm.W[rc][0];
+        const float* bc = &S.bc[0][0];
+        float* P = &sm.P[rh * kPH + 4 * rc];
+        float2 e[4], pb[4], cv[4];
+        auto front = [&](int t) {  // everything of step t that does not depend on h
+            const float2 w = W[t];
+            const float4 b0 = *reinterpret_cast<const float4*>(bc + t * kBCW + 8 * rh);
+            const float4 b1 = *reinterpret_cast<const float4*>(bc + t * kBCW + 8 * rh + 4);
+            const float4 c0 = *reinterpret_cast<const float4*>(bc + t * kBCW + kDState + 8 * rh);
+            const float4 c1 = *reinterpret_cast<const float4*>(bc + t * kBCW + kDState + 8 * rh + 4);
+            const float2 dd = make_float2(w.x, w.x);
+            const float2 du = make_float2(w.y, w.y);
+            const float2 bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                  make_float2(b1.z, b1.w)};
+            cv[0] = make_float2(c0.x, c0.y); cv[1] = make_float2(c0.z, c0.w);
+            cv[2] = make_float2(c1.x, c1.y); cv[3] = make_float2(c1.z, c1.w);
 #pragma unroll
-            for (int s = 0; s < STAGES; ++s) mbar_init(&S.full[s], 1);
-            fence_barrier_init();
+            for (int i = 0; i < 4; ++i) {
+                const float2 x = __fmul2_rn(dd, A2[i]);
+                e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                pb[i] = __fmul2_rn(du, bv[i]);
+            }
+        };
+        front(0);
+#pragma unroll
+        for (int t0 = 0; t0 < kTL; t0 += 4) {
+            float p[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = t0 + i;
+                float2 E[4], PB[4], CV[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) { E[j] = e[j]; PB[j] = pb[j]; CV[j] = cv[j]; }
+                if (t + 1 < kTL) front(t + 1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) h[j] = __ffma2_rn(E[j], h[j], PB[j]);
+                float2 acc0 = __fmul2_rn(CV[0], h[0]);
+                float2 acc1 = __fmul2_rn(CV[1], h[1]);
+                acc0 = __ffma2_rn(CV[2], h[2], acc0);
+                acc1 = __ffma2_rn(CV[3], h[3], acc1);
+                const float2 acc = __fadd2_rn(acc0, acc1);
+                p[i] = acc.x + acc.y;
+            }
+            *reinterpret_cast<float4*>(P + (t0 / 4) * kPJ) = make_float4(p[0], p[1], p[2], p[3]);
         }
-        __syncwarp();
-    }
-
-    // One steady-state iteration: recurrence of chunk c, pre-pass of c+1, epilogue
-    // of c-1. P = c & 1 is a compile-time constant so that every shared-memory
-    // buffer index is static and the three phases can be interleaved freely.
-    auto steady = [&](auto parity, int c) -> bool {
-        constexpr int P = decltype(parity)::value;
-        if (!acquire(c + 1)) return false;
-        k.scan_full(P);
-        k.prepass(S.raw[(c + 1) % STAGES], P ^ 1);
-        k.template epilogue<true>(S.raw[(c - 1) % STAGES], P ^ 1, (c - 1) * TL);
-        __syncwarp();
-        return true;
     };
 
+    auto epilogue = [&](const ScanStage<T>& S, int k) {
+        // steps 8*ej .. 8*ej+7 are the 4-step groups 2*ej and 2*ej+1
+        const float* P0 = &sm.P[(2 * ej) * kPJ + 4 * ec];
+        const float4 a0 = *reinterpret_cast<const float4*>(P0);
+        const float4 a1 = *reinterpret_cast<const float4*>(P0 + kPJ);
+        const float4 b0 = *reinterpret_cast<const float4*>(P0 + kPH);
+        const float4 b1 = *reinterpret_cast<const float4*>(P0 + kPH + kPJ);
+        float2 y[4] = {__fadd2_rn(make_float2(a0.x, a0.y), make_float2(b0.x, b0.y)),
+                       __fadd2_rn(make_float2(a0.z, a0.w), make_float2(b0.z, b0.w)),
+                       __fadd2_rn(make_float2(a1.x, a1.y), make_float2(b1.x, b1.y)),
+                       __fadd2_rn(make_float2(a1.z, a1.w), make_float2(b1.z, b1.w))};
+        float uv[8];
+        lds8(&S.u[ec][8 * ej], uv);
+        const float2 DD = make_float2(Dd, Dd);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = __ffma2_rn(DD, make_float2(uv[2 * i], uv[2 * i + 1]), y[i]);
+        if (HAS_Z) {
+            float zv[8];
+            lds8(&S.z[ec][8 * ej], zv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) y[i] = gate2(y[i], make_float2(zv[2 * i], zv[2 * i + 1]));
+        }
+        const float out[8] = {y[0].x, y[0].y, y[1].x, y[1].y, y[2].x, y[2].y, y[3].x, y[3].y};
+        const int l = k * kTL + 8 * ej;
+        if (vec_ok && l + 8 <= L) {
+            stg8(yrow + k * kTL, out, true, 8);
+        } else if (eactive && l < L) {
+            stg8(yrow + k * kTL, out, false, L - l);
+        }
+    };
+
+    // --- main loop ----------------------------------------------------------
+    // The phases run in order (recurrence k, epilogue k, pre-pass k+1), so W
+    // and P are single-buffered; the other warps on the SM fill the issue
+    // slots each phase leaves idle. The loop body is not unrolled over the
+    // ring: one copy of the (fully unrolled) chunk code stays in the
+    // instruction cache.
     if (n > 0) {
-        if (!acquire(0)) return;
-        k.prepass(S.raw[0], 0);
+        if (!wait_full(0, 0)) return;
+        prepass(sm.st[0], 0);
         __syncwarp();
-        const int last_steps = a.seqlen - (n - 1) * TL;
-        if (n == 1) {
-            if (last_steps == TL) k.scan_full(0); else k.scan_partial(0, last_steps);
-            __syncwarp();
-            k.template epilogue<false>(S.raw[0], 0, 0);
-        } else {
-            // c = 0: recurrence of chunk 0 and pre-pass of chunk 1
-            if (!acquire(1)) return;
-            k.scan_full(0);
-            k.prepass(S.raw[1 % STAGES], 1);
-            __syncwarp();
-            // steady state, two iterations per trip (odd c, then even c)
-            int c = 1;
 #pragma unroll 1
-            for (; c + 1 < n - 1; c += 2) {
-                if (!steady(std::integral_constant<int, 1>{}, c)) return;
-                if (!steady(std::integral_constant<int, 0>{}, c + 1)) return;
-            }
-            if (c < n - 1) {
-                if (!steady(std::integral_constant<int, 1>{}, c)) return;
-                ++c;
-            }
-            // c = n-1: recurrence of the last chunk, epilogue of chunk n-2
-            if (last_steps == TL) k.scan_full(c & 1); else k.scan_partial(c & 1, last_steps);
-            k.template epilogue<true>(S.raw[(c - 1) % STAGES], (c - 1) & 1, (c - 1) * TL);
+        for (int k = 0; k < n; ++k) {
+            const ScanStage<T>& S = sm.st[k % kStages];
+            recurrence(S);
             __syncwarp();
-            k.template epilogue<false>(S.raw[c % STAGES], c & 1, c * TL);
+            epilogue(S, k);
+            __syncwarp();
+            release(k);
+            if (k + 1 < n) {
+                const int s1 = (k + 1) % kStages;
+                if (!wait_full(s1, k + 1)) return;
+                prepass(sm.st[s1], k + 1);
+            }
+            __syncwarp();
         }
     }
 
-    if (a.final_state && k.d < a.dim) {
-        float4* fs = reinterpret_cast<float4*>(a.final_state + (static_cast<size_t>(k.b) * a.dim + k.d) * kDState +
-                                               8 * k.g);
-        fs[0] = make_float4(k.h[0].x, k.h[0].y, k.h[1].x, k.h[1].y);
-        fs[1] = make_float4(k.h[2].x, k.h[2].y, k.h[3].x, k.h[3].y);
+    if (a.final_state && d0 + rc < a.dim) {
+        float4* fs = reinterpret_cast<float4*>(a.final_state +
+                                               (static_cast<size_t>(b) * a.dim + d0 + rc) * kDState + 8 * rh);
+        fs[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+        fs[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+    }
+}
+
+// Packs B and C ((batch, 16, L) each, io dtype) into one fp32 buffer
+// (batch, Lp, 32): row l holds B[:, l] then C[:, l]; rows l >= L are zero.
+// One thread per (batch, row): strided reads coalesce across threads, and each
+// thread writes its 128-byte row with eight 16-byte stores.
+template <typename T>
+__global__ void __launch_bounds__(256)
+bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restrict__ out, int batch, int L,
+               int Lp) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<long long>(batch) * Lp) return;
+    const int b = static_cast<int>(i / Lp);
+    const int l = static_cast<int>(i % Lp);
+    float v[kBCW];
+    const bool ok = l < L;
+    const size_t base = static_cast<size_t>(b) * kDState * L + l;
+#pragma unroll
+    for (int s = 0; s < kDState; ++s) {
+        v[s] = ok ? Io<T>::to_f(B[base + static_cast<size_t>(s) * L]) : 0.f;
+        v[kDState + s] = ok ? Io<T>::to_f(C[base + static_cast<size_t>(s) * L]) : 0.f;
+    }
+    float4* o = reinterpret_cast<float4*>(out + i * kBCW);
+#pragma unroll
+    for (int j = 0; j < kBCW / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+// Copies rows of length L into rows of pitch Lpitch >= L (the tail is left as
+// is: TMA boxes read it, but padding steps are masked in the pre-pass). Used
+// only when L * sizeof(T) is not a multiple of 16 bytes, which a TMA tensor
+// map cannot stride over.
+template <typename T>
+__global__ void __launch_bounds__(256)
+row_pitch_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, int L, int Lpitch) {
+    const long long total = rows * L;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / L;
+        const int l = static_cast<int>(i - r * L);
+        dst[r * Lpitch + l] = src[i];
     }
 }
 

@@ -42,13 +42,20 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return s.cuda_stream
 
 
+def workspace_bytes(batch: int, dim: int, seqlen: int, dtype: torch.dtype, dstate: int = 16) -> int:
+    """Device workspace the scan needs for these sizes (mamba_scan_workspace_size)."""
+    return int(_lib.lib().mamba_scan_workspace_size(batch, dim, seqlen, dstate, _IO[dtype]))
+
+
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                   y=None, final_state=None, stream=None):
-    """Selective scan (see include/mamba_scan.h, mamba_scan_fwd).
+                   y=None, final_state=None, stream=None, workspace=None):
+    """Selective scan (see include/mamba_scan.h, mamba_scan_fwd_ws).
 
     u, delta, z: (batch, dim, L); B, C: (batch, 16, L), all fp32 or all bf16;
     A: (dim, 16) fp32; D, delta_bias: (dim,) fp32. ``final_state`` may be a
     preallocated (batch, dim, 16) fp32 tensor, or True to allocate one.
+    ``workspace`` may be a uint8 CUDA tensor of at least ``workspace_bytes(...)``
+    bytes; otherwise one is taken from torch's caching allocator.
     Returns y, or (y, final_state) when a final state was requested.
     """
     if u.dtype not in _IO:
@@ -75,10 +82,16 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     elif final_state is False:
         final_state = None
     _need(final_state, "final_state", torch.float32, (batch, dim, N), dev)
-    st = _lib.lib().mamba_scan_fwd(
+    lib = _lib.lib()
+    need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[u.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    st = lib.mamba_scan_fwd_ws(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(y), _ptr(final_state), batch, dim, L, N, _IO[u.dtype],
-        _stream_handle(stream, dev))
+        _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_fwd")
     return (y, final_state) if want_state else y
 

@@ -32,11 +32,11 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(0, -7, -1):
+    for code in range(0, -8, -1):
         s = L.mamba_status_string(code).decode()
         assert s.startswith(_lib.STATUS[code])
     assert L.mamba_status_string(42).decode() == "unknown mamba_status"
-    assert L.mamba_version() == 100
+    assert L.mamba_version() == 200
 
 
 # Fake, never-dereferenced addresses: validation fails before any CUDA call.
@@ -97,3 +97,29 @@ def test_update_rejects(L, kw, code):
 
 def test_update_empty_is_noop(L):
     assert update(L, batch=0, state=None) == 0
+
+
+def scan_ws(L, ws=P, ws_bytes=1 << 30, **kw):
+    args = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, sp=1, y=P, fs=None,
+                batch=2, dim=32, seqlen=64, dstate=16, dtype=1, stream=None)
+    args.update(kw)
+    return L.mamba_scan_fwd_ws(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["z"],
+                               args["bias"], args["sp"], args["y"], args["fs"], args["batch"], args["dim"],
+                               args["seqlen"], args["dstate"], args["dtype"], ws, ws_bytes, args["stream"])
+
+
+def test_workspace_size(L):
+    # packed fp32 B/C rows: batch * roundup(L, 16) * 128 bytes
+    assert L.mamba_scan_workspace_size(8, 2048, 4096, 16, 1) == 8 * 4096 * 128
+    assert L.mamba_scan_workspace_size(2, 64, 17, 16, 1) >= 2 * 32 * 128 + 3 * 2 * 64 * 24 * 2
+    assert L.mamba_scan_workspace_size(2, 64, 20, 16, 0) == 2 * 32 * 128   # 20 fp32 = 80 B rows: no copies
+    assert L.mamba_scan_workspace_size(1, 1, 0, 16, 1) == 0
+    assert L.mamba_scan_workspace_size(1, 1, 16, 8, 1) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), -1), (dict(ws_bytes=100), -7), (dict(ws=P + 16), -4),
+    (dict(dtype=5), -3), (dict(dstate=64), -2), (dict(u=P + 2), -4), (dict(C=None), -1),
+])
+def test_scan_ws_rejects(L, kw, code):
+    assert scan_ws(L, **kw) == code

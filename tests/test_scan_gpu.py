@@ -77,19 +77,21 @@ def test_workload_parity(name):
 EDGE = [
     # batch, dim, L, dtype, flags
     (1, 16, 32, torch.float32, {}),              # exactly one tile, two chunks
-    (2, 20, 40, torch.bfloat16, {}),             # ragged channels and ragged last chunk (TMA path)
-    (1, 33, 100, torch.float32, {}),             # ragged everything, fp32 row pitch 400 B (TMA path)
-    (3, 17, 7, torch.bfloat16, {}),              # L % 8 != 0: plain-load path
+    (2, 20, 40, torch.bfloat16, {}),             # ragged channels and ragged last chunk
+    (1, 33, 100, torch.float32, {}),             # ragged everything, fp32 row pitch 400 B
+    (3, 17, 7, torch.bfloat16, {}),              # L % 8 != 0: rows copied to a 16-byte pitch first
     (2, 5, 1, torch.float32, {}),                # L = 1
     (1, 1, 1, torch.bfloat16, {}),               # a single element row
-    (2, 48, 257, torch.bfloat16, {}),            # ragged, plain-load path, several chunks
+    (2, 48, 257, torch.bfloat16, {}),            # ragged, row-pitch copy, several chunks
+    (1, 16, 6, torch.float32, {}),               # fp32 row of 24 bytes: row-pitch copy
     (1, 64, 1000, torch.float32, dict(with_z=False)),
     (1, 64, 512, torch.bfloat16, dict(with_D=False)),
     (2, 32, 96, torch.float32, dict(softplus_in_kernel=False)),
     (1, 40, 64, torch.bfloat16, dict(with_D=False, with_z=False, softplus_in_kernel=False)),
     (4, 64, 4096, torch.bfloat16, dict(a_noise=0.1)),
-    (1, 48, 48, torch.bfloat16, {}),             # three chunks: one steady-state iteration
-    (1, 32, 80, torch.bfloat16, {}),             # five chunks: odd number of steady-state iterations
+    (1, 48, 48, torch.bfloat16, {}),             # three chunks
+    (1, 32, 80, torch.bfloat16, {}),             # five chunks: the ring (4 slots) wraps
+    (1, 16, 16 * 9, torch.bfloat16, {}),         # nine chunks: every slot reused twice
 ]
 
 
@@ -148,3 +150,22 @@ def test_inputs_not_modified():
     torch.cuda.synchronize()
     for k, v in before.items():
         assert torch.equal(v, d[k]), k
+
+
+def test_allocating_entry_point_through_the_c_abi():
+    """mamba_scan_fwd (workspace allocated stream-ordered by the library) equals the _ws path."""
+    import ctypes
+    from selective_state_space_133_b300 import _lib
+    x = syn.scan_inputs(2, 40, 203, torch.bfloat16, seed=21)   # 203: odd length, row-pitch copies too
+    d = to_dev(x)
+    y_ref, h_ref = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                      d["delta_bias"], True, final_state=True)
+    y = torch.empty_like(y_ref)
+    h = torch.empty_like(h_ref)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = _lib.lib().mamba_scan_fwd(p(d["u"]), p(d["delta"]), p(d["A"]), p(d["B"]), p(d["C"]), p(d["D"]),
+                                   p(d["z"]), p(d["delta_bias"]), 1, p(y), p(h), 2, 40, 203, 16, _lib.MAMBA_BF16,
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    ops.check_device_error()
+    assert torch.equal(y, y_ref) and torch.equal(h, h_ref)
