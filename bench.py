@@ -164,13 +164,22 @@ def oracle_rate(x, w, budget_s: float):
     return elems / elapsed, elems, rows_done, elapsed
 
 
+def workload_config(w, ws: int) -> dict:
+    """The `config` object of both arms' JSON line."""
+    return {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
+            "io_dtype": "bf16" if "bf16" in w.name else "fp32", "z_gate": w.with_z, "skip_D": w.with_D,
+            "softplus_in_kernel": w.softplus_in_kernel, "state_dtype": "fp32",
+            "parallelism": f"replicas x{ws}", "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB > 126 MB L2"}
+
+
 def run_reference(args, w):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
     from selective_state_space_133_b300 import synthetic as syn
     x = syn.workload_inputs(w)
-    per_step_budget = float(os.environ.get("BENCH_REF_STEP_S", "2.0"))
+    # about a minute of oracle work in total, so that --steps 200 still ends in minutes
+    per_step_budget = float(os.environ.get("BENCH_REF_STEP_S", str(max(0.05, min(2.0, 60.0 / max(1, args.steps))))))
     for _ in range(args.warmup):
         oracle_rate(x, w, per_step_budget / 4)
     tot_elems, tot_time, rows = 0, 0.0, 0
@@ -181,12 +190,11 @@ def run_reference(args, w):
         rows += r
     value = tot_elems / tot_time
     sample = (f"each step: whole channels (all {w.seqlen} steps x 16 states) of the workload, about "
-              f"{per_step_budget:.1f} s of single-thread fp64 oracle work; {rows} channels over {args.steps} steps")
+              f"{per_step_budget:.2f} s of single-thread fp64 oracle work; {rows} channels over {args.steps} steps")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_time / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
-                       "io_dtype": "bf16" if "bf16" in w.name else "fp32"},
+            "config": workload_config(w, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -301,10 +309,7 @@ def run_ours(args, w):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
-                   "z_gate": w.with_z, "skip_D": w.with_D, "softplus_in_kernel": w.softplus_in_kernel,
-                   "state_dtype": "fp32", "parallelism": f"replicas x{ws}",
-                   "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB > 126 MB L2"},
+        "config": workload_config(w, ws),
         "gpu_launches": 2 * K,
         "hbm_gbs": achieved,
         "roofline": roofline,
@@ -319,6 +324,124 @@ def run_ours(args, w):
     return 0
 
 
+def oracle_update_rate(w, budget_s: float):
+    """Time the fp64 oracle state update (1 thread) on whole decode steps of the workload; elem/s."""
+    import oracle
+    from selective_state_space_133_b300 import synthetic as syn
+    orc = oracle.default()
+    st = syn.decode_static(w)
+    state = st["state"].double().numpy()
+    steps, elapsed = 0, 0.0
+    while elapsed < budget_s and steps < w.steps:
+        x = syn.decode_step(w, steps)
+        t0 = time.perf_counter()
+        _, new_state = orc.state_update(state, x["u"], x["delta"], st["A"], x["B"], x["C"], st["D"], x["z"],
+                                        st["delta_bias"], True)
+        elapsed += time.perf_counter() - t0
+        state = new_state.reshape(state.shape)
+        steps += 1
+    return w.elements_per_step * steps / elapsed, steps, elapsed
+
+
+def run_decode(args, w):
+    """One step = one single-token state update of every (sequence, channel) of the workload."""
+    import torch
+    from selective_state_space_133_b300 import ops
+    from selective_state_space_133_b300 import synthetic as syn
+
+    ws, rank, local = dist_setup(want_nccl=True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st = {k: v.to(dev) for k, v in syn.decode_static(w).items()}
+    n_in = min(8, w.steps)
+    xs = [{k: v.to(dev) for k, v in syn.decode_step(w, i).items()} for i in range(n_in)]
+    y = torch.empty_like(xs[0]["u"])
+    stream = torch.cuda.current_stream(dev)
+    # the state (84 MB) fits the 126 MB L2: flush it before every timed update
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(i):
+        x = xs[i % n_in]
+        ops.mamba_state_update(st["state"], x["u"], x["delta"], st["A"], x["B"], x["C"], st["D"], x["z"],
+                               st["delta_bias"], True, y=y, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    ops.check_device_error(stream)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local] if vis else str(local)) if rank == 0 else None
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        for i in range(20):
+            flush.zero_()
+            step(i)
+        torch.cuda.synchronize(dev)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ops.check_device_error(stream)
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), ws, dev)
+    ms = total_ms / K
+    value = ws * w.elements_per_step / (ms * 1e-3)
+
+    # e2e: each step's token inputs from pinned host memory, y back to the host
+    hx = [{k: v.cpu().pin_memory() for k, v in x.items()} for x in xs]
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hx[0].values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step(i):
+        for k, v in hx[i % n_in].items():
+            xs[i % n_in][k].copy_(v, non_blocking=True)
+        step(i)
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize(dev)
+    K2 = max(3, min(K, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(stream)
+    for i in range(K2):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / K2
+    if rank != 0:
+        return 0
+    peak, peak_kind = hbm_peak()
+    achieved = w.io_bytes_per_step / (ms * 1e-3) / 1e9
+    cpu_v, cpu_steps, cpu_t = oracle_update_rate(w, float(os.environ.get("BENCH_CPU_BASELINE_S", "10")))
+    line = {
+        "metric": "state-update elems/s (B·D·N per token) & achieved HBM GB/s vs roofline, 1×B300",
+        "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": 16, "state_dtype": "fp32",
+                   "parallelism": f"replicas x{ws}", "l2": "flushed (512 MB write) before every timed step"},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes_per_step},
+        "clocks": clocks,
+        "e2e": {"value": ws * w.elements_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2},
+        "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{cpu_steps} whole decode steps of the workload, single-thread fp64, {cpu_t:.1f} s"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -328,6 +451,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     args = ap.parse_args()
     from selective_state_space_133_b300 import synthetic as syn
+    if args.workload in syn.DECODE_WORKLOADS:
+        if args.impl == "reference":
+            raise SystemExit("--impl reference times the scan workload only")
+        return run_decode(args, syn.DECODE_WORKLOADS[args.workload])
     w = syn.SCAN_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
