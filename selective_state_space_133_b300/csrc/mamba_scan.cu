@@ -130,10 +130,8 @@ int launch_scan(const mscan::ScanArgs& a, const void* u, const void* delta, cons
 
 template <typename T>
 int launch_update(const mscan::UpdateArgs& a, cudaStream_t stream) {
-    const long long rows = static_cast<long long>(a.batch) * a.dim;
-    constexpr int kRowsPerBlock = mscan::kUpdateThreads / 4;
-    const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    mscan::state_update_kernel<T><<<static_cast<unsigned>(blocks), mscan::kUpdateThreads, 0, stream>>>(a);
+    const dim3 grid((a.dim + mscan::kUpdateCh - 1) / mscan::kUpdateCh, a.batch);
+    mscan::state_update_kernel<T><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
@@ -224,16 +222,15 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
                        int dim, int dstate, int io_dtype, void* stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 0 || dim < 0 || dstate != kDState) return MAMBA_ERR_SHAPE;
-    const unsigned long long rows = static_cast<unsigned long long>(batch) * dim;
-    if (rows / 64 >= (1ull << 31)) return MAMBA_ERR_SHAPE;  // grid.x
-    if (rows == 0) return MAMBA_OK;
+    if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
+    if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!state || !u || !delta || !A || !B || !C || !y) return MAMBA_ERR_NULL;
     const void* p16[] = {state, A};
     for (const void* p : p16)
         if (!aligned(p, 16)) return MAMBA_ERR_ALIGN;
     const size_t es = dtype_size(io_dtype);
-    // B/C rows are read 4 elements at a time
-    if (!aligned(B, 4 * es) || !aligned(C, 4 * es)) return MAMBA_ERR_ALIGN;
+    // B/C rows are read 16 bytes at a time
+    if (!aligned(B, 16) || !aligned(C, 16)) return MAMBA_ERR_ALIGN;
     const void* pe[] = {u, delta, z, y};
     for (const void* p : pe)
         if (p && !aligned(p, es)) return MAMBA_ERR_ALIGN;

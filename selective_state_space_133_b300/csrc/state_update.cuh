@@ -7,11 +7,13 @@
 //     h  = exp(dt*A[d,:]) * h + dt*B[b,:]*u
 //     y  = (C[b,:] . h + D[d]*u) * silu(z)
 //
-// The step is bound by HBM: the state (64 bytes per channel) is read and written
-// once, everything else is a few bytes per channel. Four lanes share a channel,
-// each owning 4 consecutive states (one 16-byte load and store), so a warp moves
-// 512 contiguous bytes of state per instruction; the partial C.h sums are added
-// with two xor-shuffles inside the 4-lane group.
+// The step is bound by HBM: the state (64 bytes per row) is read and written
+// once, everything else is a few bytes per row or shared by a whole batch row
+// (B, C) or channel (A). Four lanes share a row, each owning 4 consecutive
+// states, so a warp moves 512 contiguous bytes of state per load and store;
+// the partial C.h sums are added with two xor-shuffles inside the 4-lane group.
+// All of a row's loads are issued before any arithmetic. The grid is
+// (channels / 64, batch), so no thread divides to find its row.
 #pragma once
 
 #include "common.cuh"
@@ -33,67 +35,71 @@ struct UpdateArgs {
     int softplus;
 };
 
-template <typename T>
-__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
+constexpr int kUpdateThreads = 256;   // 64 channels per pass, 4 lanes each
+constexpr int kUpdateRows = 1;         // rows per lane (2 doubles the registers and halves the warps: slower)
+constexpr int kUpdateCh = kUpdateThreads / 4 * kUpdateRows;  // channels per block
 
-template <>
-__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+// Four consecutive values (16-byte aligned for fp32, 8-byte for bf16) as fp32 pairs.
+__device__ __forceinline__ void ldg4(const float* p, float2& lo, float2& hi) {
     const float4 q = *reinterpret_cast<const float4*>(p);
-    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+    lo = make_float2(q.x, q.y);
+    hi = make_float2(q.z, q.w);
 }
-
-template <>
-__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+__device__ __forceinline__ void ldg4(const __nv_bfloat16* p, float2& lo, float2& hi) {
     const uint2 q = *reinterpret_cast<const uint2*>(p);
-    v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
-    v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+    lo = make_float2(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u));
+    hi = make_float2(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
 }
-
-constexpr int kUpdateThreads = 256;  // 64 channels per block
 
 template <typename T>
 __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const UpdateArgs a) {
-    const long long rows = static_cast<long long>(a.batch) * a.dim;
-    const long long row = static_cast<long long>(blockIdx.x) * (kUpdateThreads / 4) + (threadIdx.x >> 2);
+    const int b = blockIdx.y;
     const int q = threadIdx.x & 3;
-    const bool valid = row < rows;
-    const long long rr = valid ? row : rows - 1;  // padding lanes recompute the last row, store nothing
-    const int b = static_cast<int>(rr / a.dim);
-    const int d = static_cast<int>(rr % a.dim);
-
     const T* u = static_cast<const T*>(a.u);
     const T* dl = static_cast<const T*>(a.delta);
-    float dt = Io<T>::to_f(dl[rr]) + (a.bias ? a.bias[d] : 0.f);
-    if (a.softplus) dt = softplus_f(dt);
-    const float uu = Io<T>::to_f(u[rr]);
 
-    float hs[4], av[4], bv[4], cv[4];
-    float4* sp = reinterpret_cast<float4*>(a.state + rr * kDState + 4 * q);
-    {
-        const float4 s4 = *sp;
-        hs[0] = s4.x; hs[1] = s4.y; hs[2] = s4.z; hs[3] = s4.w;
-    }
-    load4<float>(a.A + static_cast<size_t>(d) * kDState + 4 * q, av);
-    load4<T>(static_cast<const T*>(a.B) + static_cast<size_t>(b) * kDState + 4 * q, bv);
-    load4<T>(static_cast<const T*>(a.C) + static_cast<size_t>(b) * kDState + 4 * q, cv);
+    // B, C of this batch row: the same for every lane of the block
+    float2 B01, B23, C01, C23;
+    ldg4(static_cast<const T*>(a.B) + static_cast<size_t>(b) * kDState + 4 * q, B01, B23);
+    ldg4(static_cast<const T*>(a.C) + static_cast<size_t>(b) * kDState + 4 * q, C01, C23);
 
-    const float w = dt * uu;
-    float yp = 0.f;
+    int d[kUpdateRows], dc[kUpdateRows];
+    size_t row[kUpdateRows];
+    float4 s4[kUpdateRows];
+    float2 A01[kUpdateRows], A23[kUpdateRows];
+    float uu[kUpdateRows], dv[kUpdateRows];
+    // all loads first
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float e = ex2_approx(dt * (av[j] * kLog2e));
-        hs[j] = fmaf(e, hs[j], w * bv[j]);
-        yp = fmaf(cv[j], hs[j], yp);
+    for (int r = 0; r < kUpdateRows; ++r) {
+        d[r] = blockIdx.x * kUpdateCh + r * (kUpdateThreads / 4) + (threadIdx.x >> 2);
+        dc[r] = d[r] < a.dim ? d[r] : a.dim - 1;  // padding lanes recompute the last channel, store nothing
+        row[r] = static_cast<size_t>(b) * a.dim + dc[r];
+        s4[r] = *reinterpret_cast<const float4*>(a.state + row[r] * kDState + 4 * q);
+        ldg4(a.A + static_cast<size_t>(dc[r]) * kDState + 4 * q, A01[r], A23[r]);
+        uu[r] = Io<T>::to_f(u[row[r]]);
+        dv[r] = Io<T>::to_f(dl[row[r]]);
     }
-    yp += __shfl_xor_sync(0xffffffffu, yp, 1);
-    yp += __shfl_xor_sync(0xffffffffu, yp, 2);
-
-    if (valid) {
-        *sp = make_float4(hs[0], hs[1], hs[2], hs[3]);
-        if (q == 0) {
-            float yy = a.D ? fmaf(a.D[d], uu, yp) : yp;
-            if (a.z) yy *= silu_f(Io<T>::to_f(static_cast<const T*>(a.z)[rr]));
-            static_cast<T*>(a.y)[rr] = Io<T>::from_f(yy);
+#pragma unroll
+    for (int r = 0; r < kUpdateRows; ++r) {
+        float dt = dv[r] + (a.bias ? a.bias[dc[r]] : 0.f);
+        if (a.softplus) dt = softplus_f(dt);
+        const float2 dlt = make_float2(dt * kLog2e, dt * kLog2e);
+        const float2 w = make_float2(dt * uu[r], dt * uu[r]);
+        float2 h01 = make_float2(s4[r].x, s4[r].y), h23 = make_float2(s4[r].z, s4[r].w);
+        const float2 x01 = __fmul2_rn(dlt, A01[r]), x23 = __fmul2_rn(dlt, A23[r]);
+        h01 = __ffma2_rn(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, __fmul2_rn(w, B01));
+        h23 = __ffma2_rn(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, __fmul2_rn(w, B23));
+        const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
+        float yp = acc.x + acc.y;
+        yp += __shfl_xor_sync(0xffffffffu, yp, 1);
+        yp += __shfl_xor_sync(0xffffffffu, yp, 2);
+        if (d[r] < a.dim) {
+            *reinterpret_cast<float4*>(a.state + row[r] * kDState + 4 * q) = make_float4(h01.x, h01.y, h23.x, h23.y);
+            if (q == 0) {
+                float yy = a.D ? fmaf(a.D[d[r]], uu[r], yp) : yp;
+                if (a.z) yy *= silu_f(Io<T>::to_f(static_cast<const T*>(a.z)[row[r]]));
+                static_cast<T*>(a.y)[row[r]] = Io<T>::from_f(yy);
+            }
         }
     }
 }

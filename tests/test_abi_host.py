@@ -90,6 +90,7 @@ def update(L, **kw):
     (dict(dtype=7), -3), (dict(dstate=4), -2), (dict(batch=-2), -2),
     (dict(state=None), -1), (dict(u=None), -1), (dict(y=None), -1), (dict(A=None), -1),
     (dict(state=P + 4), -4), (dict(A=P + 8), -4), (dict(B=P + 2), -4), (dict(u=P + 1), -4),
+    (dict(C=P + 8), -4), (dict(batch=70000), -2),
 ])
 def test_update_rejects(L, kw, code):
     assert update(L, **kw) == code
