@@ -125,6 +125,39 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       void* stream);
 
 /*
+ * mamba_scan_fwd without any allocation and without a caller workspace.
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory at call time (serving loops that reserve all
+ * memory at start-up, plugins inside a framework that owns every device
+ * allocation, programs with no allocator to provide a workspace).
+ *
+ * Same arguments, semantics and checks as mamba_scan_fwd. The scratch that
+ * mamba_scan_fwd_ws takes from the caller lives instead in a fixed 16 MiB
+ * array in device memory that the library reserves on every GPU that loads
+ * it, until the process exits.
+ *   - Sizes whose workspace (mamba_scan_workspace_size) exceeds 16 MiB are
+ *     rejected with MAMBA_ERR_WORKSPACE before anything is launched. For
+ *     lengths whose rows are whole 16-byte units that allows
+ *     batch * roundup(seqlen, 16) <= 131072 (e.g. 8 x 4096 or 1 x 131072).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it: make that
+ *     first call before any stream capture is under way.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, or other host threads) race on it and must be serialised by the
+ *     caller. Nothing needs clearing between calls: each call writes all the
+ *     scratch it reads.
+ * Returns MAMBA_OK or a negative mamba_status (MAMBA_ERR_CUDA if the address
+ * lookup fails).
+ */
+int mamba_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                           const void* B, const void* C,
+                           const float* D, const void* z,
+                           const float* delta_bias, int softplus_flag,
+                           void* y, float* final_state,
+                           int batch, int dim, int seqlen, int dstate,
+                           int io_dtype, void* stream);
+
+/*
  * Single-token recurrent state update (decode): one step of the recurrence above
  * applied in place to `state` ("mamba->jamba" §2.2: constant-time recurrent
  * inference; "Mamba 论文精读" §6: O(1) work and a fixed-size state per token).

@@ -217,6 +217,65 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void*
     return st;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free scan: a fixed scratch array instead of a workspace.
+//
+// Some callers cannot allocate device memory at call time: serving loops that
+// reserve all their memory at start-up and must not allocate afterwards,
+// plugins running inside a host framework that owns every device allocation,
+// and programs that have no allocator of their own to hand us a workspace.
+// For them, mamba_scan_fwd_noalloc runs the same kernels with its scratch in
+// this file-scope device array, which every GPU that loads the library holds
+// until the process exits.
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_scan_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_scan_scratch on the current device. In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, looked up once per device (with that device current)
+// and cached. Returns nullptr if the lookup fails.
+void* scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess) return nullptr;
+        g_scratch_addr[dev] = p;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int mamba_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                                      const void* C, const float* D, const void* z, const float* delta_bias,
+                                      int softplus_flag, void* y, float* final_state, int batch, int dim,
+                                      int seqlen, int dstate, int io_dtype, void* stream) {
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+                             io_dtype);
+    if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
+    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    if (need > kStaticScratchBytes) return MAMBA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (need > 0 && !(scratch = scratch_address())) return MAMBA_ERR_CUDA;
+    // Everything the kernels read from the scratch is written earlier in the
+    // same call (the packed B/C rows, padding rows included, and the row
+    // copies), so a previous call's contents need no clearing.
+    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
+                               seqlen, io_dtype, scratch, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" {
+
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A, const void* B, const void* C,
                        const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y, int batch,
                        int dim, int dstate, int io_dtype, void* stream) {
