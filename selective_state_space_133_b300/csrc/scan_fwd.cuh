@@ -254,21 +254,22 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     };
 
     // The recurrence is software-pipelined by one step: the loads, the ex2 of
-    // dt*A and dt*u*B of step t+1 are issued before the state update of step t,
-    // so their latencies overlap the dependent FMA chain of the previous step.
+    // dt*A and dt*u*B of step t+1 are issued before the state update of step t
+    // uses them. The next step's ex2 sit between the current step's C.h FMAs,
+    // so the MUFU and FMA pipes are fed alternately.
     auto recurrence = [&](const ScanStage<T>& S) {
         const float2* W = &sm.W[rc][0];
         const float* bc = &S.bc[0][0];
         float* P = &sm.P[rh * kPH + 4 * rc];
         float2 e[4], pb[4], cv[4];
-        auto front = [&](int t) {  // everything of step t that does not depend on h
-            const float2 w = W[t];
-            const float4 b0 = *reinterpret_cast<const float4*>(bc + t * kBCW + 8 * rh);
-            const float4 b1 = *reinterpret_cast<const float4*>(bc + t * kBCW + 8 * rh + 4);
-            const float4 c0 = *reinterpret_cast<const float4*>(bc + t * kBCW + kDState + 8 * rh);
-            const float4 c1 = *reinterpret_cast<const float4*>(bc + t * kBCW + kDState + 8 * rh + 4);
-            const float2 dd = make_float2(w.x, w.x);
-            const float2 du = make_float2(w.y, w.y);
+        // step 0's operands
+        {
+            const float2 w = W[0];
+            const float4 b0 = *reinterpret_cast<const float4*>(bc + 8 * rh);
+            const float4 b1 = *reinterpret_cast<const float4*>(bc + 8 * rh + 4);
+            const float4 c0 = *reinterpret_cast<const float4*>(bc + kDState + 8 * rh);
+            const float4 c1 = *reinterpret_cast<const float4*>(bc + kDState + 8 * rh + 4);
+            const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
             const float2 bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
                                   make_float2(b1.z, b1.w)};
             cv[0] = make_float2(c0.x, c0.y); cv[1] = make_float2(c0.z, c0.w);
@@ -279,25 +280,44 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 pb[i] = __fmul2_rn(du, bv[i]);
             }
-        };
-        front(0);
+        }
 #pragma unroll
         for (int t0 = 0; t0 < kTL; t0 += 4) {
             float p[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t = t0 + i;
-                float2 E[4], PB[4], CV[4];
+                const int tn = t + 1 < kTL ? t + 1 : t;  // the last step loads nothing new (values unused)
+                const float2 w = W[tn];
+                const float4 b0 = *reinterpret_cast<const float4*>(bc + tn * kBCW + 8 * rh);
+                const float4 b1 = *reinterpret_cast<const float4*>(bc + tn * kBCW + 8 * rh + 4);
+                const float4 c0 = *reinterpret_cast<const float4*>(bc + tn * kBCW + kDState + 8 * rh);
+                const float4 c1 = *reinterpret_cast<const float4*>(bc + tn * kBCW + kDState + 8 * rh + 4);
+                const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
+                const float2 bn[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                      make_float2(b1.z, b1.w)};
+                const float2 cn[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
+                                      make_float2(c1.z, c1.w)};
+                // Written in an issue-friendly order (a warp issues in order):
+                // every result is consumed a few independent instructions later.
 #pragma unroll
-                for (int j = 0; j < 4; ++j) { E[j] = e[j]; PB[j] = pb[j]; CV[j] = cv[j]; }
-                if (t + 1 < kTL) front(t + 1);
+                for (int j = 0; j < 4; ++j) h[j] = __ffma2_rn(e[j], h[j], pb[j]);   // step t
+                float2 x[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) h[j] = __ffma2_rn(E[j], h[j], PB[j]);
-                float2 acc0 = __fmul2_rn(CV[0], h[0]);
-                float2 acc1 = __fmul2_rn(CV[1], h[1]);
-                acc0 = __ffma2_rn(CV[2], h[2], acc0);
-                acc1 = __ffma2_rn(CV[3], h[3], acc1);
-                const float2 acc = __fadd2_rn(acc0, acc1);
+                for (int j = 0; j < 4; ++j) x[j] = __fmul2_rn(dd, A2[j]);             // step t+1
+                float2 acc = __fmul2_rn(cv[0], h[0]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (t + 1 < kTL) e[j] = make_float2(ex2_approx(x[j].x), ex2_approx(x[j].y));
+                    if (j < 3) acc = __ffma2_rn(cv[j + 1], h[j + 1], acc);
+                }
+                if (t + 1 < kTL) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        pb[j] = __fmul2_rn(du, bn[j]);
+                        cv[j] = cn[j];
+                    }
+                }
                 p[i] = acc.x + acc.y;
             }
             *reinterpret_cast<float4*>(P + (t0 / 4) * kPJ) = make_float4(p[0], p[1], p[2], p[3]);
