@@ -54,8 +54,12 @@ class Oracle:
         self.lib = ctypes.CDLL(path)
         self.lib.oracle_scan.restype = ctypes.c_int
         self.lib.oracle_scan.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                         _P, _P, _P, _P, _P, _P, _P, _P, _PI,
+                                         _P, _P, _P, _P, _P, _P, _P, _P, _PI, _P,
                                          ctypes.c_int, _P, _P]
+        self.lib.oracle_scan_bwd.restype = ctypes.c_int
+        self.lib.oracle_scan_bwd.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             _P, _P, _P, _P, _P, _P, _P, _P, _PI, _P,
+                                             ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
         self.lib.oracle_state_update.restype = ctypes.c_int
         self.lib.oracle_state_update.argtypes = [ctypes.c_int64, ctypes.c_int64, _P,
                                                  _P, _P, _P, _P, _P, _P, _P, _P, _PI,
@@ -63,11 +67,12 @@ class Oracle:
 
     # -- scan ---------------------------------------------------------------
     def scan(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-             rows=None, return_state=True):
+             rows=None, return_state=True, h0=None):
         """Selective scan of the rows ``rows`` (flat indices b*dim + d; all rows if None).
 
         u, delta, z : (batch, dim, L);  B, C : (batch, N, L);  A : (dim, N);
-        D, delta_bias : (dim,). Any float dtype (bf16 torch tensors included) is
+        D, delta_bias : (dim,); h0 : (batch, dim, N) state before the first step,
+        or None for zero. Any float dtype (bf16 torch tensors included) is
         widened exactly to float64 first.
         Returns y of shape (len(rows), L) and, if asked, the final state
         (len(rows), N), both float64.
@@ -86,14 +91,60 @@ class Oracle:
         Bf = np.ascontiguousarray(_f64(B))
         Cf = np.ascontiguousarray(_f64(C))
         assert Bf.shape == (batch, N, L) and Cf.shape == (batch, N, L)
+        hr0 = None if h0 is None else _gather_rows(h0, rows, batch * dim, N)
         y = np.empty((len(rows), L), np.float64)
         h = np.empty((len(rows), N), np.float64) if return_state else None
         rc = self.lib.oracle_scan(len(rows), L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar),
-                                  _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf), _iptr(b_idx),
+                                  _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0),
                                   int(bool(softplus)), _ptr(y), _ptr(h))
         if rc != 0:
             raise ValueError(f"oracle_scan rejected dstate={N}")
         return (y, h) if return_state else y
+
+    # -- gradients ------------------------------------------------------------
+    def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+                 dy=None, h0=None):
+        """Gradients of L = sum(dy * y) for the scan of all rows.
+
+        Same inputs as ``scan`` plus dy (batch, dim, L). Returns a dict of float64
+        arrays: du, ddelta (batch, dim, L); dz (batch, dim, L) or None; dA (dim, N);
+        dB, dC (batch, N, L); dD, ddelta_bias (dim,) or None; dh0 (batch, dim, N).
+        The C code returns per-row contributions; here they are summed over the
+        batch rows (dA, dD, ddelta_bias) and over the channels of a batch row
+        (dB, dC).
+        """
+        batch, dim, L = u.shape
+        N = _f64(A).shape[1]
+        R = batch * dim
+        rows = np.arange(R, dtype=np.int64)
+        b_idx = np.ascontiguousarray(rows // dim)
+        d_idx = rows % dim
+        ur = _gather_rows(u, rows, R, L)
+        dr = _gather_rows(delta, rows, R, L)
+        zr = None if z is None else _gather_rows(z, rows, R, L)
+        gy = _gather_rows(dy, rows, R, L)
+        Ar = np.ascontiguousarray(_f64(A)[d_idx])
+        Dr = None if D is None else np.ascontiguousarray(_f64(D)[d_idx])
+        br = None if delta_bias is None else np.ascontiguousarray(_f64(delta_bias)[d_idx])
+        hr0 = None if h0 is None else _gather_rows(h0, rows, R, N)
+        Bf = np.ascontiguousarray(_f64(B))
+        Cf = np.ascontiguousarray(_f64(C))
+        du = np.empty((R, L)); dd = np.empty((R, L)); dz = None if z is None else np.empty((R, L))
+        dA = np.empty((R, N)); dD = np.empty(R); db = np.empty(R)
+        dB = np.empty((R, N, L)); dC = np.empty((R, N, L)); dh0 = np.empty((R, N))
+        rc = self.lib.oracle_scan_bwd(R, L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar), _ptr(Dr), _ptr(br),
+                                      _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0), int(bool(softplus)),
+                                      _ptr(gy), _ptr(du), _ptr(dd), _ptr(dz), _ptr(dA), _ptr(dD), _ptr(db),
+                                      _ptr(dB), _ptr(dC), _ptr(dh0))
+        if rc != 0:
+            raise ValueError(f"oracle_scan_bwd failed ({rc})")
+        return dict(du=du.reshape(batch, dim, L), ddelta=dd.reshape(batch, dim, L),
+                    dz=None if dz is None else dz.reshape(batch, dim, L),
+                    dA=dA.reshape(batch, dim, N).sum(axis=0),
+                    dB=dB.reshape(batch, dim, N, L).sum(axis=1), dC=dC.reshape(batch, dim, N, L).sum(axis=1),
+                    dD=None if D is None else dD.reshape(batch, dim).sum(axis=0),
+                    ddelta_bias=None if delta_bias is None else db.reshape(batch, dim).sum(axis=0),
+                    dh0=dh0.reshape(batch, dim, N))
 
     # -- state update ---------------------------------------------------------
     def state_update(self, state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
@@ -176,6 +227,10 @@ def default() -> Oracle:
 
 def scan(*args, **kwargs):
     return default().scan(*args, **kwargs)
+
+
+def scan_bwd(*args, **kwargs):
+    return default().scan_bwd(*args, **kwargs)
 
 
 def state_update(*args, **kwargs):

@@ -31,6 +31,7 @@
  * function as log(1 + exp(x)) for every x but does not overflow for large x.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -75,6 +76,9 @@ static double ssm_step(double* h, int64_t dstate, const double* A_row,
  *   A           : (nrows, dstate)        the A row of each row's channel
  *   Dskip, bias : (nrows)                either may be NULL
  *   B, C        : (nbatch, dstate, seqlen), row r uses batch bidx[r]
+ *   h0          : (nrows, dstate) state before the first step, or NULL for
+ *                 zero (a scan that continues an earlier one, "mamba->jamba"
+ *                 §2.2: the recurrence carries h from one token to the next)
  *   y           : (nrows, seqlen) out
  *   hlast       : (nrows, dstate) out, may be NULL: state after the last step
  * Returns 0, or -1 if dstate is out of range.
@@ -83,14 +87,14 @@ int oracle_scan(int64_t nrows, int64_t seqlen, int64_t dstate,
                 const double* u, const double* delta, const double* z,
                 const double* A, const double* Dskip, const double* bias,
                 const double* B, const double* C, const int64_t* bidx,
-                int softplus_flag, double* y, double* hlast)
+                const double* h0, int softplus_flag, double* y, double* hlast)
 {
     double h[1024];
     if (dstate < 1 || dstate > 1024) return -1;
     for (int64_t r = 0; r < nrows; ++r) {
         const double* Bb = B + bidx[r] * dstate * seqlen;
         const double* Cb = C + bidx[r] * dstate * seqlen;
-        for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) h[n] = h0 ? h0[r * dstate + n] : 0.0;
         for (int64_t l = 0; l < seqlen; ++l) {
             int64_t i = r * seqlen + l;
             y[i] = ssm_step(h, dstate, A + r * dstate, Bb + l, Cb + l, seqlen,
@@ -127,5 +131,106 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
                         Dskip ? Dskip + r : NULL, bias ? bias + r : NULL,
                         softplus_flag);
     }
+    return 0;
+}
+
+/*
+ * Gradients of the scan (reverse-mode differentiation of the loop above, the
+ * backward pass "mamba->jamba" §2.3 describes: A_bar and B_bar are recomputed
+ * from the inputs, here by storing the forward states of the row).
+ *
+ * With the loss L = sum_l dy[l] * y[l], per row:
+ *   gate      : y = p * silu(z), p = C.h + D u; dp = dy silu(z),
+ *               dz = dy * p * silu'(z), silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   readout   : dC[n][l] = dp h_l[n];  dD += dp u;  du += dp D;  gh[n] = g[n] + dp C[n]
+ *   recurrence h_l = e h_{l-1} + dt u B, e = exp(dt A):
+ *               dB[n][l] = gh[n] dt u;  d(dt u) += gh[n] B[n];
+ *               de = gh[n] h_{l-1}[n]:  d(dt) += de e A[n],  dA[n] += de e dt;
+ *               g[n] = gh[n] e          (the gradient reaching h_{l-1})
+ *   dt u      : du += d(dt u) dt;  d(dt) += d(dt u) u
+ *   dt        : ddelta = d(dt) * sigmoid(delta + bias) with softplus, else d(dt);
+ *               dbias += ddelta
+ *   dh0 = g after step 0.
+ * Outputs per row (the caller sums dA/dD/dbias over batch rows and dB/dC over
+ * the channels of a batch row):
+ *   du, ddelta, dz : (nrows, seqlen)          dz written only if z given
+ *   dA             : (nrows, dstate)
+ *   dD, dbias      : (nrows), either may be NULL
+ *   dB, dC         : (nrows, dstate, seqlen)
+ *   dh0            : (nrows, dstate), may be NULL
+ * h0 as in oracle_scan. Returns 0, -1 if dstate is out of range, -2 if the
+ * work buffer cannot be allocated.
+ */
+int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
+                    const double* u, const double* delta, const double* z,
+                    const double* A, const double* Dskip, const double* bias,
+                    const double* B, const double* C, const int64_t* bidx,
+                    const double* h0, int softplus_flag, const double* dy,
+                    double* du, double* ddelta, double* dz, double* dA,
+                    double* dD, double* dbias, double* dB, double* dC, double* dh0)
+{
+    if (dstate < 1 || dstate > 1024) return -1;
+    /* H[(l + 1) * dstate + n] = state after step l; H[n] = state before step 0 */
+    double* H = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * (size_t)dstate);
+    if (!H) return -2;
+    double g[1024];
+    for (int64_t r = 0; r < nrows; ++r) {
+        const double* Bb = B + bidx[r] * dstate * seqlen;
+        const double* Cb = C + bidx[r] * dstate * seqlen;
+        const double* Ar = A + r * dstate;
+        const double Dr = Dskip ? Dskip[r] : 0.0;
+        for (int64_t n = 0; n < dstate; ++n) H[n] = h0 ? h0[r * dstate + n] : 0.0;
+        /* forward: states of every step */
+        for (int64_t l = 0; l < seqlen; ++l) {
+            const int64_t i = r * seqlen + l;
+            double dt = delta[i] + (bias ? bias[r] : 0.0);
+            if (softplus_flag) dt = softplus_ref(dt);
+            for (int64_t n = 0; n < dstate; ++n)
+                H[(l + 1) * dstate + n] = exp(dt * Ar[n]) * H[l * dstate + n] + dt * Bb[n * seqlen + l] * u[i];
+        }
+        /* reverse */
+        for (int64_t n = 0; n < dstate; ++n) { g[n] = 0.0; dA[r * dstate + n] = 0.0; }
+        double dDr = 0.0, dbr = 0.0;
+        for (int64_t l = seqlen - 1; l >= 0; --l) {
+            const int64_t i = r * seqlen + l;
+            const double x = delta[i] + (bias ? bias[r] : 0.0);
+            const double dt = softplus_flag ? softplus_ref(x) : x;
+            const double* hl = H + (l + 1) * dstate;
+            const double* hp = H + l * dstate;
+            double p = Dr * u[i];
+            for (int64_t n = 0; n < dstate; ++n) p += Cb[n * seqlen + l] * hl[n];
+            double dp = dy[i];
+            if (z) {
+                const double s = 1.0 / (1.0 + exp(-z[i]));
+                dz[i] = dy[i] * p * s * (1.0 + z[i] * (1.0 - s));
+                dp = dy[i] * z[i] * s;
+            }
+            dDr += dp * u[i];
+            double dui = dp * Dr;
+            double ddtu = 0.0, ddt = 0.0;
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double e = exp(dt * Ar[n]);
+                const double gh = g[n] + dp * Cb[n * seqlen + l];
+                dC[(r * dstate + n) * seqlen + l] = dp * hl[n];
+                dB[(r * dstate + n) * seqlen + l] = gh * dt * u[i];
+                ddtu += gh * Bb[n * seqlen + l];
+                const double de = gh * hp[n];
+                ddt += de * e * Ar[n];
+                dA[r * dstate + n] += de * e * dt;
+                g[n] = gh * e;
+            }
+            dui += ddtu * dt;
+            ddt += ddtu * u[i];
+            const double dx = softplus_flag ? ddt / (1.0 + exp(-x)) : ddt;
+            du[i] = dui;
+            ddelta[i] = dx;
+            dbr += dx;
+        }
+        if (dD) dD[r] = dDr;
+        if (dbias) dbias[r] = dbr;
+        if (dh0)
+            for (int64_t n = 0; n < dstate; ++n) dh0[r * dstate + n] = g[n];
+    }
+    free(H);
     return 0;
 }

@@ -25,9 +25,9 @@ MUTANTS = {
     "bias added after softplus": ("if (biasp) dt += *biasp;\n    if (softplus_flag) dt = softplus_ref(dt);",
                                   "if (softplus_flag) dt = softplus_ref(dt);\n    if (biasp) dt += *biasp;"),
     "softplus missing log1p": ("log1p(exp(-ax))", "exp(-ax)"),
-    "state not zeroed": ("h[n] = 0.0;", "h[n] = 0.5;"),
-    "state carried across rows": ("for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0;",
-                                  "if (r == 0) for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0;"),
+    "state not zeroed": ("h[n] = h0 ? h0[r * dstate + n] : 0.0;", "h[n] = h0 ? h0[r * dstate + n] : 0.5;"),
+    "state carried across rows": ("for (int64_t n = 0; n < dstate; ++n) h[n] = h0 ? h0[r * dstate + n] : 0.0;",
+                                  "if (r == 0) for (int64_t n = 0; n < dstate; ++n) h[n] = h0 ? h0[r * dstate + n] : 0.0;"),
 }
 
 
