@@ -105,8 +105,14 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A,
 size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype);
 
 /*
- * mamba_scan_fwd with a caller-provided workspace: same arguments, semantics
- * and checks, plus
+ * mamba_scan_fwd with a caller-provided workspace and an optional initial
+ * state: same arguments, semantics and checks, plus
+ *   initial_state   : (batch, dim, dstate) fp32, 16-byte aligned, or NULL for
+ *                     zero: the state before the first step, so that a long
+ *                     sequence can be scanned in pieces, each piece starting
+ *                     from the previous piece's final_state ("mamba->jamba"
+ *                     §2.2: the recurrence carries h from token to token);
+ *                     with seqlen == 0, final_state receives it unchanged
  *   workspace       : device buffer, 256-byte aligned, owned by the caller, of
  *                     at least mamba_scan_workspace_size(...) bytes (may be NULL
  *                     when that size is 0); its contents are scratch, needed
@@ -119,6 +125,7 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       const void* B, const void* C,
                       const float* D, const void* z,
                       const float* delta_bias, int softplus_flag,
+                      const float* initial_state,
                       void* y, float* final_state,
                       int batch, int dim, int seqlen, int dstate,
                       int io_dtype, void* workspace, size_t workspace_bytes,

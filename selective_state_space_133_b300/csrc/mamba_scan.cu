@@ -144,7 +144,8 @@ extern "C" {
 // Argument checks shared by the scan entry points (MAMBA_OK or the error code).
 static int check_scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
                            const float* D, const void* z, const float* delta_bias, const void* y,
-                           const float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype) {
+                           const float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype,
+                           const float* initial_state = nullptr) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate != kDState) return MAMBA_ERR_SHAPE;
     if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
@@ -158,7 +159,7 @@ static int check_scan_args(const void* u, const void* delta, const float* A, con
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!A) return MAMBA_ERR_NULL;
     if (seqlen > 0 && (!u || !delta || !B || !C || !y)) return MAMBA_ERR_NULL;
-    const void* p16[] = {u, delta, z, B, C, y, A, final_state};
+    const void* p16[] = {u, delta, z, B, C, y, A, final_state, initial_state};
     for (const void* p : p16)
         if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
     if ((D && !aligned(D, 4)) || (delta_bias && !aligned(delta_bias, 4))) return MAMBA_ERR_ALIGN;
@@ -168,9 +169,9 @@ static int check_scan_args(const void* u, const void* delta, const float* A, con
 static int scan_with_workspace(const void* u, const void* delta, const float* A, const void* B, const void* C,
                                const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
                                float* final_state, int batch, int dim, int seqlen, int io_dtype, void* workspace,
-                               cudaStream_t s) {
+                               cudaStream_t s, const float* initial_state = nullptr) {
     mscan::ScanArgs a;
-    a.A = A; a.D = D; a.bias = delta_bias; a.y = y; a.final_state = final_state;
+    a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state; a.y = y; a.final_state = final_state;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
     char* ws = static_cast<char*>(workspace);
     const int sp = softplus_flag != 0;
@@ -185,11 +186,11 @@ size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int
 }
 
 int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                      const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
-                      float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+                      const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                      const float* initial_state, void* y, float* final_state, int batch, int dim, int seqlen,
+                      int dstate, int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
-                             io_dtype);
+                             io_dtype, initial_state);
     if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
     const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
     if (need > 0) {
@@ -198,7 +199,7 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const vo
         if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
     }
     return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream));
+                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state);
 }
 
 int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,

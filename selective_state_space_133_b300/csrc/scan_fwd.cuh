@@ -66,6 +66,7 @@ struct ScanArgs {
     const float* A;
     const float* D;      // may be null
     const float* bias;   // may be null
+    const float* h0;     // state before the first step, may be null (zero)
     void* y;
     float* final_state;  // may be null
     int batch, dim, seqlen;
@@ -197,8 +198,16 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
     }
     float2 h[4];
+    if (a.h0) {
+        const float4* hp = reinterpret_cast<const float4*>(a.h0 + (static_cast<size_t>(b) * a.dim + rd) * kDState +
+                                                           8 * rh);
+        const float4 p0 = hp[0], p1 = hp[1];
+        h[0] = make_float2(p0.x, p0.y); h[1] = make_float2(p0.z, p0.w);
+        h[2] = make_float2(p1.x, p1.y); h[3] = make_float2(p1.z, p1.w);
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
+    }
 
     const int ed = d0 + ec;
     const bool eactive = ed < a.dim;

@@ -48,7 +48,7 @@ def workspace_bytes(batch: int, dim: int, seqlen: int, dtype: torch.dtype, dstat
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                   y=None, final_state=None, stream=None, workspace=None):
+                   y=None, final_state=None, stream=None, workspace=None, initial_state=None):
     """Selective scan (see include/mamba_scan.h, mamba_scan_fwd_ws).
 
     u, delta, z: (batch, dim, L); B, C: (batch, 16, L), all fp32 or all bf16;
@@ -56,6 +56,8 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     preallocated (batch, dim, 16) fp32 tensor, or True to allocate one.
     ``workspace`` may be a uint8 CUDA tensor of at least ``workspace_bytes(...)``
     bytes; otherwise one is taken from torch's caching allocator.
+    ``initial_state``: (batch, dim, 16) fp32 state before the first step, or None
+    for zero (continuing an earlier scan from its final state).
     Returns y, or (y, final_state) when a final state was requested.
     """
     if u.dtype not in _IO:
@@ -82,6 +84,7 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     elif final_state is False:
         final_state = None
     _need(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    _need(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
     lib = _lib.lib()
     need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[u.dtype]))
     if workspace is None:
@@ -90,7 +93,7 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     st = lib.mamba_scan_fwd_ws(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(y), _ptr(final_state), batch, dim, L, N, _IO[u.dtype],
+        int(bool(softplus)), _ptr(initial_state), _ptr(y), _ptr(final_state), batch, dim, L, N, _IO[u.dtype],
         _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_fwd")
     return (y, final_state) if want_state else y

@@ -169,3 +169,48 @@ def test_allocating_entry_point_through_the_c_abi():
     assert st == 0
     ops.check_device_error()
     assert torch.equal(y, y_ref) and torch.equal(h, h_ref)
+
+
+@pytest.mark.parametrize("dtype,L", [(torch.bfloat16, 96), (torch.float32, 45), (torch.bfloat16, 203)])
+def test_initial_state_parity(dtype, L):
+    x = syn.scan_inputs(2, 24, L, dtype, seed=50 + L)
+    h0 = torch.randn(2, 24, 16, generator=torch.Generator().manual_seed(L)) * 0.5
+    d = to_dev(x)
+    y, h = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                              d["softplus"], final_state=True, initial_state=h0.cuda())
+    ops.check_device_error()
+    yr, hr = oracle.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                         x["softplus"], h0=h0)
+    tol = TOL[str(dtype).replace("torch.", "")]
+    assert max_rel_err(y.double().cpu().numpy().reshape(-1, L), yr) <= tol
+    assert max_rel_err(h.cpu().numpy().reshape(-1, 16), hr) <= tol
+
+
+def test_scan_in_two_pieces_equals_whole():
+    L1, L2 = 64, 80
+    x = syn.scan_inputs(2, 32, L1 + L2, torch.float32, seed=61)
+    d = to_dev(x)
+    y, h = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                              d["softplus"], final_state=True)
+    part = lambda t, a, b: t[..., a:b].contiguous()
+    y1, h1 = ops.mamba_scan_fwd(part(d["u"], 0, L1), part(d["delta"], 0, L1), d["A"], part(d["B"], 0, L1),
+                                part(d["C"], 0, L1), d["D"], part(d["z"], 0, L1), d["delta_bias"], d["softplus"],
+                                final_state=True)
+    y2, h2 = ops.mamba_scan_fwd(part(d["u"], L1, None), part(d["delta"], L1, None), d["A"], part(d["B"], L1, None),
+                                part(d["C"], L1, None), d["D"], part(d["z"], L1, None), d["delta_bias"],
+                                d["softplus"], final_state=True, initial_state=h1)
+    ops.check_device_error()
+    L = L1 + L2
+    yy = torch.cat([y1, y2], dim=2).double().cpu().numpy().reshape(-1, L)
+    assert max_rel_err(yy, y.double().cpu().numpy().reshape(-1, L)) <= 1e-5
+    assert max_rel_err(h2.cpu().numpy().reshape(-1, 16), h.cpu().numpy().reshape(-1, 16)) <= 1e-5
+
+
+def test_zero_length_keeps_initial_state():
+    x = syn.scan_inputs(2, 20, 0, torch.bfloat16, seed=1)
+    d = to_dev(x)
+    h0 = torch.randn(2, 20, 16, device="cuda")
+    y, h = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                              d["softplus"], final_state=True, initial_state=h0)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h0)
