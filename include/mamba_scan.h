@@ -132,6 +132,49 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       void* stream);
 
 /*
+ * Bytes of device workspace mamba_scan_bwd needs for these sizes (0 when there
+ * is nothing to compute or an argument is out of range): the packed fp32 B/C
+ * rows (batch * roundup(seqlen, 16) * 128 bytes), one fp32 state per row per
+ * 16 steps (batch * dim * roundup(seqlen, 16) * 4 bytes) and fp32 sums of dB
+ * and dC (batch * roundup(seqlen, 16) * 128 bytes).
+ */
+size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype);
+
+/*
+ * Backward of the selective scan (training): the gradients of
+ * L = sum(dy * y), y the output of mamba_scan_fwd_ws with the same inputs,
+ * with respect to every input. The states are recomputed from the inputs, as
+ * "mamba->jamba" (blog.csdn.net) §2.3 describes for the backward pass, keeping
+ * one fp32 state per row every 16 steps in the workspace in between.
+ * Inputs: as mamba_scan_fwd_ws (u, delta, A, B, C, D, z, delta_bias,
+ * softplus_flag, initial_state), plus
+ *   dy              : (batch, dim, seqlen) io_dtype, the gradient reaching y
+ * Outputs (device, caller-owned, overwritten; 16-byte aligned except dD and
+ * ddelta_bias, 4-byte):
+ *   du, ddelta      : (batch, dim, seqlen) io_dtype
+ *   dz              : (batch, dim, seqlen) io_dtype; required iff z is given
+ *   dA              : (dim, dstate) fp32, summed over the batch
+ *   dB, dC          : (batch, dstate, seqlen) io_dtype, summed over the channels
+ *   dD              : (dim) fp32 or NULL (NULL required when D is NULL)
+ *   ddelta_bias     : (dim) fp32 or NULL (NULL required when delta_bias is NULL)
+ *   dinitial_state  : (batch, dim, dstate) fp32 or NULL; the gradient reaching
+ *                     the state before the first step (zeros when seqlen == 0)
+ * workspace/workspace_bytes as for mamba_scan_fwd_ws, sized by
+ * mamba_scan_bwd_workspace_size. dA, dB, dC, dD and ddelta_bias are sums of
+ * fp32 atomic additions, so their last bits may vary from run to run.
+ * Returns MAMBA_OK or a negative mamba_status.
+ */
+int mamba_scan_bwd(const void* u, const void* delta, const float* A,
+                   const void* B, const void* C,
+                   const float* D, const void* z,
+                   const float* delta_bias, int softplus_flag,
+                   const float* initial_state, const void* dy,
+                   void* du, void* ddelta, float* dA, void* dB, void* dC,
+                   float* dD, void* dz, float* ddelta_bias, float* dinitial_state,
+                   int batch, int dim, int seqlen, int dstate, int io_dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * mamba_scan_fwd without any allocation and without a caller workspace.
  * The pages have no counterpart to this call: it exists for callers that
  * cannot allocate device memory at call time (serving loops that reserve all

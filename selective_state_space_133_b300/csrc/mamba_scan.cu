@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "../../include/mamba_scan.h"
+#include "scan_bwd.cuh"
 #include "scan_fwd.cuh"
 #include "state_update.cuh"
 
@@ -132,6 +133,65 @@ template <typename T>
 int launch_update(const mscan::UpdateArgs& a, cudaStream_t stream) {
     const dim3 grid((a.dim + mscan::kUpdateCh - 1) / mscan::kUpdateCh, a.batch);
     mscan::state_update_kernel<T><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+// Workspace of one backward call: packed B/C rows, one fp32 state per row per
+// 16-step chunk, and the fp32 sums of dB and dC.
+struct BwdWorkspace {
+    int Lp, n;
+    size_t bc, hck, dbc, total;
+};
+
+BwdWorkspace bwd_workspace(long long batch, long long dim, long long L) {
+    BwdWorkspace w;
+    w.Lp = static_cast<int>(round_up(static_cast<size_t>(L), mscan::kBwdTL));
+    w.n = w.Lp / mscan::kBwdTL;
+    w.bc = 0;
+    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * 32 * sizeof(float), 256);
+    w.hck = off;
+    off += round_up(static_cast<size_t>(batch) * dim * w.n * kDState * sizeof(float), 256);
+    w.dbc = off;
+    off += round_up(static_cast<size_t>(batch) * 2 * kDState * w.Lp * sizeof(float), 256);
+    w.total = L > 0 ? off : 0;
+    return w;
+}
+
+template <typename T>
+int launch_bwd(mscan::ScanBwdArgs a, const void* B, const void* C, void* dB, void* dC, char* ws,
+               cudaStream_t stream) {
+    const BwdWorkspace w = bwd_workspace(a.batch, a.dim, a.seqlen);
+    a.Lp = w.Lp;
+    if (cudaMemsetAsync(a.dA, 0, static_cast<size_t>(a.dim) * kDState * sizeof(float), stream) != cudaSuccess)
+        return MAMBA_ERR_CUDA;
+    if (a.dD && cudaMemsetAsync(a.dD, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (a.dbias && cudaMemsetAsync(a.dbias, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (a.seqlen > 0) {
+        a.bc = reinterpret_cast<const float*>(ws + w.bc);
+        a.hck = reinterpret_cast<float*>(ws + w.hck);
+        a.dbc = reinterpret_cast<float*>(ws + w.dbc);
+        if (cudaMemsetAsync(a.dbc, 0, static_cast<size_t>(a.batch) * 2 * kDState * w.Lp * sizeof(float), stream) !=
+            cudaSuccess)
+            return MAMBA_ERR_CUDA;
+        const long long pack_threads = static_cast<long long>(a.batch) * w.Lp;
+        mscan::bc_pack_kernel<T><<<static_cast<unsigned>((pack_threads + 255) / 256), 256, 0, stream>>>(
+            static_cast<const T*>(B), static_cast<const T*>(C), const_cast<float*>(a.bc), a.batch, a.seqlen, w.Lp);
+    }
+    const dim3 grid((a.dim + mscan::kBwdCh - 1) / mscan::kBwdCh, a.batch);
+    const bool z = a.z != nullptr;
+    if (a.softplus) {
+        if (z) mscan::scan_bwd_kernel<T, true, true><<<grid, 32, 0, stream>>>(a);
+        else   mscan::scan_bwd_kernel<T, true, false><<<grid, 32, 0, stream>>>(a);
+    } else {
+        if (z) mscan::scan_bwd_kernel<T, false, true><<<grid, 32, 0, stream>>>(a);
+        else   mscan::scan_bwd_kernel<T, false, false><<<grid, 32, 0, stream>>>(a);
+    }
+    if (a.seqlen > 0) {
+        const long long total = static_cast<long long>(a.batch) * 2 * kDState * a.seqlen;
+        const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 148ll * 32));
+        mscan::dbc_unpack_kernel<T><<<blocks, 256, 0, stream>>>(a.dbc, static_cast<T*>(dB), static_cast<T*>(dC),
+                                                               a.batch, a.seqlen, w.Lp);
+    }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
@@ -276,6 +336,47 @@ extern "C" int mamba_scan_fwd_noalloc(const void* u, const void* delta, const fl
 }
 
 extern "C" {
+
+size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype) {
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate != kDState) return 0;
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return 0;
+    return bwd_workspace(batch, dim, seqlen).total;
+}
+
+int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                   const void* z, const float* delta_bias, int softplus_flag, const float* initial_state,
+                   const void* dy, void* du, void* ddelta, float* dA, void* dB, void* dC, float* dD, void* dz,
+                   float* ddelta_bias, float* dinitial_state, int batch, int dim, int seqlen, int dstate,
+                   int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, dy, nullptr, batch, dim, seqlen, dstate, io_dtype,
+                             initial_state);
+    if (st != MAMBA_OK) return st;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+    if (!dA) return MAMBA_ERR_NULL;
+    if (seqlen > 0 && (!du || !ddelta || !dB || !dC)) return MAMBA_ERR_NULL;
+    if (z && seqlen > 0 && !dz) return MAMBA_ERR_NULL;
+    if ((dD && !D) || (ddelta_bias && !delta_bias)) return MAMBA_ERR_NULL;  // a gradient of an absent input
+    const void* p16[] = {du, ddelta, dA, dB, dC, dz, dinitial_state};
+    for (const void* p : p16)
+        if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
+    if ((dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4))) return MAMBA_ERR_ALIGN;
+    const size_t need = bwd_workspace(batch, dim, seqlen).total;
+    if (need > 0) {
+        if (!workspace) return MAMBA_ERR_NULL;
+        if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
+    }
+    mscan::ScanBwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.u = u; a.delta = delta; a.z = z; a.dy = dy; a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state;
+    a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr; a.dA = dA; a.dD = dD; a.dbias = ddelta_bias;
+    a.dh0 = dinitial_state;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = softplus_flag != 0;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return io_dtype == MAMBA_BF16 ? launch_bwd<__nv_bfloat16>(a, B, C, dB, dC, ws, s)
+                                  : launch_bwd<float>(a, B, C, dB, dC, ws, s);
+}
 
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A, const void* B, const void* C,
                        const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y, int batch,

@@ -99,6 +99,49 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     return (y, final_state) if want_state else y
 
 
+def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
+                   initial_state=None, want_initial_state_grad=False, stream=None, workspace=None):
+    """Gradients of sum(dy * y) for the scan (see include/mamba_scan.h, mamba_scan_bwd).
+
+    Inputs as mamba_scan_fwd plus dy (batch, dim, L) in the I/O dtype. Returns a
+    dict with du, ddelta, dz (or None), dA (dim, 16) fp32, dB, dC (batch, 16, L),
+    dD and ddelta_bias (dim,) fp32 (or None when the input is absent) and dh0
+    (batch, dim, 16) fp32 when ``want_initial_state_grad``.
+    """
+    if u.dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {u.dtype}")
+    dev = u.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_scan_bwd runs on CUDA tensors only")
+    batch, dim, L = u.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    for name, t in (("u", u), ("delta", delta), ("z", z), ("dy", dy)):
+        _need(t, name, u.dtype, (batch, dim, L), dev)
+    _need(B, "B", u.dtype, (batch, N, L), dev)
+    _need(C, "C", u.dtype, (batch, N, L), dev)
+    _need(A, "A", torch.float32, (dim, N), dev)
+    _need(D, "D", torch.float32, (dim,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (dim,), dev)
+    _need(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    out = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u), dz=None if z is None else torch.empty_like(u),
+               dA=torch.empty((dim, N), dtype=torch.float32, device=dev),
+               dB=torch.empty_like(B), dC=torch.empty_like(C),
+               dD=None if D is None else torch.empty((dim,), dtype=torch.float32, device=dev),
+               ddelta_bias=None if delta_bias is None else torch.empty((dim,), dtype=torch.float32, device=dev),
+               dh0=torch.empty((batch, dim, N), dtype=torch.float32, device=dev) if want_initial_state_grad else None)
+    lib = _lib.lib()
+    need = int(lib.mamba_scan_bwd_workspace_size(batch, dim, L, N, _IO[u.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.mamba_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
+        _ptr(initial_state), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
+        _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(out["dh0"]),
+        batch, dim, L, N, _IO[u.dtype], _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    _lib.check(st, "mamba_scan_bwd")
+    return out
+
+
 def mamba_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
                        softplus=False, y=None, stream=None):
     """One decode step in place on ``state`` (see include/mamba_scan.h, mamba_state_update).

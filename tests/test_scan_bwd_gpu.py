@@ -1,0 +1,79 @@
+"""GPU parity of the scan's backward (C ABI through the binding) against the fp64 oracle's gradients.
+
+Every gradient the library returns (du, ddelta, dz, dA, dB, dC, dD, the bias's
+gradient and the initial state's) is compared element by element with
+oracle.scan_bwd on the same inputs (the oracle widens the same bf16 values).
+Metric and gates as for the forward (tolerance.py): max relative error with an
+RMS floor, 1e-4 for fp32 I/O and 5e-3 for bf16 I/O. The bf16 gradients are
+rounded to bf16; the fp32 ones (dA, dD, bias, initial state) are fp32 sums
+of many terms added in an order that atomics decide.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_133_b300 import ops
+from selective_state_space_133_b300 import synthetic as syn
+from tolerance import TOL, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(batch, dim, L, dtype, seed, h0=True, **flags):
+    x = syn.scan_inputs(batch, dim, L, dtype, seed=seed, **flags)
+    g = torch.Generator().manual_seed(seed + 1)
+    dy = torch.randn(batch, dim, L, generator=g).to(dtype)
+    hinit = torch.randn(batch, dim, 16, generator=g) * 0.3 if h0 else None
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    out = ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy.cuda(), d["D"], d["z"],
+                             d["delta_bias"], d["softplus"],
+                             initial_state=None if hinit is None else hinit.cuda(), want_initial_state_grad=True)
+    ops.check_device_error()
+    ref = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                          x["softplus"], dy=dy, h0=hinit)
+    tol = TOL[str(dtype).replace("torch.", "")]
+    errs = {}
+    for name in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"):
+        r = ref[name]
+        o = out[name]
+        if r is None:
+            assert o is None, name
+            continue
+        got = o.double().cpu().numpy()
+        errs[name] = max_rel_err(got.reshape(r.shape).reshape(-1, r.shape[-1]) if r.ndim > 1 else got,
+                                 r.reshape(-1, r.shape[-1]) if r.ndim > 1 else r)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"gradients beyond {tol:.0e}: {bad} (all: {errs})"
+    return errs
+
+
+CASES = [
+    (2, 24, 96, torch.bfloat16, {}),
+    (1, 16, 45, torch.float32, {}),                       # ragged length: scalar loads and stores
+    (2, 33, 203, torch.bfloat16, {}),                     # ragged channels and length
+    (1, 16, 64, torch.float32, dict(with_z=False, with_D=False, softplus_in_kernel=False)),
+    (2, 40, 130, torch.float32, dict(a_noise=0.1)),
+    (4, 64, 1024, torch.bfloat16, dict(a_noise=0.1)),     # 64 chunks, 4 CTAs adding into each dB/dC entry
+]
+
+
+@pytest.mark.parametrize("batch,dim,L,dtype,flags", CASES, ids=lambda v: str(v) if not isinstance(v, dict) else
+                         ",".join(f"{k}={w}" for k, w in v.items()) or "default")
+def test_bwd_parity(batch, dim, L, dtype, flags):
+    run_case(batch, dim, L, dtype, seed=batch * 7 + dim + L, **flags)
+
+
+def test_bwd_without_initial_state():
+    run_case(2, 16, 80, torch.float32, seed=5, h0=False)
+
+
+def test_bwd_zero_length():
+    x = syn.scan_inputs(2, 20, 0, torch.float32, seed=1)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    dy = torch.empty(2, 20, 0, device="cuda")
+    out = ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"],
+                             True, want_initial_state_grad=True)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out["dA"]) == 0 and torch.count_nonzero(out["dD"]) == 0
+    assert torch.count_nonzero(out["ddelta_bias"]) == 0 and torch.count_nonzero(out["dh0"]) == 0
