@@ -1,6 +1,7 @@
 """Builds libmambascan.so in-tree with nvcc for sm_103a (no JIT, no torch extension)."""
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
@@ -9,7 +10,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBRARY = os.path.join(HERE, "libmambascan.so")
 SOURCES = [os.path.join(CSRC, "mamba_scan.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("common.cuh", "scan_fwd.cuh", "state_update.cuh")] + [
+# every source and header the library is built from: any change triggers a rebuild
+DEPENDS = SOURCES + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [
     os.path.join(os.path.dirname(HERE), "include", "mamba_scan.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

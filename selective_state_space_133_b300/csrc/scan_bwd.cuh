@@ -60,13 +60,13 @@ struct ScanBwdArgs {
 };
 
 struct ScanBwdSmem {
-    alignas(16) float2 W[kBwdCh][kBwdTL + 2];        // {dt, dt*u}
-    alignas(16) float SG[kBwdCh][kBwdTL + 4];        // d(dt)/d(delta + bias)
-    alignas(16) float DP[kBwdCh][kBwdTL + 4];        // dp = dy * silu(z)
-    alignas(16) float U[kBwdCh][kBwdTL + 4];         // u
-    alignas(16) float4 traj[kBwdTL][32][2];          // recomputed states, per step and lane (8 floats)
+    alignas(16) float2 W[kBwdCh][kBwdTL + 1];        // {dt, dt*u}; odd row pitch: distinct banks per channel
+    alignas(16) float SG[kBwdCh][kBwdTL + 1];        // d(dt)/d(delta + bias)
+    alignas(16) float DP[kBwdCh][kBwdTL + 1];        // dp = dy * silu(z)
+    alignas(16) float U[kBwdCh][kBwdTL + 1];         // u
+    alignas(16) float4 traj[kBwdTL][2][32];          // recomputed states: [step][half of the 8][lane]
     alignas(16) float P[2][kBwdTL / 4][kBwdCh * 4 + 8];  // partial C.h: [state half][4-step group][channel][4]
-    alignas(16) float2 Q[2][kBwdCh][kBwdTL + 1];     // partial {d(dtu), d(dt)} per state half
+    alignas(16) float2 Q[kBwdCh][kBwdTL + 1];        // {d(dtu), d(dt)} per (channel, step), both halves summed
     alignas(16) float RB[kBwdCh][36];                // one step's dB (cols 0..15) and dC (16..31) per channel
     alignas(16) float BC[kBwdTL][32];                // the chunk's packed B/C rows
 };
@@ -165,13 +165,13 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         const int l = k * kBwdTL + 8 * ej;
         ldg8(static_cast<const T*>(base) + erow * L + l, v, vec_ok && l + 8 <= L, eactive ? L - l : 0);
     };
-    // the chunk's packed B/C rows into shared memory (lane: half a step's row)
+    // the chunk's packed B/C rows (2 KB, contiguous) into shared memory: each
+    // 16-byte load and store of the warp covers 512 contiguous bytes
     auto stage_bc = [&](int k) {
-        const float4* src = reinterpret_cast<const float4*>(bcb + (static_cast<size_t>(k) * kBwdTL + (lane >> 1)) * 32 +
-                                                            16 * (lane & 1));
-        float4* dst = reinterpret_cast<float4*>(&sm.BC[lane >> 1][16 * (lane & 1)]);
+        const float4* src = reinterpret_cast<const float4*>(bcb + static_cast<size_t>(k) * kBwdTL * 32);
+        float4* dst = reinterpret_cast<float4*>(&sm.BC[0][0]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = src[j];
+        for (int j = 0; j < 4; ++j) dst[32 * j + lane] = src[32 * j + lane];
     };
     auto loadB = [&](int t, float2 (&v)[4]) {
         const float4 p0 = *reinterpret_cast<const float4*>(&sm.BC[t][8 * rh]);
@@ -242,6 +242,14 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
     for (int k = n - 1; k >= 0; --k) {
         const int l0 = k * kBwdTL;
         const int le = l0 + 8 * ej;  // first step of the pre-pass lane's eight
+        // the chunk's checkpoint (issued first: its latency overlaps the pre-pass)
+        float2 hs[4];
+        {
+            const float4* hp = reinterpret_cast<const float4*>(hck + k * kDState);
+            const float4 p0 = hp[0], p1 = hp[1];
+            hs[0] = make_float2(p0.x, p0.y); hs[1] = make_float2(p0.z, p0.w);
+            hs[2] = make_float2(p1.x, p1.y); hs[3] = make_float2(p1.z, p1.w);
+        }
         // (i) dt, dt*u, d(dt)/dx and u per (channel, step), into shared memory
         {
             float uv[8], dv[8];
@@ -265,13 +273,6 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         __syncwarp();
 
         // (ii) the chunk's states, recomputed from its checkpoint, and C.h
-        float2 hs[4];
-        {
-            const float4* hp = reinterpret_cast<const float4*>(hck + k * kDState);
-            const float4 p0 = hp[0], p1 = hp[1];
-            hs[0] = make_float2(p0.x, p0.y); hs[1] = make_float2(p0.z, p0.w);
-            hs[2] = make_float2(p1.x, p1.y); hs[3] = make_float2(p1.z, p1.w);
-        }
         {
             float2 hc[4] = {hs[0], hs[1], hs[2], hs[3]};
             float* Pw = &sm.P[rh][0][4 * rc];
@@ -289,8 +290,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         hc[j] = __ffma2_rn(ex2_pair(__fmul2_rn(dd, A2[j])), hc[j], __fmul2_rn(du, Bv[j]));
-                    sm.traj[t][lane][0] = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
-                    sm.traj[t][lane][1] = make_float4(hc[2].x, hc[2].y, hc[3].x, hc[3].y);
+                    sm.traj[t][0][lane] = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
+                    sm.traj[t][1][lane] = make_float4(hc[2].x, hc[2].y, hc[3].x, hc[3].y);
                     float2 acc = __fmul2_rn(Cv[0], hc[0]);
                     acc = __ffma2_rn(Cv[1], hc[1], acc);
                     acc = __ffma2_rn(Cv[2], hc[2], acc);
@@ -350,12 +351,12 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             loadB(t, Bv);
             loadC(t, Cv);
             {
-                const float4 q0 = sm.traj[t][lane][0], q1 = sm.traj[t][lane][1];
+                const float4 q0 = sm.traj[t][0][lane], q1 = sm.traj[t][1][lane];
                 hT[0] = make_float2(q0.x, q0.y); hT[1] = make_float2(q0.z, q0.w);
                 hT[2] = make_float2(q1.x, q1.y); hT[3] = make_float2(q1.z, q1.w);
             }
             if (t > 0) {
-                const float4 q0 = sm.traj[t - 1][lane][0], q1 = sm.traj[t - 1][lane][1];
+                const float4 q0 = sm.traj[t - 1][0][lane], q1 = sm.traj[t - 1][1][lane];
                 hP[0] = make_float2(q0.x, q0.y); hP[1] = make_float2(q0.z, q0.w);
                 hP[2] = make_float2(q1.x, q1.y); hP[3] = make_float2(q1.z, q1.w);
             } else {
@@ -377,7 +378,12 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                 dAacc[j] = __ffma2_rn(dee, dd, dAacc[j]);
                 g[j] = __fmul2_rn(gh, e);
             }
-            sm.Q[rh][rc][t] = make_float2(sdtu.x + sdtu.y, (sdt.x + sdt.y) * kLn2);
+            {   // both state halves of the channel: lanes rc and rc + 16
+                float qa = sdtu.x + sdtu.y, qb = sdt.x + sdt.y;
+                qa += __shfl_xor_sync(0xffffffffu, qa, 16);
+                qb += __shfl_xor_sync(0xffffffffu, qb, 16);
+                if (rh == 0) sm.Q[rc][t] = make_float2(qa, qb * kLn2);
+            }
             // channel sums of this step's dB and dC
             float4* rb = reinterpret_cast<float4*>(&sm.RB[rc][0]);
             rb[2 * rh] = make_float4(dBv[0].x, dBv[0].y, dBv[1].x, dBv[1].y);
@@ -385,10 +391,10 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             rb[4 + 2 * rh] = make_float4(dCv[0].x, dCv[0].y, dCv[1].x, dCv[1].y);
             rb[4 + 2 * rh + 1] = make_float4(dCv[2].x, dCv[2].y, dCv[3].x, dCv[3].y);
             __syncwarp();
-            float sacc = 0.f;
+            float2 sacc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < kBwdCh; ++c) sacc += sm.RB[c][lane];
-            accBC[ti] = sacc;
+            for (int c = 0; c < kBwdCh; c += 2) sacc = __fadd2_rn(sacc, make_float2(sm.RB[c][lane], sm.RB[c + 1][lane]));
+            accBC[ti] = sacc.x + sacc.y;
             __syncwarp();
           }
           red_add4(dcol + t0, make_float4(accBC[0], accBC[1], accBC[2], accBC[3]));
@@ -400,9 +406,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = 8 * ej + i;
-                const float2 q0 = sm.Q[0][ec][t], q1 = sm.Q[1][ec][t];
-                const float sdtu = q0.x + q1.x;
-                const float sdt = fmaf(sdtu, sm.U[ec][t], q0.y + q1.y);
+                const float2 q = sm.Q[ec][t];
+                const float sdtu = q.x;
+                const float sdt = fmaf(sdtu, sm.U[ec][t], q.y);
                 duv[i] = fmaf(sm.DP[ec][t], Dd, sdtu * sm.W[ec][t].x);
                 dxv[i] = le + i < L ? sdt * sm.SG[ec][t] : 0.f;
                 dbacc += dxv[i];

@@ -19,9 +19,18 @@ def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="scan_b8_d2048_l4096_bf16")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd")
     args = ap.parse_args()
     dev = torch.device("cuda", 0)
-    if args.workload in syn.SCAN_WORKLOADS:
+    if args.workload in syn.SCAN_WORKLOADS and args.pass_ == "bwd":
+        w = syn.SCAN_WORKLOADS[args.workload]
+        x = syn.workload_inputs(w)
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+        dy = torch.randn(w.batch, w.dim, w.seqlen, device=dev).to(w.dtype)
+        for _ in range(args.launches):
+            ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"],
+                               d["softplus"])
+    elif args.workload in syn.SCAN_WORKLOADS:
         w = syn.SCAN_WORKLOADS[args.workload]
         x = syn.workload_inputs(w)
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
