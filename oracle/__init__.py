@@ -56,6 +56,9 @@ class Oracle:
         self.lib.oracle_scan.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          _P, _P, _P, _P, _P, _P, _P, _P, _PI, _P,
                                          ctypes.c_int, _P, _P]
+        self.lib.oracle_causal_conv_silu.restype = ctypes.c_int
+        self.lib.oracle_causal_conv_silu.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                     _P, _P, _P, _P, _P]
         self.lib.oracle_scan_bwd.restype = ctypes.c_int
         self.lib.oracle_scan_bwd.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              _P, _P, _P, _P, _P, _P, _P, _P, _PI, _P,
@@ -100,6 +103,34 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_scan rejected dstate={N}")
         return (y, h) if return_state else y
+
+    # -- convolution before the scan -----------------------------------------
+    def causal_conv_silu(self, x, w, bias=None, xprev=None):
+        """u = silu(causal depthwise conv1d(x) + bias) for every (batch, channel) row.
+
+        x : (batch, dim, L);  w : (dim, width);  bias : (dim,) or None;
+        xprev : (batch, dim, width-1), the inputs before step 0 (oldest first),
+        or None for zeros. Returns u (batch, dim, L) float64.
+        """
+        batch, dim, L = x.shape
+        wf = _f64(w)
+        width = wf.shape[1]
+        R = batch * dim
+        xr = np.ascontiguousarray(_f64(x).reshape(R, L))
+        wr = np.ascontiguousarray(np.tile(wf, (batch, 1)))
+        br = None if bias is None else np.ascontiguousarray(np.tile(_f64(bias), batch))
+        pr = None if xprev is None else np.ascontiguousarray(_f64(xprev).reshape(R, width - 1))
+        u = np.empty((R, L))
+        rc = self.lib.oracle_causal_conv_silu(R, L, width, _ptr(xr), _ptr(wr), _ptr(br), _ptr(pr), _ptr(u))
+        if rc != 0:
+            raise ValueError(f"oracle_causal_conv_silu rejected width={width}")
+        return u.reshape(batch, dim, L)
+
+    def conv_scan(self, x, conv_w, conv_b, conv_state, delta, A, B, C, D=None, z=None, delta_bias=None,
+                  softplus=False, h0=None):
+        """The scan of u = silu(causal conv1d(x)): returns y (batch*dim, L) and the final state."""
+        u = self.causal_conv_silu(x, conv_w, conv_b, conv_state)
+        return self.scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0)
 
     # -- gradients ------------------------------------------------------------
     def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
@@ -227,6 +258,14 @@ def default() -> Oracle:
 
 def scan(*args, **kwargs):
     return default().scan(*args, **kwargs)
+
+
+def causal_conv_silu(*args, **kwargs):
+    return default().causal_conv_silu(*args, **kwargs)
+
+
+def conv_scan(*args, **kwargs):
+    return default().conv_scan(*args, **kwargs)
 
 
 def scan_bwd(*args, **kwargs):

@@ -234,3 +234,38 @@ int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
     free(H);
     return 0;
 }
+
+/*
+ * Causal depthwise convolution followed by SiLU, the step before the scan in
+ * the Mamba block ("Mamba 论文精读" (youngju.dev) §3.4: a 1-D convolution over
+ * the sequence, padded with width-1 zeros in front and cut back to the
+ * sequence length so that step l sees only steps <= l, then SiLU):
+ *   u[l] = silu( sum_{k=0}^{width-1} w[k] * x[l - (width-1) + k] + bias )
+ * with x at negative steps taken from xprev (the last width-1 inputs of an
+ * earlier piece of the sequence, oldest first) or zero when xprev is NULL.
+ *   x, u   : (nrows, seqlen)
+ *   w      : (nrows, width)    the weights of each row's channel
+ *   bias   : (nrows) or NULL
+ *   xprev  : (nrows, width-1) or NULL
+ * Returns 0, or -1 if width is out of range.
+ */
+int oracle_causal_conv_silu(int64_t nrows, int64_t seqlen, int64_t width,
+                            const double* x, const double* w, const double* bias,
+                            const double* xprev, double* u)
+{
+    if (width < 1 || width > 64) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        for (int64_t l = 0; l < seqlen; ++l) {
+            double acc = bias ? bias[r] : 0.0;
+            for (int64_t k = 0; k < width; ++k) {
+                const int64_t src = l - (width - 1) + k;
+                double xv;
+                if (src >= 0) xv = x[r * seqlen + src];
+                else xv = xprev ? xprev[r * (width - 1) + (width - 1) + src] : 0.0;
+                acc += w[r * width + k] * xv;
+            }
+            u[r * seqlen + l] = silu_ref(acc);
+        }
+    }
+    return 0;
+}
