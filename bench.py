@@ -535,6 +535,94 @@ def run_bwd(args, w):
     return 0
 
 
+def run_conv(args, w):
+    """One step = one mamba_conv_scan_fwd call: causal conv1d(4) + SiLU fused in front of the scan."""
+    import torch
+    from selective_state_space_133_b300 import ops
+    from selective_state_space_133_b300 import synthetic as syn
+
+    ws, rank, local = dist_setup(want_nccl=True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = syn.scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed + 7919 * rank, with_D=w.with_D,
+                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+    g = torch.Generator().manual_seed(w.seed + 3)
+    cw = torch.randn(w.dim, 4, generator=g) * 0.5
+    cb = torch.randn(w.dim, generator=g) * 0.1
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    cwd, cbd = cw.to(dev), cb.to(dev)
+    y = torch.empty_like(d["u"])
+    work = torch.empty(max(1, ops.workspace_bytes(w.batch, w.dim, w.seqlen, w.dtype)), dtype=torch.uint8,
+                       device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ops.mamba_conv_scan_fwd(d["u"], cwd, d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                                d["softplus"], conv_bias=cbd, y=y, stream=stream, workspace=work)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ops.check_device_error(stream)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local] if vis else str(local)) if rank == 0 else None
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ops.check_device_error(stream)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / K
+    value = ws * w.elements / (ms * 1e-3)
+    if rank != 0:
+        return 0
+    props = torch.cuda.get_device_properties(dev)
+    sm_max = (clocks or {}).get("sm_max_mhz") or 2032.0
+    alu_peak = 32.0 * props.multi_processor_count * sm_max * 1e6
+    peak, peak_kind = hbm_peak()
+    import oracle
+    budget = float(os.environ.get("BENCH_CPU_BASELINE_S", "10"))
+    nch, el, t_cpu = 1, 0, 0.0
+    while t_cpu < budget and nch <= w.dim:
+        sl = lambda t: None if t is None else t[:1, :nch].contiguous()
+        t0 = time.perf_counter()
+        oracle.conv_scan(sl(x["u"]), cw[:nch], cb[:nch], None, sl(x["delta"]), x["A"][:nch], x["B"][:1].contiguous(),
+                         x["C"][:1].contiguous(), None if x["D"] is None else x["D"][:nch], sl(x["z"]),
+                         None if x["delta_bias"] is None else x["delta_bias"][:nch], x["softplus"])
+        t_cpu = time.perf_counter() - t0
+        el = nch * w.seqlen * 16
+        nch *= 2
+    line = {
+        "metric": "selective-scan elems/s (B·L·D·N) with the causal conv1d(4) + SiLU fused in front, 1×B300",
+        "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp32", "data": "synthetic",
+        "config": dict(workload_config(w, ws), conv="fused causal depthwise conv1d, width 4, + SiLU"),
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "alu", "achieved": value / ws, "peak": alu_peak, "unit": "elem/s",
+                     "frac": value / ws / alu_peak, "traffic": None,
+                     "peak_source": f"32 ex2/clk/SM x {props.multi_processor_count} SMs x {sm_max:.0f} MHz",
+                     "hbm_gbs": w.io_bytes / (ms * 1e-3) / 1e9, "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind,
+                     "hbm_frac": w.io_bytes / (ms * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_launch": w.io_bytes},
+        "clocks": clocks,
+        "cpu_baseline": {"value": el / t_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{nch // 2} whole channels of batch row 0 ({el} elements), fp64, {t_cpu:.1f} s"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,8 +630,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="bwd: time the backward (all gradients) on a scan workload")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "conv"], default="fwd",
+                    help="bwd: the backward (all gradients); conv: the scan with the fused conv1d + SiLU")
     args = ap.parse_args()
     from selective_state_space_133_b300 import synthetic as syn
     if args.workload in syn.DECODE_WORKLOADS:
@@ -551,10 +639,10 @@ def main():
             raise SystemExit("--impl reference times the scan workload only")
         return run_decode(args, syn.DECODE_WORKLOADS[args.workload])
     w = syn.SCAN_WORKLOADS[args.workload]
-    if args.pass_ == "bwd":
+    if args.pass_ in ("bwd", "conv"):
         if args.impl == "reference":
-            raise SystemExit("--impl reference times the forward only")
-        return run_bwd(args, w)
+            raise SystemExit("--impl reference times the plain forward only")
+        return run_bwd(args, w) if args.pass_ == "bwd" else run_conv(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -132,6 +132,34 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       void* stream);
 
 /*
+ * The scan of u = silu(conv1d(x)): the Mamba block's causal depthwise
+ * convolution and SiLU in front of the scan ("Mamba 论文精读" (youngju.dev)
+ * §3.4), fused into the scan kernel so that u never reaches device memory:
+ *   u[b,d,l] = silu( sum_{k=0}^{3} conv_weight[d,k] * x[b,d,l-3+k] + conv_bias[d] )
+ * Arguments as mamba_scan_fwd_ws with u replaced by
+ *   x            : (batch, dim, seqlen) io_dtype, the convolution's input
+ *   conv_weight  : (dim, conv_width) fp32, 16-byte aligned
+ *   conv_bias    : (dim) fp32 or NULL
+ *   conv_state   : (batch, dim, conv_width - 1) io_dtype or NULL: x at steps
+ *                  -3..-1 (oldest first), for a sequence scanned in pieces;
+ *                  NULL means zeros (the padding of a fresh sequence)
+ *   conv_width   : must be 4 (MAMBA_ERR_SHAPE otherwise)
+ * u is computed and used in fp32 (it is not rounded to the I/O dtype). The
+ * workspace is the same as mamba_scan_fwd_ws's (mamba_scan_workspace_size).
+ */
+int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float* conv_bias,
+                           const void* conv_state, int conv_width,
+                           const void* delta, const float* A,
+                           const void* B, const void* C,
+                           const float* D, const void* z,
+                           const float* delta_bias, int softplus_flag,
+                           const float* initial_state,
+                           void* y, float* final_state,
+                           int batch, int dim, int seqlen, int dstate,
+                           int io_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * Bytes of device workspace mamba_scan_bwd needs for these sizes (0 when there
  * is nothing to compute or an argument is out of range): the packed fp32 B/C
  * rows (batch * roundup(seqlen, 16) * 128 bytes), one fp32 state per row per

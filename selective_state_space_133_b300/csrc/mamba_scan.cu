@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/mamba_scan.h"
 #include "scan_bwd.cuh"
@@ -119,12 +120,19 @@ int launch_scan(const mscan::ScanArgs& a, const void* u, const void* delta, cons
     }
     const dim3 grid((a.dim + mscan::kCtaCh - 1) / mscan::kCtaCh, a.batch);
     const int threads = mscan::kScanThreads;
+    auto go = [&](auto sp, auto hz, auto cv) {
+        mscan::scan_fwd_kernel<T, decltype(sp)::value, decltype(hz)::value, decltype(cv)::value>
+            <<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
+    };
+    using Y = std::true_type;
+    using N = std::false_type;
+    const bool conv = a.conv_w != nullptr;
     if (softplus) {
-        if (z) mscan::scan_fwd_kernel<T, true, true><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
-        else   mscan::scan_fwd_kernel<T, true, false><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
+        if (z) { if (conv) go(Y{}, Y{}, Y{}); else go(Y{}, Y{}, N{}); }
+        else   { if (conv) go(Y{}, N{}, Y{}); else go(Y{}, N{}, N{}); }
     } else {
-        if (z) mscan::scan_fwd_kernel<T, false, true><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
-        else   mscan::scan_fwd_kernel<T, false, false><<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
+        if (z) { if (conv) go(N{}, Y{}, Y{}); else go(N{}, Y{}, N{}); }
+        else   { if (conv) go(N{}, N{}, Y{}); else go(N{}, N{}, N{}); }
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
@@ -226,12 +234,20 @@ static int check_scan_args(const void* u, const void* delta, const float* A, con
     return MAMBA_OK;
 }
 
+struct ConvArgs {
+    const float* w = nullptr;     // (dim, 4) or null: no convolution
+    const float* b = nullptr;
+    const void* state = nullptr;
+};
+
 static int scan_with_workspace(const void* u, const void* delta, const float* A, const void* B, const void* C,
                                const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
                                float* final_state, int batch, int dim, int seqlen, int io_dtype, void* workspace,
-                               cudaStream_t s, const float* initial_state = nullptr) {
+                               cudaStream_t s, const float* initial_state = nullptr, ConvArgs conv = ConvArgs()) {
     mscan::ScanArgs a;
+    memset(&a, 0, sizeof(a));
     a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state; a.y = y; a.final_state = final_state;
+    a.conv_w = conv.w; a.conv_b = conv.b; a.conv_state = conv.state;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
     char* ws = static_cast<char*>(workspace);
     const int sp = softplus_flag != 0;
@@ -260,6 +276,33 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const vo
     }
     return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
                                seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state);
+}
+
+int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float* conv_bias,
+                           const void* conv_state, int conv_width, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                           const float* initial_state, void* y, float* final_state, int batch, int dim,
+                           int seqlen, int dstate, int io_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    int st = check_scan_args(x, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+                             io_dtype, initial_state);
+    if (st != MAMBA_OK) return st;
+    if (conv_width != mscan::kConvW) return MAMBA_ERR_SHAPE;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+    if (!conv_weight) return MAMBA_ERR_NULL;
+    if (!aligned(conv_weight, 16) || (conv_bias && !aligned(conv_bias, 4)) ||
+        (conv_state && !aligned(conv_state, dtype_size(io_dtype))))
+        return MAMBA_ERR_ALIGN;
+    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    if (need > 0) {
+        if (!workspace) return MAMBA_ERR_NULL;
+        if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
+    }
+    ConvArgs conv;
+    conv.w = conv_weight; conv.b = conv_bias; conv.state = conv_state;
+    return scan_with_workspace(x, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
+                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state, conv);
 }
 
 int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,

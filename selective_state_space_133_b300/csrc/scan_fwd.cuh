@@ -62,6 +62,8 @@ constexpr int kPH = (kTL / 4) * kPJ;     // partial sums: stride between state h
 constexpr int kStages = 4;               // TMA ring depth
 constexpr int kScanThreads = 32;
 
+constexpr int kConvW = 4;  // width of the causal convolution fused in front of the scan
+
 struct ScanArgs {
     const float* A;
     const float* D;      // may be null
@@ -70,6 +72,11 @@ struct ScanArgs {
     void* y;
     float* final_state;  // may be null
     int batch, dim, seqlen;
+    // With the fused convolution (the kernel's CONV instantiation) the u tiles
+    // hold the convolution's input x, and u = silu(sum_k w[k] x[l-3+k] + b):
+    const float* conv_w;     // (dim, kConvW) fp32
+    const float* conv_b;     // (dim) fp32, may be null
+    const void* conv_state;  // (batch, dim, kConvW - 1) io dtype: x before step 0, oldest first; may be null
 };
 
 template <typename T>
@@ -86,6 +93,8 @@ struct ScanSmem {
     alignas(16) float2 W[kCtaCh][kWP];   // {dt, dt*u} per (channel, step)
     alignas(16) float P[2 * kPH];        // [state half][4-step group][channel][4 steps]
     alignas(8) uint64_t full[kStages];   // TMA transaction barrier per slot
+    alignas(16) float U[kCtaCh][kTL + 1];  // u after the convolution (CONV only)
+    float XH[2][kCtaCh][kConvW - 1];     // the last inputs x of the previous chunk (CONV only)
 };
 
 // ------------------------------------------------------------ helpers ------
@@ -151,7 +160,7 @@ __device__ __forceinline__ float2 gate2(float2 y, float2 z) {
 
 // ------------------------------------------------------------- kernel ------
 
-template <typename T, bool SOFTPLUS, bool HAS_Z>
+template <typename T, bool SOFTPLUS, bool HAS_Z, bool CONV>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_dl, const __grid_constant__ CUtensorMap tm_z,
@@ -214,6 +223,21 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     const int edc = eactive ? ed : a.dim - 1;
     const float bias = a.bias ? a.bias[edc] : 0.f;
     const float Dd = a.D ? a.D[edc] : 0.f;
+    float cw[kConvW] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f;
+    if (CONV) {
+        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + static_cast<size_t>(edc) * kConvW);
+        cw[0] = w4.x; cw[1] = w4.y; cw[2] = w4.z; cw[3] = w4.w;
+        cb = a.conv_b ? a.conv_b[edc] : 0.f;
+        // the inputs before step 0 (read by the same lane in the first pre-pass)
+        if (ej == 0) {
+#pragma unroll
+            for (int m = 0; m < kConvW - 1; ++m)
+                sm.XH[1][ec][m] = (a.conv_state && eactive)
+                    ? Io<T>::to_f(static_cast<const T*>(a.conv_state)[(static_cast<size_t>(b) * a.dim + ed) *
+                                                                          (kConvW - 1) + m])
+                    : 0.f;
+        }
+    }
     // this lane's output: steps 8*ej .. 8*ej+7 of every chunk of channel ed
     T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + 8 * ej;
     const bool vec_ok = eactive && (L & 7) == 0;
@@ -246,6 +270,31 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         float uv[8], dv[8];
         lds8(&S.u[ec][8 * ej], uv);
         lds8(&S.dl[ec][8 * ej], dv);
+        if (CONV) {
+            // the 3 inputs before this lane's first step: from this chunk (second
+            // half) or from the previous chunk's last inputs (first half)
+            float xm[kConvW - 1];
+#pragma unroll
+            for (int m = 0; m < kConvW - 1; ++m)
+                xm[m] = ej ? Io<T>::to_f(S.u[ec][8 - (kConvW - 1) + m]) : sm.XH[(k + 1) & 1][ec][m];
+            if (ej) {
+#pragma unroll
+                for (int m = 0; m < kConvW - 1; ++m) sm.XH[k & 1][ec][m] = uv[8 - (kConvW - 1) + m];
+            }
+            float xs[8 + kConvW - 1];
+#pragma unroll
+            for (int m = 0; m < kConvW - 1; ++m) xs[m] = xm[m];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xs[kConvW - 1 + i] = uv[i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float acc = cb;
+#pragma unroll
+                for (int m = 0; m < kConvW; ++m) acc = fmaf(cw[m], xs[i + m], acc);
+                uv[i] = silu_f(acc);
+                sm.U[ec][8 * ej + i] = uv[i];
+            }
+        }
         const float2 bb = make_float2(bias, bias);
         float4* W = reinterpret_cast<float4*>(&sm.W[ec][8 * ej]);
         const int lr = k * kTL + 8 * ej;  // first step of this lane's eight
@@ -345,7 +394,12 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                        __fadd2_rn(make_float2(a1.x, a1.y), make_float2(b1.x, b1.y)),
                        __fadd2_rn(make_float2(a1.z, a1.w), make_float2(b1.z, b1.w))};
         float uv[8];
-        lds8(&S.u[ec][8 * ej], uv);
+        if (CONV) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) uv[i] = sm.U[ec][8 * ej + i];
+        } else {
+            lds8(&S.u[ec][8 * ej], uv);
+        }
         const float2 DD = make_float2(Dd, Dd);
 #pragma unroll
         for (int i = 0; i < 4; ++i) y[i] = __ffma2_rn(DD, make_float2(uv[2 * i], uv[2 * i + 1]), y[i]);

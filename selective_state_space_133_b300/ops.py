@@ -99,6 +99,56 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     return (y, final_state) if want_state else y
 
 
+def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+                        conv_bias=None, conv_state=None, initial_state=None, final_state=None, y=None,
+                        stream=None, workspace=None):
+    """Scan of u = silu(causal conv1d(x)) (see include/mamba_scan.h, mamba_conv_scan_fwd_ws).
+
+    x: (batch, dim, L) I/O dtype; conv_weight: (dim, 4) fp32; conv_bias: (dim,)
+    fp32; conv_state: (batch, dim, 3) I/O dtype, x before step 0. Other
+    arguments and the return value as mamba_scan_fwd.
+    """
+    if x.dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {x.dtype}")
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_conv_scan_fwd runs on CUDA tensors only")
+    batch, dim, L = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    width = conv_weight.shape[1] if conv_weight.dim() == 2 else -1
+    _need(x, "x", x.dtype, (batch, dim, L), dev)
+    _need(delta, "delta", x.dtype, (batch, dim, L), dev)
+    _need(z, "z", x.dtype, (batch, dim, L), dev)
+    _need(B, "B", x.dtype, (batch, N, L), dev)
+    _need(C, "C", x.dtype, (batch, N, L), dev)
+    _need(A, "A", torch.float32, (dim, N), dev)
+    _need(D, "D", torch.float32, (dim,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (dim,), dev)
+    _need(conv_weight, "conv_weight", torch.float32, (dim, width), dev)
+    _need(conv_bias, "conv_bias", torch.float32, (dim,), dev)
+    _need(conv_state, "conv_state", x.dtype, (batch, dim, width - 1), dev)
+    _need(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    want_state = final_state is not None and final_state is not False
+    if final_state is True:
+        final_state = torch.empty((batch, dim, N), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    lib = _lib.lib()
+    need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[x.dtype]))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.mamba_conv_scan_fwd_ws(
+        _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), width, _ptr(delta), _ptr(A), _ptr(B),
+        _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(initial_state), _ptr(y),
+        _ptr(final_state), batch, dim, L, N, _IO[x.dtype], _ptr(workspace), workspace.numel(),
+        _stream_handle(stream, dev))
+    _lib.check(st, "mamba_conv_scan_fwd")
+    return (y, final_state) if want_state else y
+
+
 def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
                    initial_state=None, want_initial_state_grad=False, stream=None, workspace=None):
     """Gradients of sum(dy * y) for the scan (see include/mamba_scan.h, mamba_scan_bwd).

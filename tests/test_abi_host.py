@@ -126,3 +126,21 @@ def test_workspace_size(L):
 ])
 def test_scan_ws_rejects(L, kw, code):
     assert scan_ws(L, **kw) == code
+
+
+def conv_scan(L, **kw):
+    args = dict(x=P, w=P, cb=None, cs=None, width=4, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, sp=1,
+                h0=None, y=P, fs=None, batch=2, dim=32, seqlen=64, dstate=16, dtype=1, ws=P, ws_bytes=1 << 30)
+    args.update(kw)
+    return L.mamba_conv_scan_fwd_ws(args["x"], args["w"], args["cb"], args["cs"], args["width"], args["delta"],
+                                    args["A"], args["B"], args["C"], args["D"], args["z"], args["bias"], args["sp"],
+                                    args["h0"], args["y"], args["fs"], args["batch"], args["dim"], args["seqlen"],
+                                    args["dstate"], args["dtype"], args["ws"], args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(width=3), -2), (dict(width=5), -2), (dict(w=None), -1), (dict(w=P + 8), -4), (dict(cb=P + 2), -4),
+    (dict(cs=P + 1), -4), (dict(x=None), -1), (dict(ws=None), -1), (dict(ws_bytes=10), -7), (dict(dtype=3), -3),
+])
+def test_conv_scan_rejects(L, kw, code):
+    assert conv_scan(L, **kw) == code
