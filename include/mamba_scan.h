@@ -113,6 +113,10 @@ size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int
  *                     from the previous piece's final_state ("mamba->jamba"
  *                     §2.2: the recurrence carries h from token to token);
  *                     with seqlen == 0, final_state receives it unchanged
+ *   chunk_states    : (batch, dim, ceil(seqlen / 16), dstate) fp32, 16-byte
+ *                     aligned, or NULL: receives the state before every 16-step
+ *                     chunk (the first is initial_state), which mamba_scan_bwd
+ *                     can take instead of recomputing it (training)
  *   workspace       : device buffer, 256-byte aligned, owned by the caller, of
  *                     at least mamba_scan_workspace_size(...) bytes (may be NULL
  *                     when that size is 0); its contents are scratch, needed
@@ -126,7 +130,7 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       const float* D, const void* z,
                       const float* delta_bias, int softplus_flag,
                       const float* initial_state,
-                      void* y, float* final_state,
+                      void* y, float* final_state, float* chunk_states,
                       int batch, int dim, int seqlen, int dstate,
                       int io_dtype, void* workspace, size_t workspace_bytes,
                       void* stream);
@@ -176,6 +180,9 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
  * one fp32 state per row every 16 steps in the workspace in between.
  * Inputs: as mamba_scan_fwd_ws (u, delta, A, B, C, D, z, delta_bias,
  * softplus_flag, initial_state), plus
+ *   chunk_states    : the forward's chunk_states output for these same inputs,
+ *                     or NULL: the backward then recomputes them (one more
+ *                     sweep over the sequence)
  *   dy              : (batch, dim, seqlen) io_dtype, the gradient reaching y
  * Outputs (device, caller-owned, overwritten; 16-byte aligned except dD and
  * ddelta_bias, 4-byte):
@@ -196,7 +203,8 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A,
                    const void* B, const void* C,
                    const float* D, const void* z,
                    const float* delta_bias, int softplus_flag,
-                   const float* initial_state, const void* dy,
+                   const float* initial_state, const float* chunk_states,
+                   const void* dy,
                    void* du, void* ddelta, float* dA, void* dB, void* dC,
                    float* dD, void* dz, float* ddelta_bias, float* dinitial_state,
                    int batch, int dim, int seqlen, int dstate, int io_dtype,

@@ -21,12 +21,12 @@ _I = ctypes.c_int
 _Z = ctypes.c_size_t
 SIGNATURES = {
     "mamba_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
-    "mamba_scan_fwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "mamba_scan_fwd_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "mamba_scan_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "mamba_conv_scan_fwd_ws": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I,
                                     _I, _P, _Z, _P]),
     "mamba_scan_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
-    "mamba_scan_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+    "mamba_scan_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                             _I, _I, _I, _I, _I, _P, _Z, _P]),
     "mamba_scan_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "mamba_state_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),

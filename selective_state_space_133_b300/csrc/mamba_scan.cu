@@ -176,7 +176,7 @@ int launch_bwd(mscan::ScanBwdArgs a, const void* B, const void* C, void* dB, voi
     if (a.dbias && cudaMemsetAsync(a.dbias, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
     if (a.seqlen > 0) {
         a.bc = reinterpret_cast<const float*>(ws + w.bc);
-        a.hck = reinterpret_cast<float*>(ws + w.hck);
+        if (!a.have_hck) a.hck = reinterpret_cast<float*>(ws + w.hck);
         a.dbc = reinterpret_cast<float*>(ws + w.dbc);
         if (cudaMemsetAsync(a.dbc, 0, static_cast<size_t>(a.batch) * 2 * kDState * w.Lp * sizeof(float), stream) !=
             cudaSuccess)
@@ -243,11 +243,13 @@ struct ConvArgs {
 static int scan_with_workspace(const void* u, const void* delta, const float* A, const void* B, const void* C,
                                const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
                                float* final_state, int batch, int dim, int seqlen, int io_dtype, void* workspace,
-                               cudaStream_t s, const float* initial_state = nullptr, ConvArgs conv = ConvArgs()) {
+                               cudaStream_t s, const float* initial_state = nullptr, ConvArgs conv = ConvArgs(),
+                               float* chunk_states = nullptr) {
     mscan::ScanArgs a;
     memset(&a, 0, sizeof(a));
     a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state; a.y = y; a.final_state = final_state;
     a.conv_w = conv.w; a.conv_b = conv.b; a.conv_state = conv.state;
+    a.chunk_states = chunk_states;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
     char* ws = static_cast<char*>(workspace);
     const int sp = softplus_flag != 0;
@@ -263,11 +265,13 @@ size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int
 
 int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,
                       const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                      const float* initial_state, void* y, float* final_state, int batch, int dim, int seqlen,
-                      int dstate, int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+                      const float* initial_state, void* y, float* final_state, float* chunk_states, int batch,
+                      int dim, int seqlen, int dstate, int io_dtype, void* workspace, size_t workspace_bytes,
+                      void* stream) {
     int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
                              io_dtype, initial_state);
     if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
+    if (chunk_states && !aligned(chunk_states, 16)) return MAMBA_ERR_ALIGN;
     const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
     if (need > 0) {
         if (!workspace) return MAMBA_ERR_NULL;
@@ -275,7 +279,8 @@ int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const vo
         if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
     }
     return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state);
+                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state,
+                               ConvArgs(), chunk_states);
 }
 
 int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float* conv_bias,
@@ -388,7 +393,7 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
 
 int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
                    const void* z, const float* delta_bias, int softplus_flag, const float* initial_state,
-                   const void* dy, void* du, void* ddelta, float* dA, void* dB, void* dC, float* dD, void* dz,
+                   const float* chunk_states, const void* dy, void* du, void* ddelta, float* dA, void* dB, void* dC, float* dD, void* dz,
                    float* ddelta_bias, float* dinitial_state, int batch, int dim, int seqlen, int dstate,
                    int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
     int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, dy, nullptr, batch, dim, seqlen, dstate, io_dtype,
@@ -399,7 +404,7 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     if (seqlen > 0 && (!du || !ddelta || !dB || !dC)) return MAMBA_ERR_NULL;
     if (z && seqlen > 0 && !dz) return MAMBA_ERR_NULL;
     if ((dD && !D) || (ddelta_bias && !delta_bias)) return MAMBA_ERR_NULL;  // a gradient of an absent input
-    const void* p16[] = {du, ddelta, dA, dB, dC, dz, dinitial_state};
+    const void* p16[] = {du, ddelta, dA, dB, dC, dz, dinitial_state, chunk_states};
     for (const void* p : p16)
         if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
     if ((dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4))) return MAMBA_ERR_ALIGN;
@@ -414,6 +419,8 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     a.u = u; a.delta = delta; a.z = z; a.dy = dy; a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state;
     a.du = du; a.ddelta = ddelta; a.dz = z ? dz : nullptr; a.dA = dA; a.dD = dD; a.dbias = ddelta_bias;
     a.dh0 = dinitial_state;
+    a.hck = const_cast<float*>(chunk_states);  // read only when given
+    a.have_hck = chunk_states != nullptr;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = softplus_flag != 0;
     char* ws = static_cast<char*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -18,7 +18,8 @@
 // channel rc; pre-pass/epilogue lanes (ec, ej) = (lane >> 1, lane & 1) own
 // steps 8ej..8ej+7 of channel ec.
 //   Sweep 1 (forward, chunk by chunk): dt and dt*u, the recurrence, and the
-//            state before each chunk stored to the workspace.
+//            state before each chunk stored to the workspace; skipped when the
+//            forward already stored them (its chunk_states output).
 //   Sweep 2 (reverse, chunk by chunk): reload the chunk's starting state,
 //            recompute its 16 states into shared memory with C.h; form dp and
 //            dz; run the reverse recurrence over the 16 steps; per step, the
@@ -46,7 +47,8 @@ struct ScanBwdArgs {
     const float* D;         // may be null
     const float* bias;      // may be null
     const float* h0;        // may be null
-    float* hck;             // workspace: (batch, dim, n_chunks, 16) fp32
+    float* hck;             // (batch, dim, n_chunks, 16) fp32: the workspace, or the forward's chunk states
+    int have_hck;           // 1: hck already holds the states (from the forward): skip sweep 1
     float* dbc;             // workspace: (batch, 2, 16, Lp) fp32 sums of dB, dC (zeroed by the host)
     void* du;
     void* ddelta;
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
     }
 #pragma unroll 1
-    for (int k = 0; k < n; ++k) {
+    for (int k = 0; k < (a.have_hck ? 0 : n); ++k) {
         {
             float uv[8], dv[8];
             load8(a.u, k, uv);

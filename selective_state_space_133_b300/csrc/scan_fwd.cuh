@@ -71,6 +71,7 @@ struct ScanArgs {
     const float* h0;     // state before the first step, may be null (zero)
     void* y;
     float* final_state;  // may be null
+    float* chunk_states; // (batch, dim, ceil(seqlen / 16), 16): the state before every chunk; may be null
     int batch, dim, seqlen;
     // With the fused convolution (the kernel's CONV instantiation) the u tiles
     // hold the convolution's input x, and u = silu(sum_k w[k] x[l-3+k] + b):
@@ -428,9 +429,17 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         if (!wait_full(0, 0)) return;
         prepass(sm.st[0], 0);
         __syncwarp();
+        float* const ck = a.chunk_states ? a.chunk_states + (static_cast<size_t>(b) * a.dim + rd) * n * kDState + 8 * rh
+                                         : nullptr;
+        const bool ck_store = ck && d0 + rc < a.dim;
 #pragma unroll 1
         for (int k = 0; k < n; ++k) {
             const ScanStage<T>& S = sm.st[k % kStages];
+            if (ck_store) {  // the state before chunk k, for the backward
+                float4* p = reinterpret_cast<float4*>(ck + static_cast<size_t>(k) * kDState);
+                p[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                p[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+            }
             recurrence(S);
             __syncwarp();
             epilogue(S, k);

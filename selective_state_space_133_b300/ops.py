@@ -48,7 +48,7 @@ def workspace_bytes(batch: int, dim: int, seqlen: int, dtype: torch.dtype, dstat
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                   y=None, final_state=None, stream=None, workspace=None, initial_state=None):
+                   y=None, final_state=None, stream=None, workspace=None, initial_state=None, chunk_states=None):
     """Selective scan (see include/mamba_scan.h, mamba_scan_fwd_ws).
 
     u, delta, z: (batch, dim, L); B, C: (batch, 16, L), all fp32 or all bf16;
@@ -58,6 +58,8 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     bytes; otherwise one is taken from torch's caching allocator.
     ``initial_state``: (batch, dim, 16) fp32 state before the first step, or None
     for zero (continuing an earlier scan from its final state).
+    ``chunk_states``: a (batch, dim, ceil(L/16), 16) fp32 tensor that receives the
+    state before every 16-step chunk (for mamba_scan_bwd), or None.
     Returns y, or (y, final_state) when a final state was requested.
     """
     if u.dtype not in _IO:
@@ -85,6 +87,7 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
         final_state = None
     _need(final_state, "final_state", torch.float32, (batch, dim, N), dev)
     _need(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    _need(chunk_states, "chunk_states", torch.float32, (batch, dim, (L + 15) // 16, N), dev)
     lib = _lib.lib()
     need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[u.dtype]))
     if workspace is None:
@@ -93,7 +96,8 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     st = lib.mamba_scan_fwd_ws(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(initial_state), _ptr(y), _ptr(final_state), batch, dim, L, N, _IO[u.dtype],
+        int(bool(softplus)), _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), batch, dim, L, N,
+        _IO[u.dtype],
         _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_fwd")
     return (y, final_state) if want_state else y
@@ -150,7 +154,8 @@ def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bi
 
 
 def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
-                   initial_state=None, want_initial_state_grad=False, stream=None, workspace=None):
+                   initial_state=None, want_initial_state_grad=False, stream=None, workspace=None,
+                   chunk_states=None):
     """Gradients of sum(dy * y) for the scan (see include/mamba_scan.h, mamba_scan_bwd).
 
     Inputs as mamba_scan_fwd plus dy (batch, dim, L) in the I/O dtype. Returns a
@@ -173,6 +178,7 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
     _need(D, "D", torch.float32, (dim,), dev)
     _need(delta_bias, "delta_bias", torch.float32, (dim,), dev)
     _need(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    _need(chunk_states, "chunk_states", torch.float32, (batch, dim, (L + 15) // 16, N), dev)
     out = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u), dz=None if z is None else torch.empty_like(u),
                dA=torch.empty((dim, N), dtype=torch.float32, device=dev),
                dB=torch.empty_like(B), dC=torch.empty_like(C),
@@ -185,7 +191,7 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     st = lib.mamba_scan_bwd(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
-        _ptr(initial_state), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
+        _ptr(initial_state), _ptr(chunk_states), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
         _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(out["dh0"]),
         batch, dim, L, N, _IO[u.dtype], _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_bwd")

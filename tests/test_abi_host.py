@@ -105,7 +105,8 @@ def scan_ws(L, ws=P, ws_bytes=1 << 30, **kw):
                 batch=2, dim=32, seqlen=64, dstate=16, dtype=1, stream=None)
     args.update(kw)
     return L.mamba_scan_fwd_ws(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["z"],
-                               args["bias"], args["sp"], args.get("h0"), args["y"], args["fs"], args["batch"],
+                               args["bias"], args["sp"], args.get("h0"), args["y"], args["fs"], args.get("ck"),
+                               args["batch"],
                                args["dim"], args["seqlen"], args["dstate"], args["dtype"], ws, ws_bytes,
                                args["stream"])
 
@@ -122,7 +123,7 @@ def test_workspace_size(L):
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=None), -1), (dict(ws_bytes=100), -7), (dict(ws=P + 16), -4),
     (dict(dtype=5), -3), (dict(dstate=64), -2), (dict(u=P + 2), -4), (dict(C=None), -1),
-    (dict(h0=P + 8), -4),
+    (dict(h0=P + 8), -4), (dict(ck=P + 4), -4),
 ])
 def test_scan_ws_rejects(L, kw, code):
     assert scan_ws(L, **kw) == code

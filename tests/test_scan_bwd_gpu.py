@@ -77,3 +77,24 @@ def test_bwd_zero_length():
     torch.cuda.synchronize()
     assert torch.count_nonzero(out["dA"]) == 0 and torch.count_nonzero(out["dD"]) == 0
     assert torch.count_nonzero(out["ddelta_bias"]) == 0 and torch.count_nonzero(out["dh0"]) == 0
+
+
+@pytest.mark.parametrize("dtype,L", [(torch.bfloat16, 200), (torch.float32, 64)])
+def test_bwd_from_forward_chunk_states(dtype, L):
+    """The backward given the forward's chunk states equals the backward that recomputes them."""
+    x = syn.scan_inputs(2, 24, L, dtype, seed=L)
+    g = torch.Generator().manual_seed(L + 9)
+    dy = torch.randn(2, 24, L, generator=g).to(dtype).cuda()
+    h0 = (torch.randn(2, 24, 16, generator=g) * 0.3).cuda()
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    ck = torch.empty(2, 24, (L + 15) // 16, 16, device="cuda")
+    ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], d["softplus"],
+                       initial_state=h0, chunk_states=ck)
+    args = (d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"], d["softplus"])
+    ref = ops.mamba_scan_bwd(*args, initial_state=h0, want_initial_state_grad=True)
+    got = ops.mamba_scan_bwd(*args, initial_state=h0, want_initial_state_grad=True, chunk_states=ck)
+    ops.check_device_error()
+    assert torch.equal(ck[:, :, 0], h0)
+    for name in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"):
+        a, b = got[name].double().cpu().numpy(), ref[name].double().cpu().numpy()
+        assert max_rel_err(a.reshape(-1, a.shape[-1]), b.reshape(-1, b.shape[-1])) <= 1e-5, name
