@@ -12,9 +12,10 @@ calls it through ctypes.
 
 Every function here follows the definition on the pages:
   * "Mamba 论文精读" (youngju.dev) §2.2 (ZOH: A_bar = exp(Delta A); recurrence
-    h_t = A_bar h_{t-1} + B_bar x_t, y_t = C h_t), §3.1 (Delta = softplus(...)),
-    §3.3 (simplified scan: B_bar = Delta B, h starts at zero), §3.4 (gate
-    y * silu(z));
+    h_t = A_bar h_{t-1} + B_bar x_t, y_t = C h_t; with ``zoh=True`` the exact
+    B_bar = (Delta A)^-1 (exp(Delta A) - I) Delta B), §3.1 (Delta =
+    softplus(...)), §3.3 (simplified scan: B_bar = Delta B, the default; h
+    starts at zero), §3.4 (gate y * silu(z));
   * "Mamba的基础知识" (weblog-19d), 状态空间模型 section (skip term D u);
   * "mamba->jamba" (blog.csdn.net) §2.2 (constant-time recurrent inference).
 """
@@ -32,6 +33,13 @@ SOURCE = os.path.join(_HERE, "scan_oracle.c")
 LIBRARY = os.path.join(_HERE, "liboracle.so")
 
 _P = ctypes.POINTER(ctypes.c_double)
+SOFTPLUS = 1  # flag bits of the C entry points
+ZOH = 2
+
+
+def _flags(softplus, zoh=False):
+    return (SOFTPLUS if softplus else 0) | (ZOH if zoh else 0)
+
 _PI = ctypes.POINTER(ctypes.c_int64)
 
 
@@ -70,13 +78,14 @@ class Oracle:
 
     # -- scan ---------------------------------------------------------------
     def scan(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-             rows=None, return_state=True, h0=None):
+             rows=None, return_state=True, h0=None, zoh=False):
         """Selective scan of the rows ``rows`` (flat indices b*dim + d; all rows if None).
 
         u, delta, z : (batch, dim, L);  B, C : (batch, N, L);  A : (dim, N);
         D, delta_bias : (dim,); h0 : (batch, dim, N) state before the first step,
-        or None for zero. Any float dtype (bf16 torch tensors included) is
-        widened exactly to float64 first.
+        or None for zero; zoh: exact zero-order-hold B_bar instead of Delta B.
+        Any float dtype (bf16 torch tensors included) is widened exactly to
+        float64 first.
         Returns y of shape (len(rows), L) and, if asked, the final state
         (len(rows), N), both float64.
         """
@@ -99,7 +108,7 @@ class Oracle:
         h = np.empty((len(rows), N), np.float64) if return_state else None
         rc = self.lib.oracle_scan(len(rows), L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar),
                                   _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0),
-                                  int(bool(softplus)), _ptr(y), _ptr(h))
+                                  _flags(softplus, zoh), _ptr(y), _ptr(h))
         if rc != 0:
             raise ValueError(f"oracle_scan rejected dstate={N}")
         return (y, h) if return_state else y
@@ -127,10 +136,10 @@ class Oracle:
         return u.reshape(batch, dim, L)
 
     def conv_scan(self, x, conv_w, conv_b, conv_state, delta, A, B, C, D=None, z=None, delta_bias=None,
-                  softplus=False, h0=None):
+                  softplus=False, h0=None, zoh=False):
         """The scan of u = silu(causal conv1d(x)): returns y (batch*dim, L) and the final state."""
         u = self.causal_conv_silu(x, conv_w, conv_b, conv_state)
-        return self.scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0)
+        return self.scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, zoh=zoh)
 
     # -- gradients ------------------------------------------------------------
     def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
@@ -164,7 +173,7 @@ class Oracle:
         dA = np.empty((R, N)); dD = np.empty(R); db = np.empty(R)
         dB = np.empty((R, N, L)); dC = np.empty((R, N, L)); dh0 = np.empty((R, N))
         rc = self.lib.oracle_scan_bwd(R, L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar), _ptr(Dr), _ptr(br),
-                                      _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0), int(bool(softplus)),
+                                      _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0), _flags(softplus),
                                       _ptr(gy), _ptr(du), _ptr(dd), _ptr(dz), _ptr(dA), _ptr(dD), _ptr(db),
                                       _ptr(dB), _ptr(dC), _ptr(dh0))
         if rc != 0:
@@ -179,12 +188,12 @@ class Oracle:
 
     # -- state update ---------------------------------------------------------
     def state_update(self, state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                     softplus=False, rows=None, compact_state=False):
+                     softplus=False, rows=None, compact_state=False, zoh=False):
         """One decode step of the rows ``rows`` (flat b*dim + d; all rows if None).
 
         state : (batch, dim, N), or (len(rows), N) with compact_state=True;
         u, delta, z : (batch, dim);  B, C : (batch, N);  A : (dim, N);
-        D, delta_bias : (dim,).
+        D, delta_bias : (dim,); zoh as in ``scan``.
         Returns (y (len(rows),), new_state (len(rows), N)), float64; the input
         state is not modified.
         """
@@ -210,7 +219,7 @@ class Oracle:
         y = np.empty(len(rows), np.float64)
         rc = self.lib.oracle_state_update(len(rows), N, _ptr(sr), _ptr(ur), _ptr(dr), _ptr(zr),
                                           _ptr(Ar), _ptr(Dr), _ptr(br), _ptr(Bf), _ptr(Cf),
-                                          _iptr(b_idx), int(bool(softplus)), _ptr(y))
+                                          _iptr(b_idx), _flags(softplus, zoh), _ptr(y))
         if rc != 0:
             raise ValueError(f"oracle_state_update rejected dstate={N}")
         return y, sr

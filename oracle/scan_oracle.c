@@ -10,10 +10,15 @@
  * with the C library's exp/log1p, no vectorisation and no reassociation:
  *
  *   dt      = delta[l] (+ bias)                 -- bias of the dt projection
- *   dt      = softplus(dt)   if softplus_flag   -- "Mamba 论文精读" (youngju.dev) §3.1,
+ *   dt      = softplus(dt)   if ORACLE_SOFTPLUS -- "Mamba 论文精读" (youngju.dev) §3.1,
  *                                                  Delta_t = softplus(Linear_Delta(x_t))
  *   dA[n]   = exp(dt * A[n])                     -- same page §2.2 (ZOH: A_bar = exp(Delta A))
  *   dBu[n]  = dt * B[l][n] * u[l]                -- same page §3.3 simplified scan: B_bar = Delta * B
+ *   dBu[n]  = expm1(dt*A[n])/A[n] * B[l][n] * u[l]
+ *                            if ORACLE_ZOH       -- same page §2.2, exact zero-order hold:
+ *                                                  B_bar = (Delta A)^-1 (exp(Delta A) - I) Delta B, which
+ *                                                  for a diagonal A is (exp(dt A[n]) - 1) / A[n] per state
+ *                                                  (dt, its limit, where dt*A[n] = 0)
  *   h[n]    = dA[n] * h[n] + dBu[n],  h = 0 before the first step
  *                                                -- same page §2.2 recurrence h_t = A_bar h_{t-1} + B_bar x_t
  *   y[l]    = sum_n C[l][n] * h[n]               -- same page §2.2, y_t = C h_t (read after the update)
@@ -29,11 +34,17 @@
  *
  * softplus is written as max(x,0) + log1p(exp(-|x|)), which is the same
  * function as log(1 + exp(x)) for every x but does not overflow for large x.
+ *
+ * `flags` is a bit set: ORACLE_SOFTPLUS (1) applies softplus to dt,
+ * ORACLE_ZOH (2) uses the exact zero-order-hold B_bar instead of Delta * B.
  */
 #include <math.h>
 #include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#define ORACLE_SOFTPLUS 1
+#define ORACLE_ZOH 2
 
 static double softplus_ref(double x)
 {
@@ -46,6 +57,15 @@ static double silu_ref(double z)
     return z / (1.0 + exp(-z));
 }
 
+/* Exact zero-order-hold input gain of one diagonal state: (exp(dt a) - 1) / a,
+ * written with expm1 so that small dt*a loses nothing to cancellation; its
+ * value at dt*a = 0 is the limit dt. */
+static double zoh_gain(double dt, double a)
+{
+    double x = dt * a;
+    return x == 0.0 ? dt : expm1(x) / a;
+}
+
 /* One time step of the selective SSM for one row.
  * h[dstate] in/out; A_row[dstate]; Bt, Ct: the step's B and C, read with
  * stride bc_stride (seqlen for the scan layout (batch, dstate, seqlen), 1 for
@@ -53,15 +73,16 @@ static double silu_ref(double z)
 static double ssm_step(double* h, int64_t dstate, const double* A_row,
                        const double* Bt, const double* Ct, int64_t bc_stride,
                        double u, double delta, const double* zp,
-                       const double* Dp, const double* biasp, int softplus_flag)
+                       const double* Dp, const double* biasp, int flags)
 {
     double dt = delta;
     if (biasp) dt += *biasp;
-    if (softplus_flag) dt = softplus_ref(dt);
+    if (flags & ORACLE_SOFTPLUS) dt = softplus_ref(dt);
     double y = 0.0;
     for (int64_t n = 0; n < dstate; ++n) {
         double dA = exp(dt * A_row[n]);
-        double dBu = dt * Bt[n * bc_stride] * u;
+        double dBu = (flags & ORACLE_ZOH) ? zoh_gain(dt, A_row[n]) * Bt[n * bc_stride] * u
+                                          : dt * Bt[n * bc_stride] * u;
         h[n] = dA * h[n] + dBu;
         y += Ct[n * bc_stride] * h[n];
     }
@@ -87,7 +108,7 @@ int oracle_scan(int64_t nrows, int64_t seqlen, int64_t dstate,
                 const double* u, const double* delta, const double* z,
                 const double* A, const double* Dskip, const double* bias,
                 const double* B, const double* C, const int64_t* bidx,
-                const double* h0, int softplus_flag, double* y, double* hlast)
+                const double* h0, int flags, double* y, double* hlast)
 {
     double h[1024];
     if (dstate < 1 || dstate > 1024) return -1;
@@ -100,7 +121,7 @@ int oracle_scan(int64_t nrows, int64_t seqlen, int64_t dstate,
             y[i] = ssm_step(h, dstate, A + r * dstate, Bb + l, Cb + l, seqlen,
                             u[i], delta[i], z ? z + i : NULL,
                             Dskip ? Dskip + r : NULL, bias ? bias + r : NULL,
-                            softplus_flag);
+                            flags);
         }
         if (hlast)
             for (int64_t n = 0; n < dstate; ++n) hlast[r * dstate + n] = h[n];
@@ -121,7 +142,7 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
                         const double* u, const double* delta, const double* z,
                         const double* A, const double* Dskip, const double* bias,
                         const double* B, const double* C, const int64_t* bidx,
-                        int softplus_flag, double* y)
+                        int flags, double* y)
 {
     if (dstate < 1 || dstate > 1024) return -1;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -129,7 +150,7 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
                         B + bidx[r] * dstate, C + bidx[r] * dstate, 1,
                         u[r], delta[r], z ? z + r : NULL,
                         Dskip ? Dskip + r : NULL, bias ? bias + r : NULL,
-                        softplus_flag);
+                        flags);
     }
     return 0;
 }
@@ -158,18 +179,21 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
  *   dD, dbias      : (nrows), either may be NULL
  *   dB, dC         : (nrows, dstate, seqlen)
  *   dh0            : (nrows, dstate), may be NULL
- * h0 as in oracle_scan. Returns 0, -1 if dstate is out of range, -2 if the
- * work buffer cannot be allocated.
+ * h0 as in oracle_scan; flags as in the forward, where only ORACLE_SOFTPLUS
+ * is differentiated here. Returns 0, -1 if dstate is out of range, -2 if the
+ * work buffer cannot be allocated, -3 if flags asks for the ZOH input gain.
  */
 int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
                     const double* u, const double* delta, const double* z,
                     const double* A, const double* Dskip, const double* bias,
                     const double* B, const double* C, const int64_t* bidx,
-                    const double* h0, int softplus_flag, const double* dy,
+                    const double* h0, int flags, const double* dy,
                     double* du, double* ddelta, double* dz, double* dA,
                     double* dD, double* dbias, double* dB, double* dC, double* dh0)
 {
+    const int softplus_flag = flags & ORACLE_SOFTPLUS;
     if (dstate < 1 || dstate > 1024) return -1;
+    if (flags & ORACLE_ZOH) return -3;
     /* H[(l + 1) * dstate + n] = state after step l; H[n] = state before step 0 */
     double* H = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * (size_t)dstate);
     if (!H) return -2;

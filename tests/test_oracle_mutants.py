@@ -15,15 +15,15 @@ import oracle_pins
 MUTANTS = {
     "A_bar sign flipped": ("exp(dt * A_row[n])", "exp(-dt * A_row[n])"),
     "Delta dropped from A_bar": ("exp(dt * A_row[n])", "exp(A_row[n])"),
-    "Delta dropped from B_bar": ("double dBu = dt * Bt", "double dBu = Bt"),
+    "Delta dropped from B_bar": (": dt * Bt[n * bc_stride] * u;", ": Bt[n * bc_stride] * u;"),
     "output read before the update": ("h[n] = dA * h[n] + dBu;\n        y += Ct[n * bc_stride] * h[n];",
                                       "y += Ct[n * bc_stride] * h[n];\n        h[n] = dA * h[n] + dBu;"),
     "B used as C": ("y += Ct[n * bc_stride]", "y += Bt[n * bc_stride]"),
     "B indexed along time, not state": ("Bt[n * bc_stride]", "Bt[n]"),
     "skip term dropped": ("y += (*Dp) * u;", "y += 0.0 * u;"),
     "gate is sigmoid, not silu": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
-    "bias added after softplus": ("if (biasp) dt += *biasp;\n    if (softplus_flag) dt = softplus_ref(dt);",
-                                  "if (softplus_flag) dt = softplus_ref(dt);\n    if (biasp) dt += *biasp;"),
+    "bias added after softplus": ("if (biasp) dt += *biasp;\n    if (flags & ORACLE_SOFTPLUS) dt = softplus_ref(dt);",
+                                  "if (flags & ORACLE_SOFTPLUS) dt = softplus_ref(dt);\n    if (biasp) dt += *biasp;"),
     "softplus missing log1p": ("log1p(exp(-ax))", "exp(-ax)"),
     "state not zeroed": ("h[n] = h0 ? h0[r * dstate + n] : 0.0;", "h[n] = h0 ? h0[r * dstate + n] : 0.5;"),
     "state carried across rows": ("for (int64_t n = 0; n < dstate; ++n) h[n] = h0 ? h0[r * dstate + n] : 0.0;",
