@@ -10,6 +10,10 @@ x 4096-step bf16 workload, inputs resident in HBM. Prints ONE JSON line (rank 0)
 
 --impl reference times the fp64 CPU oracle (single thread, host cores) on a
 bounded sample of the same workload; it is a deliberately slow baseline.
+--workload also takes the variants of the same shape with other state sizes or
+the exact zero-order-hold gain (scan_b8_d2048_l4096_{n8,n32,n64,zoh}_bf16) and
+the decode workload; --pass bwd / conv time the backward and the fused
+convolution + scan.
 Under torchrun each rank runs its own independent problem (weak scaling, no
 collective on the data path); timing is the max over ranks.
 """
@@ -34,6 +38,8 @@ DEFAULT_WORKLOAD = "scan_b8_d2048_l4096_bf16"
 FALLBACK_HBM_GBS = 6400.0
 KERNEL_SOURCES = ["selective_state_space_133_b300/csrc/scan_fwd.cuh",
                   "selective_state_space_133_b300/csrc/common.cuh",
+                  "selective_state_space_133_b300/csrc/fwd_launch.cuh",
+                  "selective_state_space_133_b300/csrc/host.h",
                   "selective_state_space_133_b300/csrc/mamba_scan.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_fwd_traffic.json")
 
@@ -54,12 +60,12 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_per_launch():
-    """DRAM bytes per launch from the committed ncu capture, if the kernel is unchanged since."""
+def traffic_per_launch(workload: str):
+    """DRAM bytes per launch from the committed ncu capture of this workload, if the kernel is unchanged since."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
-        if t.get("kernel_hash") == kernel_hash():
+        if t.get("kernel_hash") == kernel_hash() and t.get("workload") == workload:
             return float(t["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -154,19 +160,20 @@ def oracle_rate(x, w, budget_s: float):
         rows = np.arange(r0, r0 + n, dtype=np.int64)
         t0 = time.perf_counter()
         orc.scan(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"], x["softplus"],
-                 rows=rows, return_state=False)
+                 rows=rows, return_state=False, zoh=w.zoh)
         dt = time.perf_counter() - t0
         elapsed += dt
         rows_done += n
         r0 += n
         probe = max(1, min(512, int(n * max(0.05, (budget_s - elapsed)) / max(dt, 1e-6))))
-    elems = rows_done * w.seqlen * 16
+    elems = rows_done * w.seqlen * w.dstate
     return elems / elapsed, elems, rows_done, elapsed
 
 
 def workload_config(w, ws: int) -> dict:
     """The `config` object of both arms' JSON line."""
-    return {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": 16,
+    return {"workload": w.name, "batch": w.batch, "dim": w.dim, "seqlen": w.seqlen, "dstate": w.dstate,
+            "input_gain": "exact zero-order hold (exp(dt A) - 1) / A * B" if w.zoh else "dt * B",
             "io_dtype": "bf16" if "bf16" in w.name else "fp32", "z_gate": w.with_z, "skip_D": w.with_D,
             "softplus_in_kernel": w.softplus_in_kernel, "state_dtype": "fp32",
             "parallelism": f"replicas x{ws}", "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB > 126 MB L2"}
@@ -189,7 +196,7 @@ def run_reference(args, w):
         tot_time += t
         rows += r
     value = tot_elems / tot_time
-    sample = (f"each step: whole channels (all {w.seqlen} steps x 16 states) of the workload, about "
+    sample = (f"each step: whole channels (all {w.seqlen} steps x {w.dstate} states) of the workload, about "
               f"{per_step_budget:.2f} s of single-thread fp64 oracle work; {rows} channels over {args.steps} steps")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_time / args.steps,
@@ -211,16 +218,17 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     # each rank: its own independent problem of the workload's shape (weak scaling)
     x = syn.scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed + 7919 * rank, with_D=w.with_D,
-                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise,
+                        dstate=w.dstate)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     y = torch.empty_like(d["u"])
-    work = torch.empty(max(1, ops.workspace_bytes(w.batch, w.dim, w.seqlen, w.dtype)), dtype=torch.uint8,
-                       device=dev)
+    work = torch.empty(max(1, ops.workspace_bytes(w.batch, w.dim, w.seqlen, w.dtype, w.dstate)),
+                       dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
-                           d["softplus"], y=y, stream=stream, workspace=work)
+                           d["softplus"], y=y, stream=stream, workspace=work, zoh=w.zoh)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -286,7 +294,7 @@ def run_ours(args, w):
         return 0
     peak, peak_kind = hbm_peak()
     achieved = w.io_bytes / (kernel_ms * 1e-3) / 1e9
-    traffic = traffic_per_launch()
+    traffic = traffic_per_launch(w.name)
     props = torch.cuda.get_device_properties(dev)
     sm_mhz = clocks["sm_mhz"] if clocks else None
     # ALU roofline: one MUFU ex2 per (b,l,d,n) element at 32 per clock per SM
@@ -317,7 +325,7 @@ def run_ours(args, w):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": K2},
         "cpu_baseline": {"value": cpu_v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{cpu_rows} whole channels (x {w.seqlen} steps x 16 states = {cpu_e} elements) "
+                         "sample": f"{cpu_rows} whole channels (x {w.seqlen} steps x {w.dstate} states = {cpu_e} elements) "
                                    f"of the workload, single-thread fp64, {cpu_t:.1f} s"},
     }
     print(json.dumps(line), flush=True)
@@ -447,6 +455,8 @@ def run_decode(args, w):
 
 def run_bwd(args, w):
     """One step = one mamba_scan_bwd call (all gradients) on the workload, inputs resident in HBM."""
+    if w.dstate != 16 or w.zoh:
+        raise SystemExit("the backward is built for 16 states and the dt * B gain")
     import torch
     from selective_state_space_133_b300 import ops
     from selective_state_space_133_b300 import synthetic as syn
@@ -565,20 +575,21 @@ def run_conv(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     x = syn.scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed + 7919 * rank, with_D=w.with_D,
-                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise,
+                        dstate=w.dstate)
     g = torch.Generator().manual_seed(w.seed + 3)
     cw = torch.randn(w.dim, 4, generator=g) * 0.5
     cb = torch.randn(w.dim, generator=g) * 0.1
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     cwd, cbd = cw.to(dev), cb.to(dev)
     y = torch.empty_like(d["u"])
-    work = torch.empty(max(1, ops.workspace_bytes(w.batch, w.dim, w.seqlen, w.dtype)), dtype=torch.uint8,
-                       device=dev)
+    work = torch.empty(max(1, ops.workspace_bytes(w.batch, w.dim, w.seqlen, w.dtype, w.dstate)),
+                       dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         ops.mamba_conv_scan_fwd(d["u"], cwd, d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
-                                d["softplus"], conv_bias=cbd, y=y, stream=stream, workspace=work)
+                                d["softplus"], conv_bias=cbd, y=y, stream=stream, workspace=work, zoh=w.zoh)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -619,9 +630,9 @@ def run_conv(args, w):
         t0 = time.perf_counter()
         oracle.conv_scan(sl(x["u"]), cw[:nch], cb[:nch], None, sl(x["delta"]), x["A"][:nch], x["B"][:1].contiguous(),
                          x["C"][:1].contiguous(), None if x["D"] is None else x["D"][:nch], sl(x["z"]),
-                         None if x["delta_bias"] is None else x["delta_bias"][:nch], x["softplus"])
+                         None if x["delta_bias"] is None else x["delta_bias"][:nch], x["softplus"], zoh=w.zoh)
         t_cpu = time.perf_counter() - t0
-        el = nch * w.seqlen * 16
+        el = nch * w.seqlen * w.dstate
         nch *= 2
     line = {
         "metric": "selective-scan elems/s (B·L·D·N) with the causal conv1d(4) + SiLU fused in front, 1×B300",
@@ -658,7 +669,7 @@ def main():
         if args.impl == "reference":
             raise SystemExit("--impl reference times the scan workload only")
         return run_decode(args, syn.DECODE_WORKLOADS[args.workload])
-    w = syn.SCAN_WORKLOADS[args.workload]
+    w = syn.SCAN_WORKLOADS.get(args.workload) or syn.VARIANT_WORKLOADS[args.workload]
     if args.pass_ in ("bwd", "conv"):
         if args.impl == "reference":
             raise SystemExit("--impl reference times the plain forward only")

@@ -5,10 +5,14 @@
  * What is computed (per batch b, channel d, state n, time l):
  *
  *   dt        = delta[b,d,l] + delta_bias[d]            (bias optional, 0 if NULL)
- *   dt        = softplus(dt)            if softplus_flag  ("Mamba 论文精读", youngju.dev,
+ *   dt        = softplus(dt)     if flags & MAMBA_FLAG_SOFTPLUS  ("Mamba 论文精读", youngju.dev,
  *                                                          §3.1: Delta_t = softplus(Linear_Delta(x_t)))
  *   dA        = exp(dt * A[d,n])                          (same page §2.2, ZOH: A_bar = exp(Delta A))
  *   dBu       = dt * B[b,n,l] * u[b,d,l]                   (same page §3.3 simplified scan: B_bar = Delta B)
+ *   dBu       = (exp(dt*A[d,n]) - 1) / A[d,n] * B[b,n,l] * u[b,d,l]
+ *                                   if flags & MAMBA_FLAG_ZOH (same page §2.2, the exact zero-order
+ *                                                          hold B_bar = (Delta A)^-1 (exp(Delta A) - I)
+ *                                                          Delta B for a diagonal A; dt where dt*A = 0)
  *   h[n]      = dA * h[n] + dBu,  h = 0 before l = 0       (same page §2.2 recurrence; §3.3 starts h at zero)
  *   y[b,d,l]  = sum_n C[b,n,l] * h[n]  (+ D[d] * u[b,d,l]) (§2.2 y_t = C h_t; the D skip term is the
  *                                                          output term of "Mamba的基础知识", weblog-19d,
@@ -35,7 +39,11 @@
  *     For the state update, u/delta/z/y are (batch, dim) and B/C are (batch, dstate).
  *   - u, delta, z, B, C and y share io_dtype (fp32 or bf16). A, D, delta_bias and
  *     the state are always fp32; the recurrence and all accumulation are fp32.
- *   - dstate must be 16.
+ *   - dstate must be 8, 16, 32 or 64 (the backward: 16); anything else is
+ *     MAMBA_ERR_SHAPE.
+ *   - `flags` is a bit set of mamba_flag values; 0 and 1 keep the meaning of a
+ *     plain softplus switch. An unknown bit, or a bit an entry point does not
+ *     support, is MAMBA_ERR_FLAGS.
  *   - Base pointers of u, delta, z, y, B, C, A and state/final_state must be
  *     16-byte aligned; D and delta_bias 4-byte aligned.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
@@ -65,8 +73,15 @@ typedef enum {
     MAMBA_ERR_ALIGN = -4,           /* a base pointer violates the alignment above */
     MAMBA_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed (launch or tensor map) */
     MAMBA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up waiting on its own copies (see below) */
-    MAMBA_ERR_WORKSPACE = -7        /* workspace_bytes < mamba_scan_workspace_size(...) */
+    MAMBA_ERR_WORKSPACE = -7,       /* workspace_bytes < mamba_scan_workspace_size(...) */
+    MAMBA_ERR_FLAGS = -8            /* flags holds an unknown bit, or one this entry point lacks */
 } mamba_status;
+
+typedef enum {
+    MAMBA_FLAG_SOFTPLUS = 1,  /* dt = softplus(delta + bias) instead of delta + bias */
+    MAMBA_FLAG_ZOH = 2        /* exact zero-order-hold input gain instead of dt * B (forward entry
+                                 points and the state update) */
+} mamba_flag;
 
 /*
  * Selective scan (prefill / training forward).
@@ -75,7 +90,8 @@ typedef enum {
  *   B, C        : (batch, dstate, seqlen) io_dtype
  *   D           : (dim) fp32 or NULL (no skip term)
  *   delta_bias  : (dim) fp32 or NULL (zero bias)
- *   softplus_flag : nonzero -> dt = softplus(delta + bias), else dt = delta + bias
+ *   flags       : MAMBA_FLAG_SOFTPLUS -> dt = softplus(delta + bias), else dt = delta + bias;
+ *                 MAMBA_FLAG_ZOH -> exact zero-order-hold input gain (see the top)
  *   y           : (batch, dim, seqlen) io_dtype, written (bf16 by round-to-nearest-even)
  *   final_state : (batch, dim, dstate) fp32 or NULL; receives h after the last step
  *                 (zeros when seqlen == 0)
@@ -83,14 +99,14 @@ typedef enum {
  * is zero-filled). When seqlen == 0, u, delta, B, C, z and y may be NULL (an
  * empty tensor's data pointer). y must not alias an input.
  * The call launches one small kernel that packs B and C into a device workspace
- * (fp32, one 128-byte row of B then C per step) and then the scan kernel; the
- * workspace is allocated and freed stream-ordered on `stream`.
+ * (fp32, one row of B then C per step) and then the scan kernel; the workspace
+ * is allocated and freed stream-ordered on `stream`.
  * Returns MAMBA_OK or a negative mamba_status.
  */
 int mamba_scan_fwd(const void* u, const void* delta, const float* A,
                    const void* B, const void* C,
                    const float* D, const void* z,
-                   const float* delta_bias, int softplus_flag,
+                   const float* delta_bias, int flags,
                    void* y, float* final_state,
                    int batch, int dim, int seqlen, int dstate,
                    int io_dtype, void* stream);
@@ -98,7 +114,7 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A,
 /*
  * Bytes of device workspace mamba_scan_fwd_ws needs for these sizes (0 when
  * there is nothing to compute or an argument is out of range): the packed
- * fp32 B/C rows, batch * roundup(seqlen, 16) * 128 bytes, plus, only when
+ * fp32 B/C rows, batch * roundup(seqlen, 16) * 8 * dstate bytes, plus, only when
  * seqlen * sizeof(io type) is not a multiple of 16 bytes, copies of u, delta
  * and z at a row pitch that is.
  */
@@ -128,7 +144,7 @@ size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int
 int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       const void* B, const void* C,
                       const float* D, const void* z,
-                      const float* delta_bias, int softplus_flag,
+                      const float* delta_bias, int flags,
                       const float* initial_state,
                       void* y, float* final_state, float* chunk_states,
                       int batch, int dim, int seqlen, int dstate,
@@ -156,7 +172,7 @@ int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float*
                            const void* delta, const float* A,
                            const void* B, const void* C,
                            const float* D, const void* z,
-                           const float* delta_bias, int softplus_flag,
+                           const float* delta_bias, int flags,
                            const float* initial_state,
                            void* y, float* final_state,
                            int batch, int dim, int seqlen, int dstate,
@@ -178,8 +194,10 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
  * with respect to every input. The states are recomputed from the inputs, as
  * "mamba->jamba" (blog.csdn.net) §2.3 describes for the backward pass, keeping
  * one fp32 state per row every 16 steps in the workspace in between.
- * Inputs: as mamba_scan_fwd_ws (u, delta, A, B, C, D, z, delta_bias,
- * softplus_flag, initial_state), plus
+ * dstate must be 16 (MAMBA_ERR_SHAPE otherwise) and MAMBA_FLAG_SOFTPLUS is the
+ * only flag (the gradient of the ZOH gain is not implemented: MAMBA_ERR_FLAGS).
+ * Inputs: as mamba_scan_fwd_ws (u, delta, A, B, C, D, z, delta_bias, flags,
+ * initial_state), plus
  *   chunk_states    : the forward's chunk_states output for these same inputs,
  *                     or NULL: the backward then recomputes them (one more
  *                     sweep over the sequence)
@@ -202,7 +220,7 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
 int mamba_scan_bwd(const void* u, const void* delta, const float* A,
                    const void* B, const void* C,
                    const float* D, const void* z,
-                   const float* delta_bias, int softplus_flag,
+                   const float* delta_bias, int flags,
                    const float* initial_state, const float* chunk_states,
                    const void* dy,
                    void* du, void* ddelta, float* dA, void* dB, void* dC,
@@ -224,7 +242,8 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A,
  *   - Sizes whose workspace (mamba_scan_workspace_size) exceeds 16 MiB are
  *     rejected with MAMBA_ERR_WORKSPACE before anything is launched. For
  *     lengths whose rows are whole 16-byte units that allows
- *     batch * roundup(seqlen, 16) <= 131072 (e.g. 8 x 4096 or 1 x 131072).
+ *     batch * roundup(seqlen, 16) * dstate <= 2097152 (e.g. 8 x 4096 or
+ *     1 x 131072 at dstate 16).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current and caches it: make that
  *     first call before any stream capture is under way.
@@ -238,7 +257,7 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A,
 int mamba_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
                            const void* B, const void* C,
                            const float* D, const void* z,
-                           const float* delta_bias, int softplus_flag,
+                           const float* delta_bias, int flags,
                            void* y, float* final_state,
                            int batch, int dim, int seqlen, int dstate,
                            int io_dtype, void* stream);
@@ -252,13 +271,14 @@ int mamba_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
  *   A           : (dim, dstate) fp32
  *   B, C        : (batch, dstate) io_dtype
  *   D           : (dim) fp32 or NULL;  delta_bias : (dim) fp32 or NULL
+ *   flags       : as for mamba_scan_fwd
  *   y           : (batch, dim) io_dtype, written
  * Returns MAMBA_OK or a negative mamba_status.
  */
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A,
                        const void* B, const void* C,
                        const float* D, const void* z,
-                       const float* delta_bias, int softplus_flag,
+                       const float* delta_bias, int flags,
                        void* y, int batch, int dim, int dstate,
                        int io_dtype, void* stream);
 

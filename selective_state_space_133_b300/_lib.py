@@ -11,9 +11,11 @@ from .build import LIBRARY
 
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
+MAMBA_FLAG_SOFTPLUS = 1
+MAMBA_FLAG_ZOH = 2
 STATUS = {0: "MAMBA_OK", -1: "MAMBA_ERR_NULL", -2: "MAMBA_ERR_SHAPE", -3: "MAMBA_ERR_DTYPE",
           -4: "MAMBA_ERR_ALIGN", -5: "MAMBA_ERR_CUDA", -6: "MAMBA_ERR_DEVICE_TIMEOUT",
-          -7: "MAMBA_ERR_WORKSPACE"}
+          -7: "MAMBA_ERR_WORKSPACE", -8: "MAMBA_ERR_FLAGS"}
 
 # (name, restype, argtypes) of every symbol the header declares.
 _P = ctypes.c_void_p

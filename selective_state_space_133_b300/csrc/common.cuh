@@ -12,11 +12,7 @@
 
 namespace mscan {
 
-constexpr int kDState = 16;  // the state size the kernels are compiled for
-
-// Device error word: 0 = fine, otherwise the mamba_status a kernel reported.
-// Read (and cleared) by mamba_check_device_error on the host.
-__device__ int g_device_error = 0;
+constexpr int kDState = 16;  // the state size of the backward kernel
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -168,7 +164,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return false;
 }
 
-__device__ __forceinline__ void report_device_error(int code) { atomicCAS(&g_device_error, 0, code); }
+// Records `code` in the device error word (0 = fine, otherwise the mamba_status
+// a kernel reported) unless an earlier error is already there. The word lives
+// in the library's host file, which passes its address to the kernels and
+// reads (and clears) it in mamba_check_device_error.
+__device__ __forceinline__ void report_device_error(int* err, int code) { atomicCAS(err, 0, code); }
 
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,

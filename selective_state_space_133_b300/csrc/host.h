@@ -1,0 +1,46 @@
+// Host-side pieces shared by the library's translation units.
+//
+// The forward-scan kernels are instantiated per state size in their own files
+// (scan_fwd_n8.cu ... scan_fwd_n64.cu, compiled in parallel); each of those
+// files defines launch_scan_n for its state size and instantiates no other
+// kernel. Everything else (argument checks, workspace layout, the B/C pack,
+// the row copies, the backward and the state update) lives in mamba_scan.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "scan_fwd.cuh"
+
+namespace mhost {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 3-D TMA tensor map over a tensor with extents (e0, e1, e2), e0 innermost, row
+// pitch `pitch0` elements (>= e0) and plane pitch pitch0 * e1; box (b0, b1, 1).
+// Defined in mamba_scan.cu. Returns false if the map cannot be encoded.
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0, uint64_t e1,
+                 uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1);
+
+// Inputs of one forward launch after the call's preparation: u/delta/z at row
+// pitch `pitch` (the caller's tensors, or copies in the workspace), and the
+// packed B/C rows (batch, Lp, 2N) fp32.
+struct FwdInputs {
+    const void* u;
+    const void* delta;
+    const void* z;   // may be null
+    const float* bc;
+    int pitch, Lp;
+};
+
+// Encodes the tensor maps and launches the forward kernel of state size NS
+// (the instantiation picked by `flags`, bits MAMBA_FLAG_*, and by whether the
+// convolution and z are given). Returns a mamba_status.
+template <typename T, int NS>
+int launch_scan_n(const mscan::ScanArgs& a, const FwdInputs& in, int flags, cudaStream_t stream);
+
+}  // namespace mhost

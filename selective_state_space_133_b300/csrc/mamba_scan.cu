@@ -1,22 +1,34 @@
-// C ABI of libmambascan.so: argument validation, TMA tensor maps, dispatch.
+// C ABI of libmambascan.so: argument validation, workspaces, dispatch.
 //
 // Declared in include/mamba_scan.h. Every check runs on the host before any
 // launch; a rejected call launches nothing and writes nothing. The library
 // keeps no state besides the device error word; mamba_scan_fwd allocates its
-// workspace stream-ordered, mamba_scan_fwd_ws takes it from the caller.
+// workspace stream-ordered, mamba_scan_fwd_ws takes it from the caller. The
+// forward-scan kernels themselves are launched from scan_fwd_n*.cu (one file
+// per state size, see host.h).
 #include <algorithm>
 #include <cstring>
 #include <mutex>
-#include <type_traits>
 
 #include "../../include/mamba_scan.h"
+#include "host.h"
 #include "scan_bwd.cuh"
-#include "scan_fwd.cuh"
 #include "state_update.cuh"
+
+// Device error word: 0 = fine, otherwise the mamba_status a kernel reported
+// (kernels get its address in their arguments). Read and cleared by
+// mamba_check_device_error.
+static __device__ int g_device_error = 0;
 
 namespace {
 
+using mhost::aligned;
+using mhost::round_up;
 using mscan::kDState;
+
+constexpr int kKnownFlags = MAMBA_FLAG_SOFTPLUS | MAMBA_FLAG_ZOH;
+
+bool forward_dstate(int dstate) { return dstate == 8 || dstate == 16 || dstate == 32 || dstate == 64; }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -36,14 +48,34 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// Device address of a file-scope __device__ object on the current device. In
+// host code such an object's name is only a host-side stand-in, so the address
+// comes from cudaGetSymbolAddress, looked up once per device (with that device
+// current) and cached in `cache`. Returns nullptr if the lookup fails.
+constexpr int kMaxDevices = 64;
+std::mutex g_symbol_mutex;
 
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+template <typename Sym>
+void* symbol_address(const Sym& sym, void* (&cache)[kMaxDevices]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_symbol_mutex);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, sym) != cudaSuccess) return nullptr;
+        cache[dev] = p;
+    }
+    return cache[dev];
+}
 
-// 3-D map over a tensor with extents (e0, e1, e2), e0 innermost, row pitch
-// `pitch0` elements (>= e0) and plane pitch pitch0 * e1; box (b0, b1, 1).
-bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0, uint64_t e1,
-                 uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1) {
+void* g_error_addr[kMaxDevices] = {};
+
+int* device_error_word() { return static_cast<int*>(symbol_address(g_device_error, g_error_addr)); }
+
+}  // namespace
+
+bool mhost::make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0,
+                        uint64_t e1, uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {e0, e1, e2};
@@ -55,6 +87,8 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 // Workspace of one scan call: the packed fp32 B/C rows and, when a row of
 // u/delta/z is not a whole number of 16-byte units (TMA strides must be), copies
 // of those tensors at a padded row pitch.
@@ -65,13 +99,13 @@ struct ScanWorkspace {
     size_t bc, u, dl, z, total;  // byte offsets of the parts, and the total
 };
 
-ScanWorkspace scan_workspace(long long batch, long long dim, long long L, size_t es) {
+ScanWorkspace scan_workspace(long long batch, long long dim, long long L, int dstate, size_t es) {
     ScanWorkspace w;
     w.Lp = static_cast<int>(round_up(static_cast<size_t>(L), mscan::kTL));
     w.copy_rows = (static_cast<size_t>(L) * es) % 16 != 0;
     w.pitch = w.copy_rows ? static_cast<int>(round_up(static_cast<size_t>(L), 16 / es)) : static_cast<int>(L);
     w.bc = 0;
-    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * mscan::kBCW * sizeof(float), 256);
+    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * 2 * dstate * sizeof(float), 256);
     const size_t rows = w.copy_rows ? round_up(static_cast<size_t>(batch) * dim * w.pitch * es, 256) : 0;
     w.u = off; off += rows;
     w.dl = off; off += rows;
@@ -80,19 +114,30 @@ ScanWorkspace scan_workspace(long long batch, long long dim, long long L, size_t
     return w;
 }
 
+template <typename T, int NS>
+void launch_pack(const void* B, const void* C, float* bc, int batch, int L, int Lp, cudaStream_t stream) {
+    const long long threads = static_cast<long long>(batch) * Lp;
+    mscan::bc_pack_kernel<T, NS><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const T*>(B), static_cast<const T*>(C), bc, batch, L, Lp);
+}
+
 template <typename T>
-int launch_scan(const mscan::ScanArgs& a, const void* u, const void* delta, const void* z, const void* B,
-                const void* C, int softplus, char* ws, cudaStream_t stream) {
+int launch_scan(mscan::ScanArgs a, const void* u, const void* delta, const void* z, const void* B,
+                const void* C, int flags, int dstate, char* ws, cudaStream_t stream) {
     constexpr size_t es = sizeof(T);
-    const ScanWorkspace w = scan_workspace(a.batch, a.dim, a.seqlen, es);
-    CUtensorMap tm_u, tm_dl, tm_z, tm_bc;
-    memset(&tm_u, 0, sizeof(tm_u)); memset(&tm_dl, 0, sizeof(tm_dl));
-    memset(&tm_z, 0, sizeof(tm_z)); memset(&tm_bc, 0, sizeof(tm_bc));
+    const ScanWorkspace w = scan_workspace(a.batch, a.dim, a.seqlen, dstate, es);
+    if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
+    mhost::FwdInputs in;
+    in.u = u; in.delta = delta; in.z = z; in.bc = nullptr; in.pitch = w.pitch; in.Lp = w.Lp;
     if (a.seqlen > 0) {
         float* bc = reinterpret_cast<float*>(ws + w.bc);
-        const long long pack_threads = static_cast<long long>(a.batch) * w.Lp;
-        mscan::bc_pack_kernel<T><<<static_cast<unsigned>((pack_threads + 255) / 256), 256, 0, stream>>>(
-            static_cast<const T*>(B), static_cast<const T*>(C), bc, a.batch, a.seqlen, w.Lp);
+        in.bc = bc;
+        switch (dstate) {
+            case 8: launch_pack<T, 8>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            case 16: launch_pack<T, 16>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            case 32: launch_pack<T, 32>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            default: launch_pack<T, 64>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+        }
         if (w.copy_rows) {
             const long long rows = static_cast<long long>(a.batch) * a.dim;
             const unsigned blocks = static_cast<unsigned>(
@@ -105,42 +150,36 @@ int launch_scan(const mscan::ScanArgs& a, const void* u, const void* delta, cons
                                                                      reinterpret_cast<T*>(ws + dst[i]), rows,
                                                                      a.seqlen, w.pitch);
             }
-            u = ws + w.u;
-            delta = ws + w.dl;
-            if (z) z = ws + w.z;
+            in.u = ws + w.u;
+            in.delta = ws + w.dl;
+            if (z) in.z = ws + w.z;
         }
-        const auto ty = mscan::Io<T>::kTmaType;
-        const uint32_t bl = mscan::kTL, bd = mscan::kCtaCh;
-        bool ok = make_map_3d(&tm_u, ty, es, u, a.seqlen, a.dim, a.batch, w.pitch, bl, bd) &&
-                  make_map_3d(&tm_dl, ty, es, delta, a.seqlen, a.dim, a.batch, w.pitch, bl, bd) &&
-                  make_map_3d(&tm_bc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), bc, mscan::kBCW, w.Lp,
-                              a.batch, mscan::kBCW, mscan::kBCW, bl);
-        if (ok && z) ok = make_map_3d(&tm_z, ty, es, z, a.seqlen, a.dim, a.batch, w.pitch, bl, bd);
-        if (!ok) return MAMBA_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return MAMBA_ERR_CUDA;
     }
-    const dim3 grid((a.dim + mscan::kCtaCh - 1) / mscan::kCtaCh, a.batch);
-    const int threads = mscan::kScanThreads;
-    auto go = [&](auto sp, auto hz, auto cv) {
-        mscan::scan_fwd_kernel<T, decltype(sp)::value, decltype(hz)::value, decltype(cv)::value>
-            <<<grid, threads, 0, stream>>>(a, tm_u, tm_dl, tm_z, tm_bc);
-    };
-    using Y = std::true_type;
-    using N = std::false_type;
-    const bool conv = a.conv_w != nullptr;
-    if (softplus) {
-        if (z) { if (conv) go(Y{}, Y{}, Y{}); else go(Y{}, Y{}, N{}); }
-        else   { if (conv) go(Y{}, N{}, Y{}); else go(Y{}, N{}, N{}); }
-    } else {
-        if (z) { if (conv) go(N{}, Y{}, Y{}); else go(N{}, Y{}, N{}); }
-        else   { if (conv) go(N{}, N{}, Y{}); else go(N{}, N{}, N{}); }
+    switch (dstate) {
+        case 8: return mhost::launch_scan_n<T, 8>(a, in, flags, stream);
+        case 16: return mhost::launch_scan_n<T, 16>(a, in, flags, stream);
+        case 32: return mhost::launch_scan_n<T, 32>(a, in, flags, stream);
+        default: return mhost::launch_scan_n<T, 64>(a, in, flags, stream);
     }
-    return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+template <typename T, int NS>
+void launch_update_n(const mscan::UpdateArgs& a, bool zoh, cudaStream_t stream) {
+    constexpr int rows = mscan::UpdateGeo<NS>::kRows;
+    const dim3 grid((a.dim + rows - 1) / rows, a.batch);
+    if (zoh) mscan::state_update_kernel<T, NS, true><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
+    else mscan::state_update_kernel<T, NS, false><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
 }
 
 template <typename T>
-int launch_update(const mscan::UpdateArgs& a, cudaStream_t stream) {
-    const dim3 grid((a.dim + mscan::kUpdateCh - 1) / mscan::kUpdateCh, a.batch);
-    mscan::state_update_kernel<T><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
+int launch_update(const mscan::UpdateArgs& a, int dstate, bool zoh, cudaStream_t stream) {
+    switch (dstate) {
+        case 8: launch_update_n<T, 8>(a, zoh, stream); break;
+        case 16: launch_update_n<T, 16>(a, zoh, stream); break;
+        case 32: launch_update_n<T, 32>(a, zoh, stream); break;
+        default: launch_update_n<T, 64>(a, zoh, stream); break;
+    }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
@@ -181,9 +220,7 @@ int launch_bwd(mscan::ScanBwdArgs a, const void* B, const void* C, void* dB, voi
         if (cudaMemsetAsync(a.dbc, 0, static_cast<size_t>(a.batch) * 2 * kDState * w.Lp * sizeof(float), stream) !=
             cudaSuccess)
             return MAMBA_ERR_CUDA;
-        const long long pack_threads = static_cast<long long>(a.batch) * w.Lp;
-        mscan::bc_pack_kernel<T><<<static_cast<unsigned>((pack_threads + 255) / 256), 256, 0, stream>>>(
-            static_cast<const T*>(B), static_cast<const T*>(C), const_cast<float*>(a.bc), a.batch, a.seqlen, w.Lp);
+        launch_pack<T, kDState>(B, C, const_cast<float*>(a.bc), a.batch, a.seqlen, w.Lp, stream);
     }
     const dim3 grid((a.dim + mscan::kBwdCh - 1) / mscan::kBwdCh, a.batch);
     const bool z = a.z != nullptr;
@@ -211,18 +248,19 @@ extern "C" {
 
 // Argument checks shared by the scan entry points (MAMBA_OK or the error code).
 static int check_scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                           const float* D, const void* z, const float* delta_bias, const void* y,
+                           const float* D, const void* z, const float* delta_bias, int flags, const void* y,
                            const float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype,
                            const float* initial_state = nullptr) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
-    if (batch < 0 || dim < 0 || seqlen < 0 || dstate != kDState) return MAMBA_ERR_SHAPE;
+    if (flags & ~kKnownFlags) return MAMBA_ERR_FLAGS;
+    if (batch < 0 || dim < 0 || seqlen < 0 || !forward_dstate(dstate)) return MAMBA_ERR_SHAPE;
     if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
     const size_t es = dtype_size(io_dtype);
     // every flat index must fit in 63 bits of bytes, and TMA strides in 40 bits
     const unsigned long long elems = static_cast<unsigned long long>(batch) * dim * seqlen;
     if (dim > 0 && seqlen > 0 && elems / dim / seqlen != static_cast<unsigned long long>(batch)) return MAMBA_ERR_SHAPE;
     if ((static_cast<unsigned long long>(seqlen) + 16) * dim * es >= (1ull << 40)) return MAMBA_ERR_SHAPE;
-    if ((static_cast<unsigned long long>(seqlen) + 16) * mscan::kBCW * sizeof(float) >= (1ull << 40))
+    if ((static_cast<unsigned long long>(seqlen) + 16) * 2 * dstate * sizeof(float) >= (1ull << 40))
         return MAMBA_ERR_SHAPE;
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!A) return MAMBA_ERR_NULL;
@@ -241,10 +279,10 @@ struct ConvArgs {
 };
 
 static int scan_with_workspace(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                               const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y,
-                               float* final_state, int batch, int dim, int seqlen, int io_dtype, void* workspace,
-                               cudaStream_t s, const float* initial_state = nullptr, ConvArgs conv = ConvArgs(),
-                               float* chunk_states = nullptr) {
+                               const float* D, const void* z, const float* delta_bias, int flags, void* y,
+                               float* final_state, int batch, int dim, int seqlen, int dstate, int io_dtype,
+                               void* workspace, cudaStream_t s, const float* initial_state = nullptr,
+                               ConvArgs conv = ConvArgs(), float* chunk_states = nullptr) {
     mscan::ScanArgs a;
     memset(&a, 0, sizeof(a));
     a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state; a.y = y; a.final_state = final_state;
@@ -252,44 +290,43 @@ static int scan_with_workspace(const void* u, const void* delta, const float* A,
     a.chunk_states = chunk_states;
     a.batch = batch; a.dim = dim; a.seqlen = seqlen;
     char* ws = static_cast<char*>(workspace);
-    const int sp = softplus_flag != 0;
-    return io_dtype == MAMBA_BF16 ? launch_scan<__nv_bfloat16>(a, u, delta, z, B, C, sp, ws, s)
-                                  : launch_scan<float>(a, u, delta, z, B, C, sp, ws, s);
+    return io_dtype == MAMBA_BF16 ? launch_scan<__nv_bfloat16>(a, u, delta, z, B, C, flags, dstate, ws, s)
+                                  : launch_scan<float>(a, u, delta, z, B, C, flags, dstate, ws, s);
 }
 
 size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype) {
-    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate != kDState) return 0;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || !forward_dstate(dstate)) return 0;
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return 0;
-    return scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    return scan_workspace(batch, dim, seqlen, dstate, dtype_size(io_dtype)).total;
 }
 
 int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                      const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                      const float* D, const void* z, const float* delta_bias, int flags,
                       const float* initial_state, void* y, float* final_state, float* chunk_states, int batch,
                       int dim, int seqlen, int dstate, int io_dtype, void* workspace, size_t workspace_bytes,
                       void* stream) {
-    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim, seqlen, dstate,
                              io_dtype, initial_state);
     if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
     if (chunk_states && !aligned(chunk_states, 16)) return MAMBA_ERR_ALIGN;
-    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    const size_t need = scan_workspace(batch, dim, seqlen, dstate, dtype_size(io_dtype)).total;
     if (need > 0) {
         if (!workspace) return MAMBA_ERR_NULL;
         if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
     }
-    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state,
+    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim,
+                               seqlen, dstate, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state,
                                ConvArgs(), chunk_states);
 }
 
 int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float* conv_bias,
                            const void* conv_state, int conv_width, const void* delta, const float* A, const void* B,
-                           const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                           const void* C, const float* D, const void* z, const float* delta_bias, int flags,
                            const float* initial_state, void* y, float* final_state, int batch, int dim,
                            int seqlen, int dstate, int io_dtype, void* workspace, size_t workspace_bytes,
                            void* stream) {
-    int st = check_scan_args(x, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+    int st = check_scan_args(x, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim, seqlen, dstate,
                              io_dtype, initial_state);
     if (st != MAMBA_OK) return st;
     if (conv_width != mscan::kConvW) return MAMBA_ERR_SHAPE;
@@ -298,7 +335,7 @@ int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float*
     if (!aligned(conv_weight, 16) || (conv_bias && !aligned(conv_bias, 4)) ||
         (conv_state && !aligned(conv_state, dtype_size(io_dtype))))
         return MAMBA_ERR_ALIGN;
-    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    const size_t need = scan_workspace(batch, dim, seqlen, dstate, dtype_size(io_dtype)).total;
     if (need > 0) {
         if (!workspace) return MAMBA_ERR_NULL;
         if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
@@ -306,22 +343,22 @@ int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float*
     }
     ConvArgs conv;
     conv.w = conv_weight; conv.b = conv_bias; conv.state = conv_state;
-    return scan_with_workspace(x, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                               seqlen, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state, conv);
+    return scan_with_workspace(x, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim,
+                               seqlen, dstate, io_dtype, workspace, static_cast<cudaStream_t>(stream), initial_state, conv);
 }
 
 int mamba_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-                   const void* z, const float* delta_bias, int softplus_flag, void* y, float* final_state,
+                   const void* z, const float* delta_bias, int flags, void* y, float* final_state,
                    int batch, int dim, int seqlen, int dstate, int io_dtype, void* stream) {
-    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim, seqlen, dstate,
                              io_dtype);
     if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    const size_t need = scan_workspace(batch, dim, seqlen, dstate, dtype_size(io_dtype)).total;
     void* ws = nullptr;
     if (need > 0 && cudaMallocAsync(&ws, need, s) != cudaSuccess) return MAMBA_ERR_CUDA;
-    st = scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                             seqlen, io_dtype, ws, s);
+    st = scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim,
+                             seqlen, dstate, io_dtype, ws, s);
     if (ws && cudaFreeAsync(ws, s) != cudaSuccess && st == MAMBA_OK) st = MAMBA_ERR_CUDA;
     return st;
 }
@@ -343,44 +380,30 @@ static __device__ __align__(256) unsigned char g_scan_scratch[kStaticScratchByte
 
 namespace {
 
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxScratchDevices] = {};
+void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_scan_scratch on the current device. In host code the
-// array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, looked up once per device (with that device current)
-// and cached. Returns nullptr if the lookup fails.
-void* scratch_address() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scan_scratch) != cudaSuccess) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
-}
+// Device address of g_scan_scratch on the current device (looked up once per
+// device with that device current, then cached); nullptr if the lookup fails.
+void* scratch_address() { return symbol_address(g_scan_scratch, g_scratch_addr); }
 
 }  // namespace
 
 extern "C" int mamba_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
                                       const void* C, const float* D, const void* z, const float* delta_bias,
-                                      int softplus_flag, void* y, float* final_state, int batch, int dim,
+                                      int flags, void* y, float* final_state, int batch, int dim,
                                       int seqlen, int dstate, int io_dtype, void* stream) {
-    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, y, final_state, batch, dim, seqlen, dstate,
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim, seqlen, dstate,
                              io_dtype);
     if (st != MAMBA_OK || batch == 0 || dim == 0) return st;
-    const size_t need = scan_workspace(batch, dim, seqlen, dtype_size(io_dtype)).total;
+    const size_t need = scan_workspace(batch, dim, seqlen, dstate, dtype_size(io_dtype)).total;
     if (need > kStaticScratchBytes) return MAMBA_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0 && !(scratch = scratch_address())) return MAMBA_ERR_CUDA;
     // Everything the kernels read from the scratch is written earlier in the
     // same call (the packed B/C rows, padding rows included, and the row
     // copies), so a previous call's contents need no clearing.
-    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, final_state, batch, dim,
-                               seqlen, io_dtype, scratch, static_cast<cudaStream_t>(stream));
+    return scan_with_workspace(u, delta, A, B, C, D, z, delta_bias, flags, y, final_state, batch, dim,
+                               seqlen, dstate, io_dtype, scratch, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" {
@@ -392,13 +415,15 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
 }
 
 int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-                   const void* z, const float* delta_bias, int softplus_flag, const float* initial_state,
+                   const void* z, const float* delta_bias, int flags, const float* initial_state,
                    const float* chunk_states, const void* dy, void* du, void* ddelta, float* dA, void* dB, void* dC, float* dD, void* dz,
                    float* ddelta_bias, float* dinitial_state, int batch, int dim, int seqlen, int dstate,
                    int io_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, dy, nullptr, batch, dim, seqlen, dstate, io_dtype,
+    int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, flags, dy, nullptr, batch, dim, seqlen, dstate, io_dtype,
                              initial_state);
     if (st != MAMBA_OK) return st;
+    if (dstate != kDState) return MAMBA_ERR_SHAPE;
+    if (flags & MAMBA_FLAG_ZOH) return MAMBA_ERR_FLAGS;
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!dA) return MAMBA_ERR_NULL;
     if (seqlen > 0 && (!du || !ddelta || !dB || !dC)) return MAMBA_ERR_NULL;
@@ -421,7 +446,7 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     a.dh0 = dinitial_state;
     a.hck = const_cast<float*>(chunk_states);  // read only when given
     a.have_hck = chunk_states != nullptr;
-    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = softplus_flag != 0;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
     char* ws = static_cast<char*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return io_dtype == MAMBA_BF16 ? launch_bwd<__nv_bfloat16>(a, B, C, dB, dC, ws, s)
@@ -429,10 +454,11 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
 }
 
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A, const void* B, const void* C,
-                       const float* D, const void* z, const float* delta_bias, int softplus_flag, void* y, int batch,
+                       const float* D, const void* z, const float* delta_bias, int flags, void* y, int batch,
                        int dim, int dstate, int io_dtype, void* stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
-    if (batch < 0 || dim < 0 || dstate != kDState) return MAMBA_ERR_SHAPE;
+    if (flags & ~kKnownFlags) return MAMBA_ERR_FLAGS;
+    if (batch < 0 || dim < 0 || !forward_dstate(dstate)) return MAMBA_ERR_SHAPE;
     if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!state || !u || !delta || !A || !B || !C || !y) return MAMBA_ERR_NULL;
@@ -440,7 +466,7 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
     for (const void* p : p16)
         if (!aligned(p, 16)) return MAMBA_ERR_ALIGN;
     const size_t es = dtype_size(io_dtype);
-    // B/C rows are read 16 bytes at a time
+    // B/C rows are read 4 values at a time (16-byte base alignment as for every entry point)
     if (!aligned(B, 16) || !aligned(C, 16)) return MAMBA_ERR_ALIGN;
     const void* pe[] = {u, delta, z, y};
     for (const void* p : pe)
@@ -449,18 +475,20 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
 
     mscan::UpdateArgs a;
     a.state = state; a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C; a.A = A; a.D = D; a.bias = delta_bias;
-    a.y = y; a.batch = batch; a.dim = dim; a.softplus = softplus_flag != 0;
+    a.y = y; a.batch = batch; a.dim = dim; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return io_dtype == MAMBA_BF16 ? launch_update<__nv_bfloat16>(a, s) : launch_update<float>(a, s);
+    const bool zoh = (flags & MAMBA_FLAG_ZOH) != 0;
+    return io_dtype == MAMBA_BF16 ? launch_update<__nv_bfloat16>(a, dstate, zoh, s)
+                                  : launch_update<float>(a, dstate, zoh, s);
 }
 
 int mamba_check_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MAMBA_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, mscan::g_device_error, sizeof(int)) != cudaSuccess) return MAMBA_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MAMBA_ERR_CUDA;
     if (v != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(mscan::g_device_error, &zero, sizeof(int)) != cudaSuccess) return MAMBA_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MAMBA_ERR_CUDA;
         return v;
     }
     return MAMBA_OK;
@@ -470,16 +498,17 @@ const char* mamba_status_string(int status) {
     switch (status) {
         case MAMBA_OK: return "MAMBA_OK";
         case MAMBA_ERR_NULL: return "MAMBA_ERR_NULL: a required pointer is NULL";
-        case MAMBA_ERR_SHAPE: return "MAMBA_ERR_SHAPE: unsupported or out-of-range size";
+        case MAMBA_ERR_SHAPE: return "MAMBA_ERR_SHAPE: unsupported or out-of-range size (dstate 8/16/32/64; backward 16)";
         case MAMBA_ERR_DTYPE: return "MAMBA_ERR_DTYPE: io_dtype is not MAMBA_F32 or MAMBA_BF16";
         case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a base pointer is not aligned as required";
         case MAMBA_ERR_CUDA: return "MAMBA_ERR_CUDA: a CUDA call failed";
         case MAMBA_ERR_DEVICE_TIMEOUT: return "MAMBA_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
         case MAMBA_ERR_WORKSPACE: return "MAMBA_ERR_WORKSPACE: the workspace is smaller than mamba_scan_workspace_size";
+        case MAMBA_ERR_FLAGS: return "MAMBA_ERR_FLAGS: an unknown flag bit, or one this entry point does not support";
         default: return "unknown mamba_status";
     }
 }
 
-int mamba_version(void) { return 200; }
+int mamba_version(void) { return 300; }
 
 }  // extern "C"

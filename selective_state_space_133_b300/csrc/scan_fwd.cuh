@@ -4,11 +4,13 @@
 // ("Mamba 论文精读", youngju.dev, §2.2 and §3.3; gate from §3.4; D skip term from
 // "Mamba的基础知识", weblog-19d, 状态空间模型 section):
 //     dt = softplus(delta + bias)            (or delta + bias)
-//     h  = exp(dt*A[d,:]) * h + dt*B[b,:,l]*u   (h = 0 before l = 0)
+//     h  = exp(dt*A[d,:]) * h + dt*B[b,:,l]*u   (h = h0, or 0, before l = 0)
 //     y  = (C[b,:,l] . h + D[d]*u) * silu(z)
 // with the state kept in registers for the whole sequence and nothing but y
 // (and the optional final state) written back ("mamba->jamba", blog.csdn.net,
 // §2.3: discretise, scan and contract on chip; HBM traffic O(BLD + BLN)).
+// With the ZOH instantiation the input gain dt*B is replaced by the exact
+// zero-order-hold B_bar = (exp(dt*A) - 1) / A * B of the same page's §2.2.
 //
 // Design (B300-first, not the pages' kernel):
 //  * At N = 16 the path is bound by the SM, not by HBM: every (b,l,d,n)
@@ -19,31 +21,33 @@
 //    one wavefront per clock per SM). Each thread therefore walks the whole
 //    sequence for its states sequentially: no cross-thread scan and no carry
 //    fix-up pass, which would add work per element.
-//  * A CTA is one warp = 16 channels of one batch row with its own copy ring,
-//    so no warp ever waits for another. In the recurrence, lane (h, c) =
-//    (lane >> 4, lane & 15) owns states 8h..8h+7 of channel c: each half-warp
-//    reads one B/C address per step (a 16-byte broadcast load, 2 wavefronts),
-//    and the per-(channel, step) values dt and dt*u are shared by two lanes.
+//  * A CTA is one warp with its own copy ring, so no warp ever waits for
+//    another. In the recurrence a lane owns kS = 8 consecutive states of one
+//    channel (4 at N = 8, so that a warp still holds 16 channels): lane
+//    (h, c) = (lane / kCh, lane % kCh) owns states kS*h .. kS*h + kS - 1 of
+//    channel c. The kG = N / kS lanes of a channel read B/C at kG addresses
+//    per step (16-byte broadcast loads), and share the per-(channel, step)
+//    values dt and dt*u. At N = 16 that is 16 channels per CTA.
 //  * The sequence is cut into 16-step chunks. Lane 0 issues 3-D TMA loads of
-//    a chunk's u/delta/z tiles (16 channels x 16 steps) and of the chunk's
-//    packed B/C rows (fp32, [step][B0..15 C0..15], written once per call by
-//    bc_pack_kernel) into a 4-deep ring with one "full" mbarrier per slot (TMA
-//    transaction count); a slot is refilled as soon as the warp is done with
-//    it, and the waits for data are bounded and report a timeout instead of
-//    hanging.
+//    a chunk's u/delta/z tiles (kCh channels x 16 steps) and of the chunk's
+//    packed B/C rows (fp32, [step][B0..N-1 C0..N-1], written once per call by
+//    bc_pack_kernel) into a ring of kStages slots with one "full" mbarrier per
+//    slot (TMA transaction count); a slot is refilled as soon as the warp is
+//    done with it, and the waits for data are bounded and report a timeout
+//    instead of hanging.
 //  * Per chunk there are three phases, run in order:
-//      pre-pass   once per (channel, step), lane (c, j) = (lane >> 1, lane & 1)
-//                 taking steps 8j..8j+7 of channel c: dt and dt*u, stored as
-//                 float2 pairs that the recurrence uses, each value broadcast
-//                 to both halves, as packed f32x2 operands;
-//      recurrence per lane, 16 steps x 8 states with packed FMUL2/FFMA2 and
+//      pre-pass   once per (channel, step), lane (c, j) = (lane / kG, lane % kG)
+//                 taking steps kSP*j .. kSP*j + kSP - 1 of channel c: dt and
+//                 dt*u, stored as float2 pairs that the recurrence uses as
+//                 packed f32x2 operands;
+//      recurrence per lane, 16 steps x kS states with packed FMUL2/FFMA2 and
 //                 software-pipelined by one step; the step's partial C.h of
-//                 the lane's 8 states goes to shared memory (one 16-byte store
+//                 the lane's states goes to shared memory (one 16-byte store
 //                 per 4 steps);
-//      epilogue   once per (channel, step), same lanes as the pre-pass: the two
-//                 partials + D*u, times silu(z), rounded, one 16-byte store.
-//    All shared-memory strides are chosen so that these accesses are free of
-//    bank conflicts.
+//      epilogue   once per (channel, step), same lanes as the pre-pass: the kG
+//                 partials + D*u, times silu(z), rounded, vector stores.
+//    The shared-memory strides are chosen so that the recurrence's accesses
+//    are free of bank conflicts.
 //  * Steps past the end of the sequence get dt = 0 (exp(0) = 1, zero input),
 //    so the padded tail leaves the state unchanged and the final state needs
 //    no masking.
@@ -53,16 +57,33 @@
 
 namespace mscan {
 
-constexpr int kTL = 16;                  // steps per chunk
-constexpr int kCtaCh = 16;               // channels per CTA (one warp)
-constexpr int kBCW = 2 * kDState;        // floats per step in the packed B/C buffer
-constexpr int kWP = kTL + 2;             // W row stride (float2): 16-byte rows, distinct banks
-constexpr int kPJ = kCtaCh * 4 + 8;      // partial sums: stride between 4-step groups (floats)
-constexpr int kPH = (kTL / 4) * kPJ;     // partial sums: stride between state halves (floats)
-constexpr int kStages = 4;               // TMA ring depth
+constexpr int kTL = 16;          // steps per chunk
 constexpr int kScanThreads = 32;
+constexpr int kConvW = 4;        // width of the causal convolution fused in front of the scan
 
-constexpr int kConvW = 4;  // width of the causal convolution fused in front of the scan
+// Geometry of the forward kernel for state size NS.
+template <int NS>
+struct FwdGeo {
+    static_assert(NS == 8 || NS == 16 || NS == 32 || NS == 64, "state sizes 8, 16, 32 and 64 are compiled");
+    static constexpr int kS = NS == 8 ? 4 : 8;    // states per recurrence lane
+    static constexpr int kG = NS / kS;            // lanes per channel
+    static constexpr int kCh = 32 / kG;           // channels per CTA (one warp)
+    static constexpr int kSP = kTL / kG;          // steps per lane in the pre-pass and epilogue
+    static constexpr int kBCW = 2 * NS;           // floats per step in the packed B/C buffer
+    static constexpr int kWP = kTL + 2;           // W row stride (float2): 16-byte rows
+    // P row strides: a quarter-warp's 16-byte stores of the recurrence land in
+    // distinct banks (kPH = 16 mod 32 words when two state groups share a
+    // quarter-warp), and so do the epilogue's loads of 4-step groups.
+    static constexpr int kPJ = kCh * 4 + (kG == 8 ? 4 : 8);  // stride between 4-step groups (floats)
+    static constexpr int kPH = (kTL / 4) * kPJ;              // stride between state groups (floats)
+    static constexpr int kStages = NS == 64 ? 3 : 4;         // TMA ring depth (N = 64: B/C rows are 8 KB a chunk)
+    // y is stored kSP steps at a time in vectors of at most 16 bytes; whole
+    // vectors need the row length to be a multiple of this many steps
+    template <typename T>
+    __host__ __device__ static constexpr int vec_steps() {
+        return 16 / static_cast<int>(sizeof(T)) < kSP ? 16 / static_cast<int>(sizeof(T)) : kSP;
+    }
+};
 
 struct ScanArgs {
     const float* A;
@@ -71,7 +92,8 @@ struct ScanArgs {
     const float* h0;     // state before the first step, may be null (zero)
     void* y;
     float* final_state;  // may be null
-    float* chunk_states; // (batch, dim, ceil(seqlen / 16), 16): the state before every chunk; may be null
+    float* chunk_states; // (batch, dim, ceil(seqlen / 16), N): the state before every chunk; may be null
+    int* err;            // device error word
     int batch, dim, seqlen;
     // With the fused convolution (the kernel's CONV instantiation) the u tiles
     // hold the convolution's input x, and u = silu(sum_k w[k] x[l-3+k] + b):
@@ -80,68 +102,107 @@ struct ScanArgs {
     const void* conv_state;  // (batch, dim, kConvW - 1) io dtype: x before step 0, oldest first; may be null
 };
 
-template <typename T>
+template <typename T, int NS>
 struct ScanStage {
-    alignas(128) T u[kCtaCh][kTL];
-    alignas(128) T dl[kCtaCh][kTL];
-    alignas(128) T z[kCtaCh][kTL];
-    alignas(128) float bc[kTL][kBCW];
+    using G = FwdGeo<NS>;
+    alignas(128) T u[G::kCh][kTL];
+    alignas(128) T dl[G::kCh][kTL];
+    alignas(128) T z[G::kCh][kTL];
+    alignas(128) float bc[kTL][G::kBCW];
 };
 
-template <typename T>
+template <typename T, int NS>
 struct ScanSmem {
-    ScanStage<T> st[kStages];
-    alignas(16) float2 W[kCtaCh][kWP];   // {dt, dt*u} per (channel, step)
-    alignas(16) float P[2 * kPH];        // [state half][4-step group][channel][4 steps]
-    alignas(8) uint64_t full[kStages];   // TMA transaction barrier per slot
-    alignas(16) float U[kCtaCh][kTL + 1];  // u after the convolution (CONV only)
-    float XH[2][kCtaCh][kConvW - 1];     // the last inputs x of the previous chunk (CONV only)
+    using G = FwdGeo<NS>;
+    ScanStage<T, NS> st[G::kStages];
+    alignas(16) float2 W[G::kCh][G::kWP];      // {dt, dt*u} per (channel, step); {dt, u} with ZOH
+    alignas(16) float P[G::kG * G::kPH];       // [state group][4-step group][channel][4 steps]
+    alignas(8) uint64_t full[G::kStages];      // TMA transaction barrier per slot
+    alignas(16) float U[G::kCh][kTL + 1];      // u after the convolution (CONV only)
+    float XH[2][G::kCh][kConvW - 1];           // the last inputs x of the previous chunk (CONV only)
 };
 
 // ------------------------------------------------------------ helpers ------
 
-// Eight consecutive values (16-byte aligned for bf16, 32-byte for fp32) as fp32.
-__device__ __forceinline__ void lds8(const float* p, float (&v)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0];
-    const float4 b = reinterpret_cast<const float4*>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void lds8(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 q = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// n consecutive values from shared memory as fp32 (aligned to n elements).
+template <int n>
+__device__ __forceinline__ void lds_n(const float* p, float (&v)[n]) {
+    if constexpr (n % 4 == 0) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        v[2 * j + 0] = __uint_as_float(w[j] << 16);
-        v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        for (int i = 0; i < n / 4; ++i) {
+            const float4 q = reinterpret_cast<const float4*>(p)[i];
+            v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+        }
+    } else {
+        static_assert(n == 2, "pairs at least");
+        const float2 q = *reinterpret_cast<const float2*>(p);
+        v[0] = q.x; v[1] = q.y;
+    }
+}
+__device__ __forceinline__ void bf16x2_to_f(uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+}
+template <int n>
+__device__ __forceinline__ void lds_n(const __nv_bfloat16* p, float (&v)[n]) {
+    if constexpr (n % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < n / 8; ++i) {
+            const uint4 q = reinterpret_cast<const uint4*>(p)[i];
+            bf16x2_to_f(q.x, v[8 * i], v[8 * i + 1]); bf16x2_to_f(q.y, v[8 * i + 2], v[8 * i + 3]);
+            bf16x2_to_f(q.z, v[8 * i + 4], v[8 * i + 5]); bf16x2_to_f(q.w, v[8 * i + 6], v[8 * i + 7]);
+        }
+    } else if constexpr (n == 4) {
+        const uint2 q = *reinterpret_cast<const uint2*>(p);
+        bf16x2_to_f(q.x, v[0], v[1]); bf16x2_to_f(q.y, v[2], v[3]);
+    } else {
+        static_assert(n == 2, "pairs at least");
+        bf16x2_to_f(*reinterpret_cast<const uint32_t*>(p), v[0], v[1]);
     }
 }
 
-// Eight consecutive outputs to global memory; `vec` = all 8 are in range and
-// the address is aligned for vector stores; otherwise the first `valid` go out
-// one by one.
-__device__ __forceinline__ void stg8(float* p, const float (&v)[8], bool vec, int valid) {
+// n consecutive outputs to global memory; `vec` = all n are in range and the
+// address is aligned for vector stores (16 bytes, or the whole n elements if
+// smaller); otherwise the first `valid` go out one by one.
+template <int n>
+__device__ __forceinline__ void stg_n(float* p, const float (&v)[n], bool vec, int valid) {
     if (vec) {
-        reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-        reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        if constexpr (n % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < n / 4; ++i)
+                reinterpret_cast<float4*>(p)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else {
+            *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < n; ++i)
             if (i < valid) p[i] = v[i];
     }
 }
-__device__ __forceinline__ void stg8(__nv_bfloat16* p, const float (&v)[8], bool vec, int valid) {
-    __nv_bfloat162 o[4];
+template <int n>
+__device__ __forceinline__ void stg_n(__nv_bfloat16* p, const float (&v)[n], bool vec, int valid) {
+    uint32_t w[n / 2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    for (int j = 0; j < n / 2; ++j) {
+        const __nv_bfloat162 o = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        w[j] = *reinterpret_cast<const uint32_t*>(&o);
+    }
     if (vec) {
-        *reinterpret_cast<uint4*>(p) = make_uint4(*reinterpret_cast<const uint32_t*>(&o[0]),
-                                                  *reinterpret_cast<const uint32_t*>(&o[1]),
-                                                  *reinterpret_cast<const uint32_t*>(&o[2]),
-                                                  *reinterpret_cast<const uint32_t*>(&o[3]));
+        if constexpr (n % 8 == 0) {
+#pragma unroll
+            for (int i = 0; i < n / 8; ++i)
+                reinterpret_cast<uint4*>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else if constexpr (n == 4) {
+            *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        } else {
+            *reinterpret_cast<uint32_t*>(p) = w[0];
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < valid) p[i] = (i & 1) ? o[i >> 1].y : o[i >> 1].x;
+        for (int i = 0; i < n; ++i)
+            if (i < valid) p[i] = __ushort_as_bfloat16(static_cast<unsigned short>((i & 1) ? (w[i >> 1] >> 16)
+                                                                                           : (w[i >> 1] & 0xffffu)));
     }
 }
 
@@ -159,25 +220,48 @@ __device__ __forceinline__ float2 gate2(float2 y, float2 z) {
     return __fmul2_rn(__fmul2_rn(y, z), r);
 }
 
+// Exact zero-order-hold gain factor on a pair of states, given x2 = dt*a*log2(e)
+// (the ex2 argument), e = 2^x2 = exp(dt*a), dt and 1/a:
+//     M = (exp(dt a) - 1) / a = dt * phi(dt a),   phi(x) = (e^x - 1) / x.
+// Where |dt a| >= 1/64 the quotient (e - 1) * (1/a) is used: e - 1 is exact
+// in fp32 there and the few-ulp error of e is at most ~1e-5 of e - 1. Below
+// that, e - 1 would cancel, and phi is taken from its Taylor series
+// 1 + x/2 + x^2/6 (next term x^3/24 <= 1.6e-7), written in x2. At dt*a = 0
+// (A = 0, or a padding step) this gives M = dt, the limit.
+__device__ __forceinline__ float2 zoh_gain2(float2 x2, float2 e, float2 dt, float2 inv_a) {
+    constexpr float kC1 = 0.34657359027997264f;   // ln2 / 2
+    constexpr float kC2 = 0.08007550231970023f;   // ln2^2 / 6
+    constexpr float kSmall = 0.022542110013890053f;  // (1/64) * log2(e): |dt a| < 1/64
+    float2 t = __ffma2_rn(x2, make_float2(kC2, kC2), make_float2(kC1, kC1));
+    t = __ffma2_rn(t, x2, make_float2(1.f, 1.f));
+    const float2 ms = __fmul2_rn(t, dt);
+    const float2 ml = __fmul2_rn(__fadd2_rn(e, make_float2(-1.f, -1.f)), inv_a);
+    return make_float2(fabsf(x2.x) < kSmall ? ms.x : ml.x, fabsf(x2.y) < kSmall ? ms.y : ml.y);
+}
+
 // ------------------------------------------------------------- kernel ------
 
-template <typename T, bool SOFTPLUS, bool HAS_Z, bool CONV>
+template <typename T, int NS, bool SOFTPLUS, bool HAS_Z, bool CONV, bool ZOH>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_dl, const __grid_constant__ CUtensorMap tm_z,
                 const __grid_constant__ CUtensorMap tm_bc) {
-    __shared__ ScanSmem<T> sm;
+    using G = FwdGeo<NS>;
+    constexpr int kS = G::kS, kG = G::kG, kCh = G::kCh, kSP = G::kSP, kBCW = G::kBCW;
+    constexpr int kPJ = G::kPJ, kPH = G::kPH, kStages = G::kStages;
+    constexpr int H = kS / 2;  // state pairs per recurrence lane
+    __shared__ ScanSmem<T, NS> sm;
     const int lane = threadIdx.x;
     const int b = blockIdx.y;
-    const int d0 = blockIdx.x * kCtaCh;
+    const int d0 = blockIdx.x * kCh;
     const int L = a.seqlen;
     const int n = (L + kTL - 1) / kTL;
 
     // Chunk k's tiles into slot k % kStages (lane 0 only).
     auto issue = [&](int k) {
-        constexpr uint32_t kTile = kCtaCh * kTL * sizeof(T);
+        constexpr uint32_t kTile = kCh * kTL * sizeof(T);
         constexpr uint32_t kStageBytes = (HAS_Z ? 3u : 2u) * kTile + kTL * kBCW * 4u;
-        ScanStage<T>& S = sm.st[k % kStages];
+        ScanStage<T, NS>& S = sm.st[k % kStages];
         uint64_t* bar = &sm.full[k % kStages];
         mbar_arrive_expect_tx(bar, kStageBytes);
         const int l0 = k * kTL;
@@ -195,28 +279,32 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     }
     __syncwarp();
 
-    // Recurrence lanes: channel rc, states 8*rh .. 8*rh+7.
-    const int rc = lane & 15, rh = lane >> 4;
-    // Pre-pass / epilogue lanes: channel ec, steps 8*ej .. 8*ej+7 of each chunk.
-    const int ec = lane >> 1, ej = lane & 1;
+    // Recurrence lanes: channel rc, states kS*rh .. kS*rh + kS - 1.
+    const int rc = lane % kCh, rh = lane / kCh;
+    // Pre-pass / epilogue lanes: channel ec, steps kSP*ej .. kSP*ej + kSP - 1 of each chunk.
+    const int ec = lane / kG, ej = lane % kG;
 
     const int rd = d0 + rc < a.dim ? d0 + rc : a.dim - 1;  // clamped for parameter loads
-    float2 A2[4];
+    float2 A2[H], IA[H];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * kDState + 8 * rh + 2 * i);
+    for (int i = 0; i < H; ++i) {
+        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i);
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
+        if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);  // inf at a = 0: that branch is never taken there
     }
-    float2 h[4];
+    float2 h[H];
     if (a.h0) {
-        const float4* hp = reinterpret_cast<const float4*>(a.h0 + (static_cast<size_t>(b) * a.dim + rd) * kDState +
-                                                           8 * rh);
-        const float4 p0 = hp[0], p1 = hp[1];
-        h[0] = make_float2(p0.x, p0.y); h[1] = make_float2(p0.z, p0.w);
-        h[2] = make_float2(p1.x, p1.y); h[3] = make_float2(p1.z, p1.w);
+        const float4* hp = reinterpret_cast<const float4*>(a.h0 + (static_cast<size_t>(b) * a.dim + rd) * NS +
+                                                           kS * rh);
+#pragma unroll
+        for (int q = 0; q < kS / 4; ++q) {
+            const float4 p = hp[q];
+            h[2 * q] = make_float2(p.x, p.y);
+            h[2 * q + 1] = make_float2(p.z, p.w);
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < H; ++i) h[i] = make_float2(0.f, 0.f);
     }
 
     const int ed = d0 + ec;
@@ -229,7 +317,7 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + static_cast<size_t>(edc) * kConvW);
         cw[0] = w4.x; cw[1] = w4.y; cw[2] = w4.z; cw[3] = w4.w;
         cb = a.conv_b ? a.conv_b[edc] : 0.f;
-        // the inputs before step 0 (read by the same lane in the first pre-pass)
+        // the inputs before step 0 (read in the first pre-pass)
         if (ej == 0) {
 #pragma unroll
             for (int m = 0; m < kConvW - 1; ++m)
@@ -239,9 +327,9 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                     : 0.f;
         }
     }
-    // this lane's output: steps 8*ej .. 8*ej+7 of every chunk of channel ed
-    T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + 8 * ej;
-    const bool vec_ok = eactive && (L & 7) == 0;
+    // this lane's output: steps kSP*ej .. kSP*ej + kSP - 1 of every chunk of channel ed
+    T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + kSP * ej;
+    const bool vec_ok = eactive && (L % G::template vec_steps<T>()) == 0;
 
     // Bounded wait for the tiles of chunk k in slot s; warp-uniform verdict. On
     // a timeout the warp records the error and waits (bounded again) for the
@@ -249,7 +337,7 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     auto wait_full = [&](int s, int k) -> bool {
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.full[s], (k / kStages) & 1));
         if (!ok) {
-            report_device_error(-6);
+            report_device_error(a.err, -6);
             for (int j = k + 1; j < n && j < k + kStages; ++j)
                 mbar_wait_bounded(&sm.full[j % kStages], (j / kStages) & 1);
         }
@@ -267,44 +355,47 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     };
 
     // --- the three phases --------------------------------------------------
-    auto prepass = [&](const ScanStage<T>& S, int k) {
-        float uv[8], dv[8];
-        lds8(&S.u[ec][8 * ej], uv);
-        lds8(&S.dl[ec][8 * ej], dv);
+    auto prepass = [&](const ScanStage<T, NS>& S, int k) {
+        float uv[kSP], dv[kSP];
+        lds_n<kSP>(&S.u[ec][kSP * ej], uv);
+        lds_n<kSP>(&S.dl[ec][kSP * ej], dv);
         if (CONV) {
-            // the 3 inputs before this lane's first step: from this chunk (second
-            // half) or from the previous chunk's last inputs (first half)
-            float xm[kConvW - 1];
+            // the 3 inputs before this lane's first step: from this chunk's
+            // tile, or (before step 0 of the chunk) from the previous chunk's
+            // last inputs; both indices stay in range whichever is read
+            float xs[kSP + kConvW - 1];
 #pragma unroll
-            for (int m = 0; m < kConvW - 1; ++m)
-                xm[m] = ej ? Io<T>::to_f(S.u[ec][8 - (kConvW - 1) + m]) : sm.XH[(k + 1) & 1][ec][m];
-            if (ej) {
-#pragma unroll
-                for (int m = 0; m < kConvW - 1; ++m) sm.XH[k & 1][ec][m] = uv[8 - (kConvW - 1) + m];
+            for (int m = 0; m < kConvW - 1; ++m) {
+                const int idx = kSP * ej - (kConvW - 1) + m;
+                xs[m] = idx >= 0 ? Io<T>::to_f(S.u[ec][idx >= 0 ? idx : 0])
+                                 : sm.XH[(k + 1) & 1][ec][idx < 0 ? idx + kConvW - 1 : 0];
             }
-            float xs[8 + kConvW - 1];
+            if (ej == kG - 1) {  // this chunk's last inputs, for the next chunk
 #pragma unroll
-            for (int m = 0; m < kConvW - 1; ++m) xs[m] = xm[m];
+                for (int m = 0; m < kConvW - 1; ++m)
+                    sm.XH[k & 1][ec][m] = Io<T>::to_f(S.u[ec][kTL - (kConvW - 1) + m]);
+            }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xs[kConvW - 1 + i] = uv[i];
+            for (int i = 0; i < kSP; ++i) xs[kConvW - 1 + i] = uv[i];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < kSP; ++i) {
                 float acc = cb;
 #pragma unroll
                 for (int m = 0; m < kConvW; ++m) acc = fmaf(cw[m], xs[i + m], acc);
                 uv[i] = silu_f(acc);
-                sm.U[ec][8 * ej + i] = uv[i];
+                sm.U[ec][kSP * ej + i] = uv[i];
             }
         }
         const float2 bb = make_float2(bias, bias);
-        float4* W = reinterpret_cast<float4*>(&sm.W[ec][8 * ej]);
-        const int lr = k * kTL + 8 * ej;  // first step of this lane's eight
+        float4* W = reinterpret_cast<float4*>(&sm.W[ec][kSP * ej]);
+        const int lr = k * kTL + kSP * ej;  // first step of this lane's kSP
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kSP / 2; ++i) {
             float2 x = __fadd2_rn(make_float2(dv[2 * i], dv[2 * i + 1]), bb);
             if (SOFTPLUS) x = softplus2(x);
-            float2 w = __fmul2_rn(x, make_float2(uv[2 * i], uv[2 * i + 1]));
-            if (lr + 8 > L) {  // sequence tail: padding steps leave the state unchanged
+            const float2 uu = make_float2(uv[2 * i], uv[2 * i + 1]);
+            float2 w = ZOH ? uu : __fmul2_rn(x, uu);
+            if (lr + kSP > L) {  // sequence tail: padding steps leave the state unchanged
                 if (lr + 2 * i >= L) { x.x = 0.f; w.x = 0.f; }
                 if (lr + 2 * i + 1 >= L) { x.y = 0.f; w.y = 0.f; }
             }
@@ -313,31 +404,35 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     };
 
     // The recurrence is software-pipelined by one step: the loads, the ex2 of
-    // dt*A and dt*u*B of step t+1 are issued before the state update of step t
-    // uses them. The next step's ex2 sit between the current step's C.h FMAs,
-    // so the MUFU and FMA pipes are fed alternately.
-    auto recurrence = [&](const ScanStage<T>& S) {
+    // dt*A and the input term of step t+1 are issued before the state update
+    // of step t uses them. The next step's ex2 sit between the current step's
+    // C.h FMAs, so the MUFU and FMA pipes are fed alternately.
+    auto recurrence = [&](const ScanStage<T, NS>& S) {
         const float2* W = &sm.W[rc][0];
-        const float* bc = &S.bc[0][0];
+        const float* bc = &S.bc[0][0] + kS * rh;  // B of this lane's states; their C is NS floats further
         float* P = &sm.P[rh * kPH + 4 * rc];
-        float2 e[4], pb[4], cv[4];
+        auto load_bc = [&](int t, float2 (&bn)[H], float2 (&cn)[H]) {
+#pragma unroll
+            for (int q = 0; q < kS / 4; ++q) {
+                const float4 bq = *reinterpret_cast<const float4*>(bc + t * kBCW + 4 * q);
+                const float4 cq = *reinterpret_cast<const float4*>(bc + t * kBCW + NS + 4 * q);
+                bn[2 * q] = make_float2(bq.x, bq.y); bn[2 * q + 1] = make_float2(bq.z, bq.w);
+                cn[2 * q] = make_float2(cq.x, cq.y); cn[2 * q + 1] = make_float2(cq.z, cq.w);
+            }
+        };
+        float2 e[H], pb[H], cv[H];
         // step 0's operands
         {
             const float2 w = W[0];
-            const float4 b0 = *reinterpret_cast<const float4*>(bc + 8 * rh);
-            const float4 b1 = *reinterpret_cast<const float4*>(bc + 8 * rh + 4);
-            const float4 c0 = *reinterpret_cast<const float4*>(bc + kDState + 8 * rh);
-            const float4 c1 = *reinterpret_cast<const float4*>(bc + kDState + 8 * rh + 4);
+            float2 bn[H];
+            load_bc(0, bn, cv);
             const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
-            const float2 bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                                  make_float2(b1.z, b1.w)};
-            cv[0] = make_float2(c0.x, c0.y); cv[1] = make_float2(c0.z, c0.w);
-            cv[2] = make_float2(c1.x, c1.y); cv[3] = make_float2(c1.z, c1.w);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < H; ++i) {
                 const float2 x = __fmul2_rn(dd, A2[i]);
                 e[i] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                pb[i] = __fmul2_rn(du, bv[i]);
+                pb[i] = __fmul2_rn(du, bn[i]);
+                if (ZOH) pb[i] = __fmul2_rn(zoh_gain2(x, e[i], dd, IA[i]), pb[i]);
             }
         }
 #pragma unroll
@@ -348,32 +443,27 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 const int t = t0 + i;
                 const int tn = t + 1 < kTL ? t + 1 : t;  // the last step loads nothing new (values unused)
                 const float2 w = W[tn];
-                const float4 b0 = *reinterpret_cast<const float4*>(bc + tn * kBCW + 8 * rh);
-                const float4 b1 = *reinterpret_cast<const float4*>(bc + tn * kBCW + 8 * rh + 4);
-                const float4 c0 = *reinterpret_cast<const float4*>(bc + tn * kBCW + kDState + 8 * rh);
-                const float4 c1 = *reinterpret_cast<const float4*>(bc + tn * kBCW + kDState + 8 * rh + 4);
+                float2 bn[H], cn[H];
+                load_bc(tn, bn, cn);
                 const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
-                const float2 bn[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                                      make_float2(b1.z, b1.w)};
-                const float2 cn[4] = {make_float2(c0.x, c0.y), make_float2(c0.z, c0.w), make_float2(c1.x, c1.y),
-                                      make_float2(c1.z, c1.w)};
                 // Written in an issue-friendly order (a warp issues in order):
                 // every result is consumed a few independent instructions later.
 #pragma unroll
-                for (int j = 0; j < 4; ++j) h[j] = __ffma2_rn(e[j], h[j], pb[j]);   // step t
-                float2 x[4];
+                for (int j = 0; j < H; ++j) h[j] = __ffma2_rn(e[j], h[j], pb[j]);   // step t
+                float2 x[H];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = __fmul2_rn(dd, A2[j]);             // step t+1
+                for (int j = 0; j < H; ++j) x[j] = __fmul2_rn(dd, A2[j]);             // step t+1
                 float2 acc = __fmul2_rn(cv[0], h[0]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < H; ++j) {
                     if (t + 1 < kTL) e[j] = make_float2(ex2_approx(x[j].x), ex2_approx(x[j].y));
-                    if (j < 3) acc = __ffma2_rn(cv[j + 1], h[j + 1], acc);
+                    if (j < H - 1) acc = __ffma2_rn(cv[j + 1], h[j + 1], acc);
                 }
                 if (t + 1 < kTL) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < H; ++j) {
                         pb[j] = __fmul2_rn(du, bn[j]);
+                        if (ZOH) pb[j] = __fmul2_rn(zoh_gain2(x[j], e[j], dd, IA[j]), pb[j]);
                         cv[j] = cn[j];
                     }
                 }
@@ -383,40 +473,61 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         }
     };
 
-    auto epilogue = [&](const ScanStage<T>& S, int k) {
-        // steps 8*ej .. 8*ej+7 are the 4-step groups 2*ej and 2*ej+1
-        const float* P0 = &sm.P[(2 * ej) * kPJ + 4 * ec];
-        const float4 a0 = *reinterpret_cast<const float4*>(P0);
-        const float4 a1 = *reinterpret_cast<const float4*>(P0 + kPJ);
-        const float4 b0 = *reinterpret_cast<const float4*>(P0 + kPH);
-        const float4 b1 = *reinterpret_cast<const float4*>(P0 + kPH + kPJ);
-        float2 y[4] = {__fadd2_rn(make_float2(a0.x, a0.y), make_float2(b0.x, b0.y)),
-                       __fadd2_rn(make_float2(a0.z, a0.w), make_float2(b0.z, b0.w)),
-                       __fadd2_rn(make_float2(a1.x, a1.y), make_float2(b1.x, b1.y)),
-                       __fadd2_rn(make_float2(a1.z, a1.w), make_float2(b1.z, b1.w))};
-        float uv[8];
+    auto epilogue = [&](const ScanStage<T, NS>& S, int k) {
+        // the kG partial sums of each of this lane's steps
+        float y[kSP];
+        const float* P0 = &sm.P[4 * ec];
+        if constexpr (kSP >= 4) {
+#pragma unroll
+            for (int g = 0; g < kSP / 4; ++g) {
+                const float* pg = P0 + ((kSP / 4) * ej + g) * kPJ;
+                const float4 s = *reinterpret_cast<const float4*>(pg);
+                float2 lo = make_float2(s.x, s.y), hi = make_float2(s.z, s.w);
+#pragma unroll
+                for (int r = 1; r < kG; ++r) {
+                    const float4 q = *reinterpret_cast<const float4*>(pg + r * kPH);
+                    lo = __fadd2_rn(lo, make_float2(q.x, q.y));
+                    hi = __fadd2_rn(hi, make_float2(q.z, q.w));
+                }
+                y[4 * g] = lo.x; y[4 * g + 1] = lo.y; y[4 * g + 2] = hi.x; y[4 * g + 3] = hi.y;
+            }
+        } else {  // two steps: half of a 4-step group
+            const float* pg = P0 + (ej / 2) * kPJ + 2 * (ej % 2);
+            float2 s = *reinterpret_cast<const float2*>(pg);
+#pragma unroll
+            for (int r = 1; r < kG; ++r) s = __fadd2_rn(s, *reinterpret_cast<const float2*>(pg + r * kPH));
+            y[0] = s.x; y[1] = s.y;
+        }
+        float uv[kSP];
         if (CONV) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) uv[i] = sm.U[ec][8 * ej + i];
+            for (int i = 0; i < kSP; ++i) uv[i] = sm.U[ec][kSP * ej + i];
         } else {
-            lds8(&S.u[ec][8 * ej], uv);
+            lds_n<kSP>(&S.u[ec][kSP * ej], uv);
         }
+        float zv[kSP];
+        if (HAS_Z) lds_n<kSP>(&S.z[ec][kSP * ej], zv);
         const float2 DD = make_float2(Dd, Dd);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] = __ffma2_rn(DD, make_float2(uv[2 * i], uv[2 * i + 1]), y[i]);
-        if (HAS_Z) {
-            float zv[8];
-            lds8(&S.z[ec][8 * ej], zv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) y[i] = gate2(y[i], make_float2(zv[2 * i], zv[2 * i + 1]));
+        for (int i = 0; i < kSP / 2; ++i) {
+            float2 yy = __ffma2_rn(DD, make_float2(uv[2 * i], uv[2 * i + 1]), make_float2(y[2 * i], y[2 * i + 1]));
+            if (HAS_Z) yy = gate2(yy, make_float2(zv[2 * i], zv[2 * i + 1]));
+            y[2 * i] = yy.x;
+            y[2 * i + 1] = yy.y;
         }
-        const float out[8] = {y[0].x, y[0].y, y[1].x, y[1].y, y[2].x, y[2].y, y[3].x, y[3].y};
-        const int l = k * kTL + 8 * ej;
-        if (vec_ok && l + 8 <= L) {
-            stg8(yrow + k * kTL, out, true, 8);
+        const int l = k * kTL + kSP * ej;
+        if (vec_ok && l + kSP <= L) {
+            stg_n<kSP>(yrow + k * kTL, y, true, kSP);
         } else if (eactive && l < L) {
-            stg8(yrow + k * kTL, out, false, L - l);
+            stg_n<kSP>(yrow + k * kTL, y, false, L - l);
         }
+    };
+
+    // this lane's states as 16-byte groups, to global memory
+    auto store_state = [&](float* p) {
+#pragma unroll
+        for (int q = 0; q < kS / 4; ++q)
+            reinterpret_cast<float4*>(p)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
     };
 
     // --- main loop ----------------------------------------------------------
@@ -429,17 +540,14 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         if (!wait_full(0, 0)) return;
         prepass(sm.st[0], 0);
         __syncwarp();
-        float* const ck = a.chunk_states ? a.chunk_states + (static_cast<size_t>(b) * a.dim + rd) * n * kDState + 8 * rh
-                                         : nullptr;
+        float* const ck = a.chunk_states
+            ? a.chunk_states + (static_cast<size_t>(b) * a.dim + rd) * n * NS + kS * rh
+            : nullptr;
         const bool ck_store = ck && d0 + rc < a.dim;
 #pragma unroll 1
         for (int k = 0; k < n; ++k) {
-            const ScanStage<T>& S = sm.st[k % kStages];
-            if (ck_store) {  // the state before chunk k, for the backward
-                float4* p = reinterpret_cast<float4*>(ck + static_cast<size_t>(k) * kDState);
-                p[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-                p[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
-            }
+            const ScanStage<T, NS>& S = sm.st[k % kStages];
+            if (ck_store) store_state(ck + static_cast<size_t>(k) * NS);  // the state before chunk k, for the backward
             recurrence(S);
             __syncwarp();
             epilogue(S, k);
@@ -454,19 +562,15 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         }
     }
 
-    if (a.final_state && d0 + rc < a.dim) {
-        float4* fs = reinterpret_cast<float4*>(a.final_state +
-                                               (static_cast<size_t>(b) * a.dim + d0 + rc) * kDState + 8 * rh);
-        fs[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-        fs[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
-    }
+    if (a.final_state && d0 + rc < a.dim)
+        store_state(a.final_state + (static_cast<size_t>(b) * a.dim + d0 + rc) * NS + kS * rh);
 }
 
-// Packs B and C ((batch, 16, L) each, io dtype) into one fp32 buffer
-// (batch, Lp, 32): row l holds B[:, l] then C[:, l]; rows l >= L are zero.
+// Packs B and C ((batch, NS, L) each, io dtype) into one fp32 buffer
+// (batch, Lp, 2*NS): row l holds B[:, l] then C[:, l]; rows l >= L are zero.
 // One thread per (batch, row): strided reads coalesce across threads, and each
-// thread writes its 128-byte row with eight 16-byte stores.
-template <typename T>
+// thread writes its row with 16-byte stores.
+template <typename T, int NS>
 __global__ void __launch_bounds__(256)
 bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restrict__ out, int batch, int L,
                int Lp) {
@@ -474,17 +578,20 @@ bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restri
     if (i >= static_cast<long long>(batch) * Lp) return;
     const int b = static_cast<int>(i / Lp);
     const int l = static_cast<int>(i % Lp);
-    float v[kBCW];
     const bool ok = l < L;
-    const size_t base = static_cast<size_t>(b) * kDState * L + l;
+    const size_t base = static_cast<size_t>(b) * NS * L + l;
+    float4* o = reinterpret_cast<float4*>(out + i * (2 * NS));
 #pragma unroll
-    for (int s = 0; s < kDState; ++s) {
-        v[s] = ok ? Io<T>::to_f(B[base + static_cast<size_t>(s) * L]) : 0.f;
-        v[kDState + s] = ok ? Io<T>::to_f(C[base + static_cast<size_t>(s) * L]) : 0.f;
+    for (int which = 0; which < 2; ++which) {
+        const T* src = which ? C : B;
+#pragma unroll
+        for (int s = 0; s < NS; s += 4) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = ok ? Io<T>::to_f(src[base + static_cast<size_t>(s + j) * L]) : 0.f;
+            o[(which * NS + s) / 4] = make_float4(v[0], v[1], v[2], v[3]);
+        }
     }
-    float4* o = reinterpret_cast<float4*>(out + i * kBCW);
-#pragma unroll
-    for (int j = 0; j < kBCW / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
 }
 
 // Copies rows of length L into rows of pitch Lpitch >= L (the tail is left as

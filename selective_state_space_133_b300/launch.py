@@ -30,15 +30,15 @@ def main() -> int:
         for _ in range(args.launches):
             ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"],
                                d["softplus"])
-    elif args.workload in syn.SCAN_WORKLOADS:
-        w = syn.SCAN_WORKLOADS[args.workload]
+    elif args.workload in syn.SCAN_WORKLOADS or args.workload in syn.VARIANT_WORKLOADS:
+        w = syn.SCAN_WORKLOADS.get(args.workload) or syn.VARIANT_WORKLOADS[args.workload]
         x = syn.workload_inputs(w)
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
         y = torch.empty_like(d["u"])
-        fs = torch.empty(w.batch, w.dim, syn.DSTATE, device=dev) if w.final_state else None
+        fs = torch.empty(w.batch, w.dim, w.dstate, device=dev) if w.final_state else None
         for _ in range(args.launches):
             ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
-                               d["softplus"], y=y, final_state=fs)
+                               d["softplus"], y=y, final_state=fs, zoh=w.zoh)
     else:
         w = syn.DECODE_WORKLOADS[args.workload]
         st = {k: v.to(dev) for k, v in syn.decode_static(w).items()}

@@ -42,23 +42,30 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
     return s.cuda_stream
 
 
+def _flags(softplus, zoh=False) -> int:
+    return (_lib.MAMBA_FLAG_SOFTPLUS if softplus else 0) | (_lib.MAMBA_FLAG_ZOH if zoh else 0)
+
+
 def workspace_bytes(batch: int, dim: int, seqlen: int, dtype: torch.dtype, dstate: int = 16) -> int:
     """Device workspace the scan needs for these sizes (mamba_scan_workspace_size)."""
     return int(_lib.lib().mamba_scan_workspace_size(batch, dim, seqlen, dstate, _IO[dtype]))
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                   y=None, final_state=None, stream=None, workspace=None, initial_state=None, chunk_states=None):
+                   y=None, final_state=None, stream=None, workspace=None, initial_state=None, chunk_states=None,
+                   zoh=False):
     """Selective scan (see include/mamba_scan.h, mamba_scan_fwd_ws).
 
-    u, delta, z: (batch, dim, L); B, C: (batch, 16, L), all fp32 or all bf16;
-    A: (dim, 16) fp32; D, delta_bias: (dim,) fp32. ``final_state`` may be a
-    preallocated (batch, dim, 16) fp32 tensor, or True to allocate one.
+    u, delta, z: (batch, dim, L); B, C: (batch, N, L), all fp32 or all bf16;
+    A: (dim, N) fp32 with N in {8, 16, 32, 64}; D, delta_bias: (dim,) fp32.
+    ``zoh``: exact zero-order-hold input gain instead of delta * B.
+    ``final_state`` may be a preallocated (batch, dim, N) fp32 tensor, or True
+    to allocate one.
     ``workspace`` may be a uint8 CUDA tensor of at least ``workspace_bytes(...)``
     bytes; otherwise one is taken from torch's caching allocator.
-    ``initial_state``: (batch, dim, 16) fp32 state before the first step, or None
+    ``initial_state``: (batch, dim, N) fp32 state before the first step, or None
     for zero (continuing an earlier scan from its final state).
-    ``chunk_states``: a (batch, dim, ceil(L/16), 16) fp32 tensor that receives the
+    ``chunk_states``: a (batch, dim, ceil(L/16), N) fp32 tensor that receives the
     state before every 16-step chunk (for mamba_scan_bwd), or None.
     Returns y, or (y, final_state) when a final state was requested.
     """
@@ -96,7 +103,7 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     st = lib.mamba_scan_fwd_ws(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), batch, dim, L, N,
+        _flags(softplus, zoh), _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), batch, dim, L, N,
         _IO[u.dtype],
         _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_fwd")
@@ -105,7 +112,7 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
 
 def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
                         conv_bias=None, conv_state=None, initial_state=None, final_state=None, y=None,
-                        stream=None, workspace=None):
+                        stream=None, workspace=None, zoh=False):
     """Scan of u = silu(causal conv1d(x)) (see include/mamba_scan.h, mamba_conv_scan_fwd_ws).
 
     x: (batch, dim, L) I/O dtype; conv_weight: (dim, 4) fp32; conv_bias: (dim,)
@@ -146,7 +153,7 @@ def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bi
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     st = lib.mamba_conv_scan_fwd_ws(
         _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), width, _ptr(delta), _ptr(A), _ptr(B),
-        _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(initial_state), _ptr(y),
+        _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _flags(softplus, zoh), _ptr(initial_state), _ptr(y),
         _ptr(final_state), batch, dim, L, N, _IO[x.dtype], _ptr(workspace), workspace.numel(),
         _stream_handle(stream, dev))
     _lib.check(st, "mamba_conv_scan_fwd")
@@ -158,7 +165,7 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
                    chunk_states=None):
     """Gradients of sum(dy * y) for the scan (see include/mamba_scan.h, mamba_scan_bwd).
 
-    Inputs as mamba_scan_fwd plus dy (batch, dim, L) in the I/O dtype. Returns a
+    Inputs as mamba_scan_fwd (N = 16, no ZOH gain) plus dy (batch, dim, L) in the I/O dtype. Returns a
     dict with du, ddelta, dz (or None), dA (dim, 16) fp32, dB, dC (batch, 16, L),
     dD and ddelta_bias (dim,) fp32 (or None when the input is absent) and dh0
     (batch, dim, 16) fp32 when ``want_initial_state_grad``.
@@ -190,7 +197,7 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     st = lib.mamba_scan_bwd(
-        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _flags(softplus),
         _ptr(initial_state), _ptr(chunk_states), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
         _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(out["dh0"]),
         batch, dim, L, N, _IO[u.dtype], _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
@@ -199,11 +206,12 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
 
 
 def mamba_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       softplus=False, y=None, stream=None):
+                       softplus=False, y=None, stream=None, zoh=False):
     """One decode step in place on ``state`` (see include/mamba_scan.h, mamba_state_update).
 
-    state: (batch, dim, 16) fp32; u, delta, z: (batch, dim); B, C: (batch, 16),
-    all fp32 or all bf16; A: (dim, 16) fp32; D, delta_bias: (dim,) fp32.
+    state: (batch, dim, N) fp32, N in {8, 16, 32, 64}; u, delta, z: (batch, dim);
+    B, C: (batch, N), all fp32 or all bf16; A: (dim, N) fp32; D, delta_bias:
+    (dim,) fp32; ``zoh`` as in mamba_scan_fwd.
     Returns y (batch, dim).
     """
     if u.dtype not in _IO:
@@ -225,7 +233,7 @@ def mamba_state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None
     _need(y, "y", u.dtype, (batch, dim), dev)
     st = _lib.lib().mamba_state_update(
         _ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-        _ptr(delta_bias), int(bool(softplus)), _ptr(y), batch, dim, N, _IO[u.dtype],
+        _ptr(delta_bias), _flags(softplus, zoh), _ptr(y), batch, dim, N, _IO[u.dtype],
         _stream_handle(stream, dev))
     _lib.check(st, "mamba_state_update")
     return y

@@ -15,7 +15,9 @@ distributions of the workloads, not a step of the scan:
 
 Draw order on one torch CPU generator seeded with the workload's seed:
 u, w, dt, A-noise, B, C, D, z. Values are drawn in fp32 and rounded to the
-I/O dtype (bf16: round-to-nearest-even); A, D and the bias stay fp32.
+I/O dtype (bf16: round-to-nearest-even); A, D and the bias stay fp32. The
+state size N (rows of A, B and C) is 16 unless a workload says otherwise;
+A = -(n+1) for n < N, as for N = 16.
 """
 from __future__ import annotations
 
@@ -41,18 +43,20 @@ class ScanWorkload:
     a_noise: float            # std of the log-normal factor on A = -(n+1); 0 = exact S4D-real
     seed: int
     final_state: bool = False
+    dstate: int = DSTATE
+    zoh: bool = False         # exact zero-order-hold input gain instead of delta * B
 
     @property
     def elements(self) -> int:
         """Work units: batch * seqlen * dim * dstate."""
-        return self.batch * self.seqlen * self.dim * DSTATE
+        return self.batch * self.seqlen * self.dim * self.dstate
 
     @property
     def io_bytes(self) -> int:
         """Unique bytes the scan must move: u, delta, z, B, C read; y written."""
         es = torch.finfo(self.dtype).bits // 8
         per_row = (3 + (1 if self.with_z else 0)) * self.batch * self.dim * self.seqlen
-        bc = 2 * self.batch * DSTATE * self.seqlen
+        bc = 2 * self.batch * self.dstate * self.seqlen
         return es * (per_row + bc)
 
 
@@ -87,6 +91,19 @@ SCAN_WORKLOADS: Dict[str, ScanWorkload] = {w.name: w for w in [
                  final_state=True),
 ]}
 
+# Variants of the 8 x 2048 x 4096 bf16 workload: other state sizes and the
+# exact zero-order-hold gain (the pages' discretisation, §2.2 of the paper
+# walkthrough, and the larger states it mentions for Mamba-2).
+VARIANT_WORKLOADS: Dict[str, ScanWorkload] = {w.name: w for w in [
+    ScanWorkload("scan_b8_d2048_l4096_n8_bf16", 8, 2048, 4096, torch.bfloat16, True, True, True, 0.1, 5, dstate=8),
+    ScanWorkload("scan_b8_d2048_l4096_n32_bf16", 8, 2048, 4096, torch.bfloat16, True, True, True, 0.1, 6,
+                 dstate=32),
+    ScanWorkload("scan_b8_d2048_l4096_n64_bf16", 8, 2048, 4096, torch.bfloat16, True, True, True, 0.1, 7,
+                 dstate=64),
+    ScanWorkload("scan_b8_d2048_l4096_zoh_bf16", 8, 2048, 4096, torch.bfloat16, True, True, True, 0.1, 8,
+                 zoh=True),
+]}
+
 DECODE_WORKLOADS: Dict[str, DecodeWorkload] = {w.name: w for w in [
     DecodeWorkload("decode_b256_d5120_x1024_bf16", 256, 5120, 1024, torch.bfloat16, 0.1, 4),
 ]}
@@ -102,24 +119,25 @@ def _dt_init(g: torch.Generator, dim: int) -> torch.Tensor:
     return torch.exp(lo + torch.rand(dim, generator=g, dtype=torch.float64) * (hi - lo))
 
 
-def _a_matrix(g: torch.Generator, dim: int, noise: float) -> torch.Tensor:
-    A = -torch.arange(1, DSTATE + 1, dtype=torch.float32).repeat(dim, 1)
+def _a_matrix(g: torch.Generator, dim: int, noise: float, dstate: int = DSTATE) -> torch.Tensor:
+    A = -torch.arange(1, dstate + 1, dtype=torch.float32).repeat(dim, 1)
     if noise > 0:
-        A = A * torch.exp(torch.randn(dim, DSTATE, generator=g) * noise)
+        A = A * torch.exp(torch.randn(dim, dstate, generator=g) * noise)
     return A.contiguous()
 
 
 def scan_inputs(batch: int, dim: int, seqlen: int, dtype: torch.dtype = torch.float32, *,
                 seed: int = 0, with_D: bool = True, with_z: bool = True,
-                softplus_in_kernel: bool = True, a_noise: float = 0.0) -> Dict[str, Optional[torch.Tensor]]:
+                softplus_in_kernel: bool = True, a_noise: float = 0.0,
+                dstate: int = DSTATE) -> Dict[str, Optional[torch.Tensor]]:
     """CPU tensors for one scan call: u, delta, A, B, C, D, z, delta_bias, softplus."""
     g = torch.Generator().manual_seed(seed)
     u = torch.randn(batch, dim, seqlen, generator=g)
     w = torch.randn(batch, dim, seqlen, generator=g) * 0.5
     dt = _dt_init(g, dim)
-    A = _a_matrix(g, dim, a_noise)
-    B = torch.randn(batch, DSTATE, seqlen, generator=g)
-    C = torch.randn(batch, DSTATE, seqlen, generator=g)
+    A = _a_matrix(g, dim, a_noise, dstate)
+    B = torch.randn(batch, dstate, seqlen, generator=g)
+    C = torch.randn(batch, dstate, seqlen, generator=g)
     D = torch.randn(dim, generator=g) if with_D else None
     z = torch.randn(batch, dim, seqlen, generator=g) if with_z else None
     if softplus_in_kernel:
@@ -136,7 +154,7 @@ def scan_inputs(batch: int, dim: int, seqlen: int, dtype: torch.dtype = torch.fl
 
 def workload_inputs(w: ScanWorkload) -> Dict[str, Optional[torch.Tensor]]:
     return scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed, with_D=w.with_D, with_z=w.with_z,
-                       softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+                       softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise, dstate=w.dstate)
 
 
 def decode_static(w: DecodeWorkload) -> Dict[str, torch.Tensor]:

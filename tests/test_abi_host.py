@@ -32,11 +32,11 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         s = L.mamba_status_string(code).decode()
         assert s.startswith(_lib.STATUS[code])
     assert L.mamba_status_string(42).decode() == "unknown mamba_status"
-    assert L.mamba_version() == 200
+    assert L.mamba_version() == 300
 
 
 # Fake, never-dereferenced addresses: validation fails before any CUDA call.
@@ -54,7 +54,10 @@ def scan(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=2), -3), (dict(dtype=-1), -3),
-    (dict(dstate=8), -2), (dict(dstate=32), -2), (dict(batch=-1), -2), (dict(dim=-5), -2),
+    (dict(dstate=4), -2), (dict(dstate=12), -2), (dict(dstate=128), -2), (dict(dstate=0), -2),
+    (dict(batch=-1), -2), (dict(dim=-5), -2),
+    (dict(sp=4), -8), (dict(sp=-1), -8), (dict(sp=1 << 20), -8),
+    (dict(dstate=8, u=P + 8), -4), (dict(dstate=32, y=P + 4), -4), (dict(dstate=64, B=None), -1),
     (dict(seqlen=-1), -2), (dict(batch=70000), -2),
     (dict(dim=1 << 20, seqlen=1 << 20), -2),
     (dict(u=None), -1), (dict(delta=None), -1), (dict(A=None), -1), (dict(B=None), -1),
@@ -87,7 +90,8 @@ def update(L, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dtype=7), -3), (dict(dstate=4), -2), (dict(batch=-2), -2),
+    (dict(dtype=7), -3), (dict(dstate=4), -2), (dict(dstate=128), -2), (dict(batch=-2), -2),
+    (dict(sp=6), -8), (dict(dstate=64, state=P + 4), -4), (dict(dstate=8, y=None), -1),
     (dict(state=None), -1), (dict(u=None), -1), (dict(y=None), -1), (dict(A=None), -1),
     (dict(state=P + 4), -4), (dict(A=P + 8), -4), (dict(B=P + 2), -4), (dict(u=P + 1), -4),
     (dict(C=P + 8), -4), (dict(batch=70000), -2),
@@ -112,17 +116,20 @@ def scan_ws(L, ws=P, ws_bytes=1 << 30, **kw):
 
 
 def test_workspace_size(L):
-    # packed fp32 B/C rows: batch * roundup(L, 16) * 128 bytes
+    # packed fp32 B/C rows: batch * roundup(L, 16) * 8 * dstate bytes
     assert L.mamba_scan_workspace_size(8, 2048, 4096, 16, 1) == 8 * 4096 * 128
+    assert L.mamba_scan_workspace_size(8, 2048, 4096, 64, 1) == 8 * 4096 * 512
+    assert L.mamba_scan_workspace_size(1, 1, 16, 8, 1) == 16 * 64
     assert L.mamba_scan_workspace_size(2, 64, 17, 16, 1) >= 2 * 32 * 128 + 3 * 2 * 64 * 24 * 2
     assert L.mamba_scan_workspace_size(2, 64, 20, 16, 0) == 2 * 32 * 128   # 20 fp32 = 80 B rows: no copies
     assert L.mamba_scan_workspace_size(1, 1, 0, 16, 1) == 0
-    assert L.mamba_scan_workspace_size(1, 1, 16, 8, 1) == 0
+    assert L.mamba_scan_workspace_size(1, 1, 16, 24, 1) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=None), -1), (dict(ws_bytes=100), -7), (dict(ws=P + 16), -4),
-    (dict(dtype=5), -3), (dict(dstate=64), -2), (dict(u=P + 2), -4), (dict(C=None), -1),
+    (dict(dtype=5), -3), (dict(dstate=48), -2), (dict(u=P + 2), -4), (dict(C=None), -1),
+    (dict(sp=8), -8), (dict(dstate=64, ws_bytes=8 * 64 * 64 - 1), -7),
     (dict(h0=P + 8), -4), (dict(ck=P + 4), -4),
 ])
 def test_scan_ws_rejects(L, kw, code):
@@ -142,6 +149,34 @@ def conv_scan(L, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(width=3), -2), (dict(width=5), -2), (dict(w=None), -1), (dict(w=P + 8), -4), (dict(cb=P + 2), -4),
     (dict(cs=P + 1), -4), (dict(x=None), -1), (dict(ws=None), -1), (dict(ws_bytes=10), -7), (dict(dtype=3), -3),
+    (dict(sp=16), -8), (dict(dstate=20), -2),
 ])
 def test_conv_scan_rejects(L, kw, code):
     assert conv_scan(L, **kw) == code
+
+
+def scan_bwd(L, **kw):
+    args = dict(u=P, delta=P, A=P, B=P, C=P, D=None, z=None, bias=None, sp=1, h0=None, ck=None, dy=P, du=P, ddl=P,
+                dA=P, dB=P, dC=P, dD=None, dz=None, dbias=None, dh0=None, batch=2, dim=32, seqlen=64, dstate=16,
+                dtype=1, ws=P, ws_bytes=1 << 30)
+    args.update(kw)
+    return L.mamba_scan_bwd(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["z"],
+                            args["bias"], args["sp"], args["h0"], args["ck"], args["dy"], args["du"], args["ddl"],
+                            args["dA"], args["dB"], args["dC"], args["dD"], args["dz"], args["dbias"], args["dh0"],
+                            args["batch"], args["dim"], args["seqlen"], args["dstate"], args["dtype"], args["ws"],
+                            args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dstate=8), -2), (dict(dstate=64), -2), (dict(sp=2), -8), (dict(sp=3), -8), (dict(sp=4), -8),
+    (dict(dA=None), -1), (dict(z=P, dz=None), -1), (dict(dD=P), -1), (dict(du=P + 4), -4),
+    (dict(ws_bytes=100), -7),
+])
+def test_scan_bwd_rejects(L, kw, code):
+    assert scan_bwd(L, **kw) == code
+
+
+def test_bwd_workspace_size_only_for_16_states(L):
+    assert L.mamba_scan_bwd_workspace_size(2, 32, 64, 16, 1) > 0
+    for n in (8, 32, 64):
+        assert L.mamba_scan_bwd_workspace_size(2, 32, 64, n, 1) == 0
