@@ -405,8 +405,7 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
 
     // The recurrence is software-pipelined by one step: the loads, the ex2 of
     // dt*A and the input term of step t+1 are issued before the state update
-    // of step t uses them. The next step's ex2 sit between the current step's
-    // C.h FMAs, so the MUFU and FMA pipes are fed alternately.
+    // of step t uses them.
     auto recurrence = [&](const ScanStage<T, NS>& S) {
         const float2* W = &sm.W[rc][0];
         const float* bc = &S.bc[0][0] + kS * rh;  // B of this lane's states; their C is NS floats further
@@ -435,41 +434,55 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 if (ZOH) pb[i] = __fmul2_rn(zoh_gain2(x, e[i], dd, IA[i]), pb[i]);
             }
         }
+        // Step t's contraction C.h is taken in iteration t + 1, from the state
+        // before that iteration's update: its FMA chain then depends on
+        // nothing computed in the same iteration and interleaves with the
+        // update, the ex2 and the loads of the next step.
+        float2 cp[H];  // C of the step whose contraction is pending
+        float p[kTL];
 #pragma unroll
-        for (int t0 = 0; t0 < kTL; t0 += 4) {
-            float p[4];
+        for (int t = 0; t < kTL; ++t) {
+            const int tn = t + 1 < kTL ? t + 1 : t;  // the last step loads nothing new (values unused)
+            const float2 w = W[tn];
+            float2 bn[H], cn[H];
+            load_bc(tn, bn, cn);
+            const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
+            float2 acc = make_float2(0.f, 0.f);
+            if (t > 0) {  // step t - 1
+                acc = __fmul2_rn(cp[0], h[0]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = t0 + i;
-                const int tn = t + 1 < kTL ? t + 1 : t;  // the last step loads nothing new (values unused)
-                const float2 w = W[tn];
-                float2 bn[H], cn[H];
-                load_bc(tn, bn, cn);
-                const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
-                // Written in an issue-friendly order (a warp issues in order):
-                // every result is consumed a few independent instructions later.
+                for (int j = 1; j < H; ++j) acc = __ffma2_rn(cp[j], h[j], acc);
+            }
 #pragma unroll
-                for (int j = 0; j < H; ++j) h[j] = __ffma2_rn(e[j], h[j], pb[j]);   // step t
-                float2 x[H];
+            for (int j = 0; j < H; ++j) h[j] = __ffma2_rn(e[j], h[j], pb[j]);   // step t
+            float2 x[H];
 #pragma unroll
-                for (int j = 0; j < H; ++j) x[j] = __fmul2_rn(dd, A2[j]);             // step t+1
-                float2 acc = __fmul2_rn(cv[0], h[0]);
+            for (int j = 0; j < H; ++j) x[j] = __fmul2_rn(dd, A2[j]);             // step t+1
+            if (t + 1 < kTL) {
+#pragma unroll
+                for (int j = 0; j < H; ++j) e[j] = make_float2(ex2_approx(x[j].x), ex2_approx(x[j].y));
 #pragma unroll
                 for (int j = 0; j < H; ++j) {
-                    if (t + 1 < kTL) e[j] = make_float2(ex2_approx(x[j].x), ex2_approx(x[j].y));
-                    if (j < H - 1) acc = __ffma2_rn(cv[j + 1], h[j + 1], acc);
+                    pb[j] = __fmul2_rn(du, bn[j]);
+                    if (ZOH) pb[j] = __fmul2_rn(zoh_gain2(x[j], e[j], dd, IA[j]), pb[j]);
                 }
-                if (t + 1 < kTL) {
-#pragma unroll
-                    for (int j = 0; j < H; ++j) {
-                        pb[j] = __fmul2_rn(du, bn[j]);
-                        if (ZOH) pb[j] = __fmul2_rn(zoh_gain2(x[j], e[j], dd, IA[j]), pb[j]);
-                        cv[j] = cn[j];
-                    }
-                }
-                p[i] = acc.x + acc.y;
             }
-            *reinterpret_cast<float4*>(P + (t0 / 4) * kPJ) = make_float4(p[0], p[1], p[2], p[3]);
+            if (t > 0) p[t - 1] = acc.x + acc.y;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+                cp[j] = cv[j];
+                cv[j] = cn[j];
+            }
+            if (t > 0 && t % 4 == 0)  // steps t-4 .. t-1: one 16-byte store
+                *reinterpret_cast<float4*>(P + (t / 4 - 1) * kPJ) = make_float4(p[t - 4], p[t - 3], p[t - 2], p[t - 1]);
+        }
+        {  // the last step's contraction
+            float2 acc = __fmul2_rn(cp[0], h[0]);
+#pragma unroll
+            for (int j = 1; j < H; ++j) acc = __ffma2_rn(cp[j], h[j], acc);
+            p[kTL - 1] = acc.x + acc.y;
+            *reinterpret_cast<float4*>(P + (kTL / 4 - 1) * kPJ) =
+                make_float4(p[kTL - 4], p[kTL - 3], p[kTL - 2], p[kTL - 1]);
         }
     };
 
