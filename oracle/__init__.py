@@ -71,6 +71,8 @@ class Oracle:
         self.lib.oracle_scan_bwd.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              _P, _P, _P, _P, _P, _P, _P, _P, _PI, _P,
                                              ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        self.lib.oracle_ssd.restype = ctypes.c_int
+        self.lib.oracle_ssd.argtypes = [ctypes.c_int64] * 5 + [_P] * 8 + [ctypes.c_int, _P, _P]
         self.lib.oracle_state_update.restype = ctypes.c_int
         self.lib.oracle_state_update.argtypes = [ctypes.c_int64, ctypes.c_int64, _P,
                                                  _P, _P, _P, _P, _P, _P, _P, _P, _PI,
@@ -186,6 +188,37 @@ class Oracle:
                     ddelta_bias=None if delta_bias is None else db.reshape(batch, dim).sum(axis=0),
                     dh0=dh0.reshape(batch, dim, N))
 
+    # -- SSD (Mamba-2) ------------------------------------------------------------
+    def ssd(self, x, delta, A, B, C, D=None, delta_bias=None, softplus=False, h0=None, return_state=True):
+        """State-space dual layer: per batch row and head a (headdim x N) state.
+
+        x : (batch, nheads * headdim, L);  delta : (batch, nheads, L);  A, D,
+        delta_bias : (nheads,);  B, C : (batch, N, L);  h0 : (batch, nheads,
+        headdim, N) or None. Returns y (batch, nheads * headdim, L) and, if asked,
+        the final state (batch, nheads, headdim, N), float64.
+        """
+        xf = np.ascontiguousarray(_f64(x))
+        df = np.ascontiguousarray(_f64(delta))
+        batch, nheads, L = df.shape
+        dim = xf.shape[1]
+        assert xf.shape == (batch, dim, L) and dim % max(nheads, 1) == 0
+        P = dim // nheads
+        Bf = np.ascontiguousarray(_f64(B))
+        Cf = np.ascontiguousarray(_f64(C))
+        N = Bf.shape[1]
+        assert Bf.shape == (batch, N, L) and Cf.shape == (batch, N, L)
+        Af = np.ascontiguousarray(_f64(A))
+        Dr = None if D is None else np.ascontiguousarray(_f64(D))
+        br = None if delta_bias is None else np.ascontiguousarray(_f64(delta_bias))
+        hr0 = None if h0 is None else np.ascontiguousarray(_f64(h0))
+        y = np.empty((batch, dim, L))
+        h = np.empty((batch, nheads, P, N)) if return_state else None
+        rc = self.lib.oracle_ssd(batch, nheads, P, N, L, _ptr(xf), _ptr(df), _ptr(Af), _ptr(Bf), _ptr(Cf),
+                                 _ptr(Dr), _ptr(br), _ptr(hr0), _flags(softplus), _ptr(y), _ptr(h))
+        if rc != 0:
+            raise ValueError(f"oracle_ssd failed ({rc})")
+        return (y, h) if return_state else y
+
     # -- state update ---------------------------------------------------------
     def state_update(self, state, u, delta, A, B, C, D=None, z=None, delta_bias=None,
                      softplus=False, rows=None, compact_state=False, zoh=False):
@@ -283,3 +316,7 @@ def scan_bwd(*args, **kwargs):
 
 def state_update(*args, **kwargs):
     return default().state_update(*args, **kwargs)
+
+
+def ssd(*args, **kwargs):
+    return default().ssd(*args, **kwargs)

@@ -293,3 +293,68 @@ int oracle_causal_conv_silu(int64_t nrows, int64_t seqlen, int64_t width,
     }
     return 0;
 }
+
+/*
+ * State-space dual (SSD) layer of Mamba-2 ("Mamba 论文精读" (youngju.dev) §4.1:
+ * the recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t, whose matrix form
+ * is Y = (T o M) X with T the causal mask and M semiseparable), read as the
+ * Mamba-2 layer of the same page's §5.2 (multi-head, headdim channels a head,
+ * a larger state): per batch row b and head h the state is a
+ * (headdim x dstate) matrix, the decay is one scalar per head and step, and
+ * B, C (one group) are shared by all heads:
+ *
+ *   dt      = delta[b,h,l] (+ bias[h]);  softplus(dt) if ORACLE_SOFTPLUS
+ *   a       = exp(dt * A[h])
+ *   H[p][n] = a * H[p][n] + dt * B[b,n,l] * x[b,h*P+p,l]
+ *   y[b,h*P+p,l] = sum_n C[b,n,l] * H[p][n]  (+ D[h] * x[b,h*P+p,l])
+ *
+ *   x, y   : (batch, nheads * headdim, seqlen)   channel d = h * headdim + p
+ *   delta  : (batch, nheads, seqlen)
+ *   A, D, bias : (nheads)                        D and bias may be NULL
+ *   B, C   : (batch, dstate, seqlen)
+ *   h0, hlast : (batch, nheads, headdim, dstate) state before the first step
+ *               (NULL: zero) and after the last (NULL: not returned)
+ * Returns 0, -1 if a size is out of range, -2 if the state buffer cannot be
+ * allocated, -3 if flags asks for the ZOH gain (not defined for this form).
+ */
+int oracle_ssd(int64_t batch, int64_t nheads, int64_t headdim, int64_t dstate, int64_t seqlen,
+               const double* x, const double* delta, const double* A,
+               const double* B, const double* C, const double* Dskip, const double* bias,
+               const double* h0, int flags, double* y, double* hlast)
+{
+    if (batch < 0 || nheads < 0 || headdim < 1 || dstate < 1 || seqlen < 0) return -1;
+    if (flags & ORACLE_ZOH) return -3;
+    double* H = (double*)malloc(sizeof(double) * (size_t)headdim * (size_t)dstate);
+    if (!H) return -2;
+    const int64_t dim = nheads * headdim;
+    for (int64_t b = 0; b < batch; ++b) {
+        const double* Bb = B + b * dstate * seqlen;
+        const double* Cb = C + b * dstate * seqlen;
+        for (int64_t h = 0; h < nheads; ++h) {
+            const int64_t s0 = ((b * nheads + h) * headdim) * dstate;
+            for (int64_t i = 0; i < headdim * dstate; ++i) H[i] = h0 ? h0[s0 + i] : 0.0;
+            for (int64_t l = 0; l < seqlen; ++l) {
+                double dt = delta[(b * nheads + h) * seqlen + l];
+                if (bias) dt += bias[h];
+                if (flags & ORACLE_SOFTPLUS) dt = softplus_ref(dt);
+                const double a = exp(dt * A[h]);
+                for (int64_t p = 0; p < headdim; ++p) {
+                    const int64_t i = (b * dim + h * headdim + p) * seqlen + l;
+                    const double xv = x[i];
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < dstate; ++n) {
+                        double* hp = H + p * dstate + n;
+                        *hp = a * (*hp) + dt * Bb[n * seqlen + l] * xv;
+                        acc += Cb[n * seqlen + l] * (*hp);
+                    }
+                    if (Dskip) acc += Dskip[h] * xv;
+                    y[i] = acc;
+                }
+            }
+            if (hlast)
+                for (int64_t i = 0; i < headdim * dstate; ++i) hlast[s0 + i] = H[i];
+        }
+    }
+    free(H);
+    return 0;
+}
