@@ -283,6 +283,42 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
                        int io_dtype, void* stream);
 
 /*
+ * State-space dual (SSD) layer, the Mamba-2 form ("Mamba 论文精读" (youngju.dev)
+ * §4.1: the recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t is dual to
+ * the masked product Y = (T o M) X with M semiseparable; §5.2: multi-head,
+ * headdim 64, larger states). Per batch row b and head h the state S is a
+ * (headdim x dstate) fp32 matrix and the decay one scalar per step:
+ *
+ *   dt   = delta[b,h,l] + delta_bias[h]; softplus(dt) if flags & MAMBA_FLAG_SOFTPLUS
+ *   S    = exp(dt * A[h]) * S + dt * x[b,h*64+p,l] * B[b,:,l]      (row p of S)
+ *   y[b,h*64+p,l] = S[p,:] . C[b,:,l] + D[h] * x[b,h*64+p,l]
+ *
+ * computed chunk by chunk (64 steps) with the contractions on the tensor cores.
+ *   x, y          : (batch, nheads * headdim, seqlen) bf16, channel = h * 64 + p
+ *   delta         : (batch, nheads, seqlen) bf16
+ *   A             : (nheads) fp32;  D, delta_bias : (nheads) fp32 or NULL
+ *   B, C          : (batch, dstate, seqlen) bf16, one group shared by the heads
+ *   initial_state : (batch, nheads, headdim, dstate) fp32 or NULL (zero)
+ *   final_state   : the same shape, or NULL; receives S after the last step
+ *   workspace     : as for mamba_scan_fwd_ws, sized by mamba_ssd_workspace_size
+ *                   (0 bytes unless seqlen is not a multiple of 8: then row
+ *                   copies of x, B and C at a 16-byte pitch)
+ * Supported: io_dtype MAMBA_BF16 (MAMBA_ERR_DTYPE otherwise), headdim 64 and
+ * dstate 64 or 128 (MAMBA_ERR_SHAPE otherwise), flags MAMBA_FLAG_SOFTPLUS only
+ * (MAMBA_ERR_FLAGS otherwise). Alignment: x, y, B, C and the states 16 bytes,
+ * delta 2, A, D, delta_bias 4. State and accumulation are fp32; y is rounded to
+ * bf16 once. Returns MAMBA_OK or a negative mamba_status.
+ */
+size_t mamba_ssd_workspace_size(int batch, int nheads, int headdim, int seqlen, int dstate, int io_dtype);
+
+int mamba_ssd_fwd(const void* x, const void* delta, const float* A,
+                  const void* B, const void* C,
+                  const float* D, const float* delta_bias, int flags,
+                  const float* initial_state, void* y, float* final_state,
+                  int batch, int nheads, int headdim, int seqlen, int dstate,
+                  int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device error word.
  * Kernels that wait on their own asynchronous copies give up after a bounded
  * number of polls (far beyond any normal copy time), set this word and return

@@ -3,8 +3,9 @@
 // The forward-scan kernels are instantiated per state size in their own files
 // (scan_fwd_n8.cu ... scan_fwd_n64.cu, compiled in parallel); each of those
 // files defines launch_scan_n for its state size and instantiates no other
-// kernel. Everything else (argument checks, workspace layout, the B/C pack,
-// the row copies, the backward and the state update) lives in mamba_scan.cu.
+// kernel; ssd_fwd.cu does the same for the SSD kernels (launch_ssd_n).
+// Everything else (argument checks, workspace layout, the B/C pack, the row
+// copies, the backward and the state update) lives in mamba_scan.cu.
 #pragma once
 
 #include <cuda.h>
@@ -13,6 +14,7 @@
 #include <stdint.h>
 
 #include "scan_fwd.cuh"
+#include "ssd_fwd.cuh"
 
 namespace mhost {
 
@@ -24,7 +26,8 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // pitch `pitch0` elements (>= e0) and plane pitch pitch0 * e1; box (b0, b1, 1).
 // Defined in mamba_scan.cu. Returns false if the map cannot be encoded.
 bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0, uint64_t e1,
-                 uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1);
+                 uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1,
+                 CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // Inputs of one forward launch after the call's preparation: u/delta/z at row
 // pitch `pitch` (the caller's tensors, or copies in the workspace), and the
@@ -42,5 +45,11 @@ struct FwdInputs {
 // convolution and z are given). Returns a mamba_status.
 template <typename T, int NS>
 int launch_scan_n(const mscan::ScanArgs& a, const FwdInputs& in, int flags, cudaStream_t stream);
+
+// Launches the SSD kernel of state size NS (64 or 128) on x, B and C at row
+// pitch `pitch` elements (defined in ssd_fwd.cu). Returns a mamba_status.
+template <int NS>
+int launch_ssd_n(const mscan::SsdArgs& a, const void* x, const void* B, const void* C, int pitch,
+                 cudaStream_t stream);
 
 }  // namespace mhost

@@ -75,7 +75,8 @@ int* device_error_word() { return static_cast<int*>(symbol_address(g_device_erro
 }  // namespace
 
 bool mhost::make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* base, uint64_t e0,
-                        uint64_t e1, uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1) {
+                        uint64_t e1, uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1,
+                        CUtensorMapSwizzle swizzle) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {e0, e1, e2};
@@ -83,7 +84,7 @@ bool mhost::make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const 
     const cuuint32_t box[3] = {b0, b1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -480,6 +481,92 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
     const bool zoh = (flags & MAMBA_FLAG_ZOH) != 0;
     return io_dtype == MAMBA_BF16 ? launch_update<__nv_bfloat16>(a, dstate, zoh, s)
                                   : launch_update<float>(a, dstate, zoh, s);
+}
+
+// --- SSD (Mamba-2 chunked form) ---------------------------------------------
+
+static bool ssd_dstate(int dstate) { return dstate == 64 || dstate == 128; }
+
+// Workspace of one SSD call: row-pitched copies of x, B and C when a row of
+// seqlen bf16 values is not a whole number of 16-byte units (a TMA stride rule).
+struct SsdWorkspace {
+    int pitch;
+    bool copy_rows;
+    size_t x, b, c, total;
+};
+
+static SsdWorkspace ssd_workspace(long long batch, long long nheads, long long L, int dstate) {
+    SsdWorkspace w;
+    w.copy_rows = (L * 2) % 16 != 0;
+    w.pitch = w.copy_rows ? static_cast<int>(round_up(static_cast<size_t>(L), 8)) : static_cast<int>(L);
+    const size_t xr = static_cast<size_t>(batch) * nheads * mscan::kSsdP * w.pitch * 2;
+    const size_t br = static_cast<size_t>(batch) * dstate * w.pitch * 2;
+    w.x = 0;
+    w.b = round_up(xr, 256);
+    w.c = w.b + round_up(br, 256);
+    w.total = (w.copy_rows && L > 0) ? w.c + round_up(br, 256) : 0;
+    return w;
+}
+
+size_t mamba_ssd_workspace_size(int batch, int nheads, int headdim, int seqlen, int dstate, int io_dtype) {
+    if (batch <= 0 || nheads <= 0 || seqlen <= 0 || headdim != mscan::kSsdP || !ssd_dstate(dstate)) return 0;
+    if (io_dtype != MAMBA_BF16) return 0;
+    return ssd_workspace(batch, nheads, seqlen, dstate).total;
+}
+
+int mamba_ssd_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                  const float* delta_bias, int flags, const float* initial_state, void* y, float* final_state,
+                  int batch, int nheads, int headdim, int seqlen, int dstate, int io_dtype, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+    if (io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (flags & ~MAMBA_FLAG_SOFTPLUS) return MAMBA_ERR_FLAGS;
+    if (batch < 0 || nheads < 0 || seqlen < 0 || headdim != mscan::kSsdP || !ssd_dstate(dstate))
+        return MAMBA_ERR_SHAPE;
+    if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
+    const unsigned long long dim = static_cast<unsigned long long>(nheads) * headdim;
+    if ((static_cast<unsigned long long>(seqlen) + 16) * dim * 2 >= (1ull << 40)) return MAMBA_ERR_SHAPE;
+    if (dim > 0 && seqlen > 0 &&
+        static_cast<unsigned long long>(batch) * dim * static_cast<unsigned long long>(seqlen) >= (1ull << 62))
+        return MAMBA_ERR_SHAPE;
+    if (batch == 0 || nheads == 0) return MAMBA_OK;
+    if (!A) return MAMBA_ERR_NULL;
+    if (seqlen > 0 && (!x || !delta || !B || !C || !y)) return MAMBA_ERR_NULL;
+    const void* p16[] = {x, B, C, y, initial_state, final_state};
+    for (const void* p : p16)
+        if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
+    if ((delta && !aligned(delta, 2)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+        (delta_bias && !aligned(delta_bias, 4)))
+        return MAMBA_ERR_ALIGN;
+    const SsdWorkspace w = ssd_workspace(batch, nheads, seqlen, dstate);
+    if (w.total > 0) {
+        if (!workspace) return MAMBA_ERR_NULL;
+        if (workspace_bytes < w.total) return MAMBA_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return MAMBA_ERR_ALIGN;
+    }
+    mscan::SsdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.delta = delta; a.A = A; a.D = D; a.bias = delta_bias; a.h0 = initial_state; a.y = y;
+    a.final_state = final_state; a.batch = batch; a.nheads = nheads; a.seqlen = seqlen;
+    a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w.total > 0) {  // rows of x, B and C at a 16-byte pitch
+        char* ws = static_cast<char*>(workspace);
+        const long long rows[3] = {static_cast<long long>(batch) * nheads * headdim,
+                                   static_cast<long long>(batch) * dstate, static_cast<long long>(batch) * dstate};
+        const void* src[3] = {x, B, C};
+        const size_t dst[3] = {w.x, w.b, w.c};
+        for (int i = 0; i < 3; ++i) {
+            const unsigned blocks = static_cast<unsigned>(std::min<long long>((rows[i] * seqlen + 255) / 256, 148ll * 16));
+            mscan::row_pitch_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(src[i]), reinterpret_cast<__nv_bfloat16*>(ws + dst[i]), rows[i],
+                seqlen, w.pitch);
+        }
+        if (cudaGetLastError() != cudaSuccess) return MAMBA_ERR_CUDA;
+        x = ws + w.x; B = ws + w.b; C = ws + w.c;
+    }
+    return dstate == 64 ? mhost::launch_ssd_n<64>(a, x, B, C, w.pitch, s)
+                        : mhost::launch_ssd_n<128>(a, x, B, C, w.pitch, s);
 }
 
 int mamba_check_device_error(void* stream) {

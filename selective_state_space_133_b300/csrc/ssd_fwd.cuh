@@ -1,0 +1,388 @@
+// State-space dual (SSD) layer, chunked form on the tensor cores, sm_103a.
+//
+// The Mamba-2 form of the selective SSM ("Mamba 论文精读", youngju.dev, §4.1:
+// the recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t is dual to the
+// masked product Y = (T o M) X with M semiseparable; §5.2: multi-head,
+// headdim 64, larger states). Per batch row b and head h the state S is a
+// (64 x N) matrix, the decay a_t = exp(dt_t A_h) one scalar per step:
+//     S_t = a_t S_{t-1} + dt_t x_t B_t^T,   y_t = S_t C_t + D_h x_t.
+// Over a chunk of Q = 64 steps with c_l = sum_{r<=l} dt_r A_h (inclusive):
+//     y_l = sum_{s<=l} (C_l . B_s) e^{c_l - c_s} dt_s x_s        (intra-chunk)
+//         + e^{c_l} S_prev C_l                                    (carried state)
+//         + D_h x_l
+//     S_new = e^{c_Q} S_prev + sum_s x_s (e^{c_Q - c_s} dt_s) B_s^T.
+// The four contractions (C B^T, its masked product with X, the state update
+// and C S^T) run on the tensor cores: bf16 operands, fp32 accumulation.
+// Three operands are not bf16 inputs but values computed in fp32 (the masked
+// C B^T, the decay-weighted x and the carried state); each is split into a
+// bf16 high part and a bf16 remainder and multiplied twice, which keeps them
+// to ~2^-17 relative (one bf16 rounding of those operands alone costs up to
+// 1e-2 relative error in y at N = 128, over the bf16 I/O tolerance).
+//
+// One CTA (4 warps) per (head, batch row) walks the chunks in order; the fp32
+// state never leaves the registers (it is the state-update product's
+// accumulator). Warp w owns rows 16w..16w+15 of every per-chunk product:
+// steps l for the outputs and C B^T, channels p for the state. Lane 0 of warp
+// 0 loads the x, B and C tiles of a chunk with 3-D TMA (128-byte swizzled
+// rows) into a 2-slot ring while the CTA works on the previous chunk; the
+// operands the CTA writes itself use padded rows. Steps past the end of the
+// sequence get dt = 0, so they leave the state unchanged.
+#pragma once
+
+#include "common.cuh"
+
+namespace mscan {
+
+constexpr int kSsdQ = 64;         // chunk length
+constexpr int kSsdP = 64;         // head dimension
+constexpr int kSsdThreads = 128;  // 4 warps
+constexpr int kSsdPad = 8;        // row padding (bf16) of the operands written in shared memory
+
+struct SsdArgs {
+    const void* delta;   // (batch, nheads, L) bf16
+    const float* A;      // (nheads)
+    const float* D;      // (nheads) or null
+    const float* bias;   // (nheads) or null
+    const float* h0;     // (batch, nheads, 64, N) or null
+    void* y;             // (batch, nheads * 64, L) bf16
+    float* final_state;  // (batch, nheads, 64, N) or null
+    int* err;            // device error word
+    int batch, nheads, seqlen;
+    int softplus;
+};
+
+template <int NS>
+struct SsdSmem {
+    // TMA tiles: rows of 64 bf16 (128 bytes), 128-byte swizzle, two slots
+    alignas(1024) __nv_bfloat16 X[2][kSsdP][kSsdQ];   // x   [p][s]
+    alignas(1024) __nv_bfloat16 Bt[2][NS][kSsdQ];     // B   [n][s]
+    alignas(1024) __nv_bfloat16 Ct[2][NS][kSsdQ];     // C   [n][l]
+    // operands computed here, high and low bf16 parts
+    alignas(16) __nv_bfloat16 Gh[kSsdQ][kSsdQ + kSsdPad], Gl[kSsdQ][kSsdQ + kSsdPad];  // masked C B^T [l][s]
+    alignas(16) __nv_bfloat16 Wh[kSsdP][kSsdQ + kSsdPad], Wl[kSsdP][kSsdQ + kSsdPad];  // weighted x   [p][s]
+    alignas(16) __nv_bfloat16 Sh[kSsdP][NS + kSsdPad], Sl[kSsdP][NS + kSsdPad];        // state        [p][n]
+    alignas(16) float Yt[kSsdP][kSsdQ + 4];  // the chunk's outputs [p][l], for row-contiguous stores
+    float c2[kSsdQ];                         // c_l * log2(e)
+    float dt[kSsdQ];
+    alignas(8) uint64_t full[2];
+};
+
+// ------------------------------------------------------------ helpers ------
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+// D += A B, A 16x16 (row), B 16x8 (col), bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Shared address of 16-byte unit `chunk` (0..7) of row `row` in a tile of
+// 128-byte rows written by TMA with the 128-byte swizzle (tile base 1024-aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+    return base + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ float swz_ld(const __nv_bfloat16* tile, int row, int col) {
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(tile) + row * 128 +
+                             ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1));
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+}
+// v as a bf16 pair hi + lo: hi = bf16(v), lo = bf16(v - hi).
+__device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// ------------------------------------------------------------- kernel ------
+
+template <int NS>
+__global__ void __launch_bounds__(kSsdThreads, 1)
+ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_c) {
+    extern __shared__ unsigned char ssd_smem_raw[];
+    SsdSmem<NS>& sm = *reinterpret_cast<SsdSmem<NS>*>(
+        (reinterpret_cast<uintptr_t>(ssd_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int kNT = NS / 8;  // 8-column tiles of the state
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, tq = lane & 3;      // accumulator row group / column pair
+    const int mi = lane >> 3, rr = lane & 7;     // ldmatrix: which 8x8 matrix, which row of it
+    const int m0 = 16 * warp;                    // this warp's rows
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int L = a.seqlen;
+    const int n = (L + kSsdQ - 1) / kSsdQ;
+    const int dim = a.nheads * kSsdP;
+    const int ch0 = h * kSsdP;                   // first channel of the head
+    const float Ah2 = a.A[h] * kLog2e;
+    const float bias = a.bias ? a.bias[h] : 0.f;
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const size_t head_row = static_cast<size_t>(b) * a.nheads + h;
+
+    // Chunk k's x, B and C tiles into slot k & 1 (one thread).
+    auto issue = [&](int k) {
+        uint64_t* bar = &sm.full[k & 1];
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>((kSsdP + 2 * NS) * kSsdQ * 2));
+        tma_load_3d(&sm.X[k & 1][0][0], &tm_x, bar, k * kSsdQ, ch0, b);
+        tma_load_3d(&sm.Bt[k & 1][0][0], &tm_b, bar, k * kSsdQ, 0, b);
+        tma_load_3d(&sm.Ct[k & 1][0][0], &tm_c, bar, k * kSsdQ, 0, b);
+    };
+    if (tid == 0) {
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        fence_barrier_init();
+        if (n > 0) issue(0);
+    }
+
+    // The state: rows m0 + g (+8) and columns 8j + 2tq (+1) of this warp's block.
+    float S[kNT][4];
+    const bool have_state = a.h0 != nullptr;
+#pragma unroll
+    for (int j = 0; j < kNT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int p = m0 + g + 8 * (e >> 1), c = 8 * j + 2 * tq + (e & 1);
+            S[j][e] = have_state ? a.h0[(head_row * kSsdP + p) * NS + c] : 0.f;
+        }
+    }
+    // high and low bf16 parts of the state, for the next chunk's C S^T
+    auto store_state_parts = [&]() {
+#pragma unroll
+        for (int j = 0; j < kNT; ++j) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t hi, lo;
+                split2(S[j][2 * hf], S[j][2 * hf + 1], hi, lo);
+                const int p = m0 + g + 8 * hf, c = 8 * j + 2 * tq;
+                *reinterpret_cast<uint32_t*>(&sm.Sh[p][c]) = hi;
+                *reinterpret_cast<uint32_t*>(&sm.Sl[p][c]) = lo;
+            }
+        }
+    };
+    if (have_state) store_state_parts();
+    __syncthreads();
+
+    const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(a.delta) + head_row * L;
+    __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
+    const bool vec_ok = (L & 7) == 0;
+
+#pragma unroll 1
+    for (int k = 0; k < n; ++k) {
+        const int s = k & 1;
+        // the next chunk into the other slot: its last reader (chunk k - 1)
+        // finished at the barrier that ended the previous iteration
+        if (tid == 0 && k + 1 < n) {
+            fence_proxy_async_smem();
+            issue(k + 1);
+        }
+        // dt and the cumulative decay of the chunk (warp 0); padding steps get dt = 0
+        if (warp == 0) {
+            float v[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int l = 2 * lane + i, gl = k * kSsdQ + l;
+                float d = 0.f;
+                if (gl < L) {
+                    d = __bfloat162float(dl[gl]) + bias;
+                    if (a.softplus) d = softplus_f(d);
+                }
+                sm.dt[l] = d;
+                v[i] = d * Ah2;
+            }
+            const float pair = v[0] + v[1];
+            float incl = pair;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const float excl = incl - pair;
+            sm.c2[2 * lane] = excl + v[0];
+            sm.c2[2 * lane + 1] = excl + pair;
+        }
+        // the chunk's tiles (bounded wait); the barrier also publishes dt and c2
+        const bool ok = mbar_wait_bounded(&sm.full[s], static_cast<uint32_t>((k >> 1) & 1));
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) {
+                report_device_error(a.err, -6);
+                if (k + 1 < n) mbar_wait_bounded(&sm.full[(k + 1) & 1], static_cast<uint32_t>(((k + 1) >> 1) & 1));
+            }
+            return;
+        }
+        const uint32_t xt = smem_u32(&sm.X[s][0][0]);
+        const uint32_t bt = smem_u32(&sm.Bt[s][0][0]);
+        const uint32_t ct = smem_u32(&sm.Ct[s][0][0]);
+
+        // --- C S^T (carried state) and C B^T, sharing the C fragments ---
+        float Y[8][4], G[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { Y[j][e] = 0.f; G[j][e] = 0.f; }
+        const bool carry = have_state || k > 0;
+#pragma unroll 2
+        for (int k0 = 0; k0 < NS; k0 += 16) {
+            uint32_t af[4];  // A = C^T rows m0.., from Ct[n][l]
+            ldsm_x4_t(swz(ct, k0 + rr + ((mi >> 1) << 3), (m0 >> 3) + (mi & 1)), af);
+            if (carry) {
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {  // B = S^T from Sh/Sl[p][n]
+                    uint32_t bh[4], bl[4];
+                    const int prow = 8 * j + rr + ((mi >> 1) << 3);
+                    ldsm_x4(smem_u32(&sm.Sh[prow][k0 + 8 * (mi & 1)]), bh);
+                    ldsm_x4(smem_u32(&sm.Sl[prow][k0 + 8 * (mi & 1)]), bl);
+                    mma_bf16(Y[j], af, bh[0], bh[1]);
+                    mma_bf16(Y[j + 1], af, bh[2], bh[3]);
+                    mma_bf16(Y[j], af, bl[0], bl[1]);
+                    mma_bf16(Y[j + 1], af, bl[2], bl[3]);
+                }
+            }
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp) {  // B from Bt[n][s]: columns s < m0 + 16 only
+                if (jp <= warp) {
+                    uint32_t bf[4];
+                    ldsm_x4_t(swz(bt, k0 + rr + ((mi & 1) << 3), 2 * jp + (mi >> 1)), bf);
+                    mma_bf16(G[2 * jp], af, bf[0], bf[1]);
+                    mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
+                }
+            }
+        }
+        const float cl0 = sm.c2[m0 + g], cl1 = sm.c2[m0 + g + 8];
+        if (carry) {
+            const float e0 = ex2_approx(cl0), e1 = ex2_approx(cl1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { Y[j][0] *= e0; Y[j][1] *= e0; Y[j][2] *= e1; Y[j][3] *= e1; }
+        }
+        // masked, decay-weighted C B^T -> high/low parts, rows of this warp
+#pragma unroll
+        for (int jt = 0; jt < 8; ++jt) {
+            if (jt <= 2 * warp + 1) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int l = m0 + g + 8 * hf;
+                    const float cl = hf ? cl1 : cl0;
+                    float v[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int sc = 8 * jt + 2 * tq + c;
+                        v[c] = sc <= l ? G[jt][2 * hf + c] * ex2_approx(cl - sm.c2[sc]) * sm.dt[sc] : 0.f;
+                    }
+                    uint32_t hi, lo;
+                    split2(v[0], v[1], hi, lo);
+                    *reinterpret_cast<uint32_t*>(&sm.Gh[l][8 * jt + 2 * tq]) = hi;
+                    *reinterpret_cast<uint32_t*>(&sm.Gl[l][8 * jt + 2 * tq]) = lo;
+                }
+            }
+        }
+        __syncwarp();
+        // --- Y += (masked C B^T) X^T over s < m0 + 16 ---
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            if (kb <= warp) {
+                uint32_t ah[4], al[4];
+                const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
+                ldsm_x4(smem_u32(&sm.Gh[arow][acol]), ah);
+                ldsm_x4(smem_u32(&sm.Gl[arow][acol]), al);
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {  // B = X^T from X[p][s]
+                    uint32_t bx[4];
+                    ldsm_x4(swz(xt, 8 * j + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bx);
+                    mma_bf16(Y[j], ah, bx[0], bx[1]);
+                    mma_bf16(Y[j + 1], ah, bx[2], bx[3]);
+                    mma_bf16(Y[j], al, bx[0], bx[1]);
+                    mma_bf16(Y[j + 1], al, bx[2], bx[3]);
+                }
+            }
+        }
+        // --- outputs: + D x, transposed through shared memory, row-contiguous stores ---
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int l = m0 + g + 8 * (e >> 1), p = 8 * j + 2 * tq + (e & 1);
+                sm.Yt[p][l] = Y[j][e] + Dh * swz_ld(&sm.X[s][0][0], p, l);
+            }
+        }
+        // decay-weighted x of this warp's channels -> high/low parts
+        const float clast = sm.c2[kSsdQ - 1];
+        {
+            const int p = m0 + (lane >> 1);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int sc = 32 * (lane & 1) + i;
+                const float w0 = ex2_approx(clast - sm.c2[sc]) * sm.dt[sc];
+                const float w1 = ex2_approx(clast - sm.c2[sc + 1]) * sm.dt[sc + 1];
+                uint32_t hi, lo;
+                split2(swz_ld(&sm.X[s][0][0], p, sc) * w0, swz_ld(&sm.X[s][0][0], p, sc + 1) * w1, hi, lo);
+                *reinterpret_cast<uint32_t*>(&sm.Wh[p][sc]) = hi;
+                *reinterpret_cast<uint32_t*>(&sm.Wl[p][sc]) = lo;
+            }
+        }
+        __syncthreads();  // Yt complete; Wh/Wl rows of every warp written
+        // y rows of the head's 64 channels, 8 steps per store
+#pragma unroll
+        for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
+            const int p = v >> 3, lc = (v & 7) * 8, gl = k * kSsdQ + lc;
+            if (gl >= L) continue;
+            __nv_bfloat16* dst = yb + static_cast<size_t>(p) * L + gl;
+            const float* src = &sm.Yt[p][lc];
+            if (vec_ok && gl + 8 <= L) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 o = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
+                    w[q] = *reinterpret_cast<const uint32_t*>(&o);
+                }
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                for (int q = 0; q < 8 && gl + q < L; ++q) dst[q] = __float2bfloat16_rn(src[q]);
+            }
+        }
+        // --- state: S = e^{c_Q} S + (weighted x) B^T, rows p of this warp ---
+        const float ed = ex2_approx(clast);
+#pragma unroll
+        for (int j = 0; j < kNT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) S[j][e] *= ed;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            uint32_t ah[4], al[4];
+            const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
+            ldsm_x4(smem_u32(&sm.Wh[arow][acol]), ah);
+            ldsm_x4(smem_u32(&sm.Wl[arow][acol]), al);
+#pragma unroll
+            for (int j = 0; j < kNT; j += 2) {  // B = Bt^T from Bt[n][s]
+                uint32_t bb[4];
+                ldsm_x4(swz(bt, 8 * j + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bb);
+                mma_bf16(S[j], ah, bb[0], bb[1]);
+                mma_bf16(S[j + 1], ah, bb[2], bb[3]);
+                mma_bf16(S[j], al, bb[0], bb[1]);
+                mma_bf16(S[j + 1], al, bb[2], bb[3]);
+            }
+        }
+        store_state_parts();
+        __syncthreads();  // state parts complete for the next chunk; this slot free for a refill
+    }
+
+    if (a.final_state) {
+#pragma unroll
+        for (int j = 0; j < kNT; ++j) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int p = m0 + g + 8 * hf, c = 8 * j + 2 * tq;
+                *reinterpret_cast<float2*>(a.final_state + (head_row * kSsdP + p) * NS + c) =
+                    make_float2(S[j][2 * hf], S[j][2 * hf + 1]);
+            }
+        }
+    }
+}
+
+}  // namespace mscan

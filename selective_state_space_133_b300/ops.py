@@ -244,3 +244,54 @@ def check_device_error(stream=None) -> None:
     dev = torch.device("cuda", torch.cuda.current_device())
     _lib.check(_lib.lib().mamba_check_device_error(_stream_handle(stream, dev)),
                "mamba_check_device_error")
+
+
+def ssd_workspace_bytes(batch: int, nheads: int, seqlen: int, dstate: int, headdim: int = 64) -> int:
+    """Device workspace the SSD needs for these sizes (mamba_ssd_workspace_size)."""
+    return int(_lib.lib().mamba_ssd_workspace_size(batch, nheads, headdim, seqlen, dstate, _lib.MAMBA_BF16))
+
+
+def mamba_ssd_fwd(x, delta, A, B, C, D=None, delta_bias=None, softplus=False, initial_state=None,
+                  final_state=None, y=None, stream=None, workspace=None):
+    """SSD (Mamba-2) layer (see include/mamba_scan.h, mamba_ssd_fwd).
+
+    x: (batch, nheads * 64, L) bf16; delta: (batch, nheads, L) bf16; A, D,
+    delta_bias: (nheads,) fp32; B, C: (batch, N, L) bf16, N in {64, 128};
+    initial_state: (batch, nheads, 64, N) fp32 or None; final_state: a tensor of
+    that shape, or True to allocate one. Returns y, or (y, final_state).
+    """
+    if x.dtype != torch.bfloat16:
+        raise TypeError("mamba_ssd_fwd takes bf16 inputs")
+    dev = x.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_ssd_fwd runs on CUDA tensors only")
+    batch, dim, L = x.shape
+    nheads = delta.shape[1] if delta.dim() == 3 else -1
+    P = dim // nheads if nheads > 0 else -1
+    N = B.shape[1] if B.dim() == 3 else -1
+    _need(x, "x", torch.bfloat16, (batch, dim, L), dev)
+    _need(delta, "delta", torch.bfloat16, (batch, nheads, L), dev)
+    _need(A, "A", torch.float32, (nheads,), dev)
+    _need(B, "B", torch.bfloat16, (batch, N, L), dev)
+    _need(C, "C", torch.bfloat16, (batch, N, L), dev)
+    _need(D, "D", torch.float32, (nheads,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (nheads,), dev)
+    _need(initial_state, "initial_state", torch.float32, (batch, nheads, P, N), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, (batch, dim, L), dev)
+    want_state = final_state is not None and final_state is not False
+    if final_state is True:
+        final_state = torch.empty((batch, nheads, P, N), dtype=torch.float32, device=dev)
+    elif final_state is False:
+        final_state = None
+    _need(final_state, "final_state", torch.float32, (batch, nheads, P, N), dev)
+    lib = _lib.lib()
+    need = int(lib.mamba_ssd_workspace_size(batch, nheads, P, L, N, _lib.MAMBA_BF16))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.mamba_ssd_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(delta_bias),
+                           _flags(softplus), _ptr(initial_state), _ptr(y), _ptr(final_state), batch, nheads, P, L,
+                           N, _lib.MAMBA_BF16, _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+    _lib.check(st, "mamba_ssd_fwd")
+    return (y, final_state) if want_state else y

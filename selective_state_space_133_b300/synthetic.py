@@ -109,6 +109,68 @@ DECODE_WORKLOADS: Dict[str, DecodeWorkload] = {w.name: w for w in [
 ]}
 
 
+@dataclass(frozen=True)
+class SsdWorkload:
+    """Mamba-2 layer shapes: nheads heads of 64 channels, dstate states, one B/C group."""
+    name: str
+    batch: int
+    nheads: int
+    seqlen: int
+    dstate: int
+    seed: int
+    headdim: int = 64
+
+    @property
+    def elements(self) -> int:
+        """Work units: batch * seqlen * channels * dstate (as for the scan)."""
+        return self.batch * self.seqlen * self.nheads * self.headdim * self.dstate
+
+    @property
+    def io_bytes(self) -> int:
+        """Unique bytes: x, delta, B, C read; y written (bf16)."""
+        rows = 2 * self.batch * self.nheads * self.headdim * self.seqlen
+        return 2 * (rows + self.batch * self.nheads * self.seqlen + 2 * self.batch * self.dstate * self.seqlen)
+
+
+# The paper walkthrough's Mamba-2 usage example (§5.2: d_model 2048, expand 2,
+# headdim 64, d_state 128, one sequence of 1024 tokens), and the same layer on
+# 8 x 4096 tokens.
+SSD_WORKLOADS: Dict[str, SsdWorkload] = {w.name: w for w in [
+    SsdWorkload("ssd_b1_h64_l1024_n128_bf16", 1, 64, 1024, 128, 9),
+    SsdWorkload("ssd_b8_h64_l4096_n128_bf16", 8, 64, 4096, 128, 10),
+]}
+
+
+def ssd_inputs(batch: int, nheads: int, seqlen: int, dstate: int = 128, *, headdim: int = 64, seed: int = 0,
+               with_D: bool = True, softplus_in_kernel: bool = True) -> Dict[str, Optional[torch.Tensor]]:
+    """CPU tensors for one SSD call: x, delta, A, B, C, D, delta_bias, softplus.
+
+    Draw order: x, w, dt, A, B, C, D. x, B, C ~ N(0,1); delta = w ~ 0.5 N(0,1)
+    with bias inv_softplus(dt), dt log-uniform in [1e-3, 1e-1] per head (or,
+    with softplus off, delta = softplus(w + bias) computed here); A_h drawn
+    uniformly in [-16, -1] per head. All I/O in bf16; A, D, bias fp32.
+    """
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(batch, nheads * headdim, seqlen, generator=g)
+    w = torch.randn(batch, nheads, seqlen, generator=g) * 0.5
+    dt = _dt_init(g, nheads)
+    A = -(1.0 + 15.0 * torch.rand(nheads, generator=g))
+    B = torch.randn(batch, dstate, seqlen, generator=g)
+    C = torch.randn(batch, dstate, seqlen, generator=g)
+    D = torch.randn(nheads, generator=g) if with_D else None
+    if softplus_in_kernel:
+        delta, bias = w, inv_softplus(dt).float()
+    else:
+        delta, bias = torch.nn.functional.softplus(w.double() + inv_softplus(dt)[None, :, None]).float(), None
+    cast = (lambda t: t.to(torch.bfloat16).contiguous())
+    return dict(x=cast(x), delta=cast(delta), A=A.float().contiguous(), B=cast(B), C=cast(C),
+                D=None if D is None else D.contiguous(), delta_bias=bias, softplus=softplus_in_kernel)
+
+
+def ssd_workload_inputs(w: SsdWorkload) -> Dict[str, Optional[torch.Tensor]]:
+    return ssd_inputs(w.batch, w.nheads, w.seqlen, w.dstate, headdim=w.headdim, seed=w.seed)
+
+
 def inv_softplus(dt: torch.Tensor) -> torch.Tensor:
     """x such that softplus(x) = dt (time-step bias init)."""
     return dt + torch.log(-torch.expm1(-dt))

@@ -180,3 +180,39 @@ def test_bwd_workspace_size_only_for_16_states(L):
     assert L.mamba_scan_bwd_workspace_size(2, 32, 64, 16, 1) > 0
     for n in (8, 32, 64):
         assert L.mamba_scan_bwd_workspace_size(2, 32, 64, n, 1) == 0
+
+
+def ssd(L, **kw):
+    args = dict(x=P, delta=P, A=P, B=P, C=P, D=None, bias=None, flags=1, h0=None, y=P, fs=None, batch=2, nheads=4,
+                headdim=64, seqlen=128, dstate=128, dtype=1, ws=None, ws_bytes=0)
+    args.update(kw)
+    return L.mamba_ssd_fwd(args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["bias"],
+                           args["flags"], args["h0"], args["y"], args["fs"], args["batch"], args["nheads"],
+                           args["headdim"], args["seqlen"], args["dstate"], args["dtype"], args["ws"],
+                           args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=0), -3), (dict(dtype=4), -3), (dict(flags=2), -8), (dict(flags=4), -8),
+    (dict(headdim=32), -2), (dict(headdim=128), -2), (dict(dstate=16), -2), (dict(dstate=256), -2),
+    (dict(batch=-1), -2), (dict(nheads=-1), -2), (dict(seqlen=-3), -2), (dict(batch=70000), -2),
+    (dict(A=None), -1), (dict(x=None), -1), (dict(delta=None), -1), (dict(B=None), -1), (dict(y=None), -1),
+    (dict(x=P + 8), -4), (dict(y=P + 4), -4), (dict(C=P + 2), -4), (dict(delta=P + 1), -4), (dict(fs=P + 8), -4),
+    (dict(h0=P + 4), -4), (dict(D=P + 2), -4),
+    (dict(seqlen=100), -1), (dict(seqlen=100, ws=P, ws_bytes=10), -7), (dict(seqlen=100, ws=P + 16, ws_bytes=1 << 30), -4),
+])
+def test_ssd_rejects(L, kw, code):
+    assert ssd(L, **kw) == code
+
+
+def test_ssd_empty_is_noop(L):
+    assert ssd(L, batch=0, x=None, y=None) == 0
+    assert ssd(L, nheads=0, x=None, y=None) == 0
+
+
+def test_ssd_workspace_size(L):
+    assert L.mamba_ssd_workspace_size(2, 4, 64, 128, 128, 1) == 0            # 256-byte rows: no copies
+    w = L.mamba_ssd_workspace_size(2, 4, 64, 100, 128, 1)                    # 200-byte rows: pitched copies
+    assert w >= 2 * (2 * 4 * 64 + 2 * 2 * 128) * 104
+    assert L.mamba_ssd_workspace_size(2, 4, 64, 100, 128, 0) == 0            # fp32 I/O is not supported
+    assert L.mamba_ssd_workspace_size(2, 4, 32, 100, 128, 1) == 0
