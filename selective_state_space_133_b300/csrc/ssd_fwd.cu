@@ -22,8 +22,11 @@ int launch_ssd_n(const mscan::SsdArgs& a, const void* x, const void* B, const vo
     }
     // the tiles need 1024-byte alignment inside the dynamic shared memory
     const size_t smem = sizeof(mscan::SsdSmem<NS>) + 1024;
+    // two CTAs (110 KB each at N = 128) share an SM: ask for the whole carveout
     if (cudaFuncSetAttribute(mscan::ssd_fwd_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(mscan::ssd_fwd_kernel<NS>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return MAMBA_ERR_CUDA;
     const dim3 grid(a.nheads, a.batch);
     mscan::ssd_fwd_kernel<NS><<<grid, mscan::kSsdThreads, smem, stream>>>(a, tm_x, tm_b, tm_c);

@@ -19,14 +19,19 @@
 // to ~2^-17 relative (one bf16 rounding of those operands alone costs up to
 // 1e-2 relative error in y at N = 128, over the bf16 I/O tolerance).
 //
-// One CTA (4 warps) per (head, batch row) walks the chunks in order; the fp32
+// One CTA (8 warps) per (head, batch row) walks the chunks in order; the fp32
 // state never leaves the registers (it is the state-update product's
-// accumulator). Warp w owns rows 16w..16w+15 of every per-chunk product:
-// steps l for the outputs and C B^T, channels p for the state. Lane 0 of warp
-// 0 loads the x, B and C tiles of a chunk with 3-D TMA (128-byte swizzled
-// rows) into a 2-slot ring while the CTA works on the previous chunk; the
-// operands the CTA writes itself use padded rows. Steps past the end of the
-// sequence get dt = 0, so they leave the state unchanged.
+// accumulator). Warp w owns row block w & 3 (16 rows: steps l of the outputs
+// and of C B^T, channels p of the state) and column half w >> 2 of every
+// per-chunk product, so that two CTAs (16 warps) fit on an SM and hide each
+// other's latencies. The x, B and C tiles arrive by 3-D TMA (128-byte swizzled
+// rows), each on its own barrier and refilled for the next chunk as soon as
+// its last reader is done (C after C S^T and C B^T, x after the outputs, B
+// after the state update); the operands the CTA writes itself use padded
+// rows. Within each product the high-part MMAs of all column tiles are issued
+// before the low-part ones, so no two consecutive MMAs share an accumulator.
+// Steps past the end of the sequence get dt = 0, so they leave the state
+// unchanged.
 #pragma once
 
 #include "common.cuh"
@@ -35,7 +40,7 @@ namespace mscan {
 
 constexpr int kSsdQ = 64;         // chunk length
 constexpr int kSsdP = 64;         // head dimension
-constexpr int kSsdThreads = 128;  // 4 warps
+constexpr int kSsdThreads = 256;  // 8 warps
 constexpr int kSsdPad = 8;        // row padding (bf16) of the operands written in shared memory
 
 struct SsdArgs {
@@ -53,19 +58,20 @@ struct SsdArgs {
 
 template <int NS>
 struct SsdSmem {
-    // TMA tiles: rows of 64 bf16 (128 bytes), 128-byte swizzle, two slots
-    alignas(1024) __nv_bfloat16 X[2][kSsdP][kSsdQ];   // x   [p][s]
-    alignas(1024) __nv_bfloat16 Bt[2][NS][kSsdQ];     // B   [n][s]
-    alignas(1024) __nv_bfloat16 Ct[2][NS][kSsdQ];     // C   [n][l]
-    // operands computed here, high and low bf16 parts
-    alignas(16) __nv_bfloat16 Gh[kSsdQ][kSsdQ + kSsdPad], Gl[kSsdQ][kSsdQ + kSsdPad];  // masked C B^T [l][s]
-    alignas(16) __nv_bfloat16 Wh[kSsdP][kSsdQ + kSsdPad], Wl[kSsdP][kSsdQ + kSsdPad];  // weighted x   [p][s]
-    alignas(16) __nv_bfloat16 Sh[kSsdP][NS + kSsdPad], Sl[kSsdP][NS + kSsdPad];        // state        [p][n]
+    // TMA tiles: rows of 64 bf16 (128 bytes), 128-byte swizzle
+    alignas(1024) __nv_bfloat16 X[kSsdP][kSsdQ];   // x   [p][s]
+    alignas(1024) __nv_bfloat16 Bt[NS][kSsdQ];     // B   [n][s]
+    alignas(1024) __nv_bfloat16 Ct[NS][kSsdQ];     // C   [n][l]
+    // operands computed here, high and low bf16 parts: the masked C B^T [l][s]
+    // until its product with x is done, then the decay-weighted x [p][s]
+    alignas(16) __nv_bfloat16 Oh[kSsdQ][kSsdQ + kSsdPad], Ol[kSsdQ][kSsdQ + kSsdPad];
+    alignas(16) __nv_bfloat16 Sh[kSsdP][NS + kSsdPad], Sl[kSsdP][NS + kSsdPad];  // state [p][n]
     alignas(16) float Yt[kSsdP][kSsdQ + 4];  // the chunk's outputs [p][l], for row-contiguous stores
     float c2[kSsdQ];                         // c_l * log2(e)
     float dt[kSsdQ];
-    alignas(8) uint64_t full[2];
+    alignas(8) uint64_t full[3];             // x, B, C tiles
 };
+static_assert(kSsdQ == kSsdP, "the O buffers hold both Q x Q and P x Q operands");
 
 // ------------------------------------------------------------ helpers ------
 
@@ -103,20 +109,24 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+
 // ------------------------------------------------------------- kernel ------
 
 template <int NS>
-__global__ void __launch_bounds__(kSsdThreads, 1)
+__global__ void __launch_bounds__(kSsdThreads, 2)
 ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c) {
     extern __shared__ unsigned char ssd_smem_raw[];
     SsdSmem<NS>& sm = *reinterpret_cast<SsdSmem<NS>*>(
         (reinterpret_cast<uintptr_t>(ssd_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    constexpr int kNT = NS / 8;  // 8-column tiles of the state
+    constexpr int kNH = NS / 16;  // 8-column state tiles of a warp (half of the state)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;      // accumulator row group / column pair
     const int mi = lane >> 3, rr = lane & 7;     // ldmatrix: which 8x8 matrix, which row of it
-    const int m0 = 16 * warp;                    // this warp's rows
+    const int rb = warp & 3, chalf = warp >> 2;
+    const int m0 = 16 * rb;                      // this warp's rows
+    const int c0 = 32 * chalf;                   // its half of the 64 columns (channels p, or steps s of C B^T)
+    const int n0 = chalf * (NS / 2);             // its half of the state columns
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = a.seqlen;
     const int n = (L + kSsdQ - 1) / kSsdQ;
@@ -127,41 +137,50 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const float Dh = a.D ? a.D[h] : 0.f;
     const size_t head_row = static_cast<size_t>(b) * a.nheads + h;
 
-    // Chunk k's x, B and C tiles into slot k & 1 (one thread).
-    auto issue = [&](int k) {
-        uint64_t* bar = &sm.full[k & 1];
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>((kSsdP + 2 * NS) * kSsdQ * 2));
-        tma_load_3d(&sm.X[k & 1][0][0], &tm_x, bar, k * kSsdQ, ch0, b);
-        tma_load_3d(&sm.Bt[k & 1][0][0], &tm_b, bar, k * kSsdQ, 0, b);
-        tma_load_3d(&sm.Ct[k & 1][0][0], &tm_c, bar, k * kSsdQ, 0, b);
+    // tile loads of chunk k (thread 0): barrier 0 = x, 1 = B, 2 = C; parity k & 1
+    int last[3] = {-1, -1, -1};
+    auto issue = [&](int which, int k) {
+        uint64_t* bar = &sm.full[which];
+        const int l0 = k * kSsdQ;
+        if (which == 0) {
+            mbar_arrive_expect_tx(bar, kSsdP * kSsdQ * 2);
+            tma_load_3d(&sm.X[0][0], &tm_x, bar, l0, ch0, b);
+        } else {
+            mbar_arrive_expect_tx(bar, NS * kSsdQ * 2);
+            tma_load_3d(which == 1 ? &sm.Bt[0][0] : &sm.Ct[0][0], which == 1 ? &tm_b : &tm_c, bar, l0, 0, b);
+        }
+        last[which] = k;
+    };
+    // after a timeout: wait (bounded) for this thread's copies still in flight
+    auto drain = [&]() {
+        for (int i = 0; i < 3; ++i)
+            if (last[i] >= 0) mbar_wait_bounded(&sm.full[i], static_cast<uint32_t>(last[i] & 1));
     };
     if (tid == 0) {
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&sm.full[i], 1);
         fence_barrier_init();
-        if (n > 0) issue(0);
+        if (n > 0) { issue(2, 0); issue(1, 0); issue(0, 0); }
     }
 
-    // The state: rows m0 + g (+8) and columns 8j + 2tq (+1) of this warp's block.
-    float S[kNT][4];
+    // The state: rows m0 + g (+8), columns n0 + 8j + 2tq (+1).
+    float S[kNH][4];
     const bool have_state = a.h0 != nullptr;
 #pragma unroll
-    for (int j = 0; j < kNT; ++j) {
+    for (int j = 0; j < kNH; ++j) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int p = m0 + g + 8 * (e >> 1), c = 8 * j + 2 * tq + (e & 1);
+            const int p = m0 + g + 8 * (e >> 1), c = n0 + 8 * j + 2 * tq + (e & 1);
             S[j][e] = have_state ? a.h0[(head_row * kSsdP + p) * NS + c] : 0.f;
         }
     }
-    // high and low bf16 parts of the state, for the next chunk's C S^T
     auto store_state_parts = [&]() {
 #pragma unroll
-        for (int j = 0; j < kNT; ++j) {
+        for (int j = 0; j < kNH; ++j) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t hi, lo;
                 split2(S[j][2 * hf], S[j][2 * hf + 1], hi, lo);
-                const int p = m0 + g + 8 * hf, c = 8 * j + 2 * tq;
+                const int p = m0 + g + 8 * hf, c = n0 + 8 * j + 2 * tq;
                 *reinterpret_cast<uint32_t*>(&sm.Sh[p][c]) = hi;
                 *reinterpret_cast<uint32_t*>(&sm.Sl[p][c]) = lo;
             }
@@ -173,16 +192,13 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(a.delta) + head_row * L;
     __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
     const bool vec_ok = (L & 7) == 0;
+    const uint32_t xt = smem_u32(&sm.X[0][0]);
+    const uint32_t bt = smem_u32(&sm.Bt[0][0]);
+    const uint32_t ct = smem_u32(&sm.Ct[0][0]);
 
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
-        const int s = k & 1;
-        // the next chunk into the other slot: its last reader (chunk k - 1)
-        // finished at the barrier that ended the previous iteration
-        if (tid == 0 && k + 1 < n) {
-            fence_proxy_async_smem();
-            issue(k + 1);
-        }
+        const uint32_t par = static_cast<uint32_t>(k & 1);
         // dt and the cumulative decay of the chunk (warp 0); padding steps get dt = 0
         if (warp == 0) {
             float v[2];
@@ -208,23 +224,19 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             sm.c2[2 * lane] = excl + v[0];
             sm.c2[2 * lane + 1] = excl + pair;
         }
-        // the chunk's tiles (bounded wait); the barrier also publishes dt and c2
-        const bool ok = mbar_wait_bounded(&sm.full[s], static_cast<uint32_t>((k >> 1) & 1));
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0) {
-                report_device_error(a.err, -6);
-                if (k + 1 < n) mbar_wait_bounded(&sm.full[(k + 1) & 1], static_cast<uint32_t>(((k + 1) >> 1) & 1));
+        // C and B tiles (bounded wait); the barrier also publishes dt and c2
+        {
+            const bool ok = mbar_wait_bounded(&sm.full[2], par) && mbar_wait_bounded(&sm.full[1], par);
+            if (!__syncthreads_and(ok)) {
+                if (tid == 0) { report_device_error(a.err, -6); drain(); }
+                return;
             }
-            return;
         }
-        const uint32_t xt = smem_u32(&sm.X[s][0][0]);
-        const uint32_t bt = smem_u32(&sm.Bt[s][0][0]);
-        const uint32_t ct = smem_u32(&sm.Ct[s][0][0]);
 
         // --- C S^T (carried state) and C B^T, sharing the C fragments ---
-        float Y[8][4], G[8][4];
+        float Y[4][4], G[4][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) { Y[j][e] = 0.f; G[j][e] = 0.f; }
         const bool carry = have_state || k > 0;
@@ -232,24 +244,30 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         for (int k0 = 0; k0 < NS; k0 += 16) {
             uint32_t af[4];  // A = C^T rows m0.., from Ct[n][l]
             ldsm_x4_t(swz(ct, k0 + rr + ((mi >> 1) << 3), (m0 >> 3) + (mi & 1)), af);
-            if (carry) {
+            if (carry) {  // B = S^T from Sh/Sl[p][n], p in this warp's column half
+                uint32_t bh[2][4], bl[2][4];
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) {  // B = S^T from Sh/Sl[p][n]
-                    uint32_t bh[4], bl[4];
-                    const int prow = 8 * j + rr + ((mi >> 1) << 3);
-                    ldsm_x4(smem_u32(&sm.Sh[prow][k0 + 8 * (mi & 1)]), bh);
-                    ldsm_x4(smem_u32(&sm.Sl[prow][k0 + 8 * (mi & 1)]), bl);
-                    mma_bf16(Y[j], af, bh[0], bh[1]);
-                    mma_bf16(Y[j + 1], af, bh[2], bh[3]);
-                    mma_bf16(Y[j], af, bl[0], bl[1]);
-                    mma_bf16(Y[j + 1], af, bl[2], bl[3]);
+                for (int jp = 0; jp < 2; ++jp) {
+                    const int prow = c0 + 16 * jp + rr + ((mi >> 1) << 3);
+                    ldsm_x4(smem_u32(&sm.Sh[prow][k0 + 8 * (mi & 1)]), bh[jp]);
+                    ldsm_x4(smem_u32(&sm.Sl[prow][k0 + 8 * (mi & 1)]), bl[jp]);
+                }
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mma_bf16(Y[2 * jp], af, bh[jp][0], bh[jp][1]);
+                    mma_bf16(Y[2 * jp + 1], af, bh[jp][2], bh[jp][3]);
+                }
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mma_bf16(Y[2 * jp], af, bl[jp][0], bl[jp][1]);
+                    mma_bf16(Y[2 * jp + 1], af, bl[jp][2], bl[jp][3]);
                 }
             }
 #pragma unroll
-            for (int jp = 0; jp < 4; ++jp) {  // B from Bt[n][s]: columns s < m0 + 16 only
-                if (jp <= warp) {
+            for (int jp = 0; jp < 2; ++jp) {  // B from Bt[n][s]: columns s <= m0 + 15 only
+                if (2 * chalf + jp <= rb) {
                     uint32_t bf[4];
-                    ldsm_x4_t(swz(bt, k0 + rr + ((mi & 1) << 3), 2 * jp + (mi >> 1)), bf);
+                    ldsm_x4_t(swz(bt, k0 + rr + ((mi & 1) << 3), (c0 >> 3) + 2 * jp + (mi >> 1)), bf);
                     mma_bf16(G[2 * jp], af, bf[0], bf[1]);
                     mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
                 }
@@ -259,12 +277,12 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         if (carry) {
             const float e0 = ex2_approx(cl0), e1 = ex2_approx(cl1);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) { Y[j][0] *= e0; Y[j][1] *= e0; Y[j][2] *= e1; Y[j][3] *= e1; }
+            for (int j = 0; j < 4; ++j) { Y[j][0] *= e0; Y[j][1] *= e0; Y[j][2] *= e1; Y[j][3] *= e1; }
         }
-        // masked, decay-weighted C B^T -> high/low parts, rows of this warp
+        // masked, decay-weighted C B^T -> high/low parts (rows m0.., this warp's columns)
 #pragma unroll
-        for (int jt = 0; jt < 8; ++jt) {
-            if (jt <= 2 * warp + 1) {
+        for (int jt = 0; jt < 4; ++jt) {
+            if (2 * chalf + (jt >> 1) <= rb) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int l = m0 + g + 8 * hf;
@@ -272,61 +290,81 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                     float v[2];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const int sc = 8 * jt + 2 * tq + c;
+                        const int sc = c0 + 8 * jt + 2 * tq + c;
                         v[c] = sc <= l ? G[jt][2 * hf + c] * ex2_approx(cl - sm.c2[sc]) * sm.dt[sc] : 0.f;
                     }
                     uint32_t hi, lo;
                     split2(v[0], v[1], hi, lo);
-                    *reinterpret_cast<uint32_t*>(&sm.Gh[l][8 * jt + 2 * tq]) = hi;
-                    *reinterpret_cast<uint32_t*>(&sm.Gl[l][8 * jt + 2 * tq]) = lo;
+                    *reinterpret_cast<uint32_t*>(&sm.Oh[l][c0 + 8 * jt + 2 * tq]) = hi;
+                    *reinterpret_cast<uint32_t*>(&sm.Ol[l][c0 + 8 * jt + 2 * tq]) = lo;
                 }
             }
         }
-        __syncwarp();
+        // C is consumed: load the next chunk's; wait for this chunk's x. The
+        // barrier also publishes the masked rows of both column halves.
+        if (tid == 0 && k + 1 < n) {
+            fence_proxy_async_smem();
+            issue(2, k + 1);
+        }
+        {
+            const bool ok = mbar_wait_bounded(&sm.full[0], par);
+            if (!__syncthreads_and(ok)) {
+                if (tid == 0) { report_device_error(a.err, -6); drain(); }
+                return;
+            }
+        }
         // --- Y += (masked C B^T) X^T over s < m0 + 16 ---
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
-            if (kb <= warp) {
-                uint32_t ah[4], al[4];
+            if (kb <= rb) {
+                uint32_t ah[4], al[4], bx[2][4];
                 const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
-                ldsm_x4(smem_u32(&sm.Gh[arow][acol]), ah);
-                ldsm_x4(smem_u32(&sm.Gl[arow][acol]), al);
+                ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
+                ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) {  // B = X^T from X[p][s]
-                    uint32_t bx[4];
-                    ldsm_x4(swz(xt, 8 * j + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bx);
-                    mma_bf16(Y[j], ah, bx[0], bx[1]);
-                    mma_bf16(Y[j + 1], ah, bx[2], bx[3]);
-                    mma_bf16(Y[j], al, bx[0], bx[1]);
-                    mma_bf16(Y[j + 1], al, bx[2], bx[3]);
+                for (int jp = 0; jp < 2; ++jp)  // B = X^T from X[p][s]
+                    ldsm_x4(swz(xt, c0 + 16 * jp + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bx[jp]);
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mma_bf16(Y[2 * jp], ah, bx[jp][0], bx[jp][1]);
+                    mma_bf16(Y[2 * jp + 1], ah, bx[jp][2], bx[jp][3]);
+                }
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mma_bf16(Y[2 * jp], al, bx[jp][0], bx[jp][1]);
+                    mma_bf16(Y[2 * jp + 1], al, bx[jp][2], bx[jp][3]);
                 }
             }
         }
-        // --- outputs: + D x, transposed through shared memory, row-contiguous stores ---
+        __syncthreads();  // every warp is done with the masked rows: the O buffers take the weighted x
+        // --- outputs (+ D x) into Yt; decay-weighted x into the O buffers ---
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int l = m0 + g + 8 * (e >> 1), p = 8 * j + 2 * tq + (e & 1);
-                sm.Yt[p][l] = Y[j][e] + Dh * swz_ld(&sm.X[s][0][0], p, l);
+                const int l = m0 + g + 8 * (e >> 1), p = c0 + 8 * j + 2 * tq + (e & 1);
+                sm.Yt[p][l] = Y[j][e] + Dh * swz_ld(&sm.X[0][0], p, l);
             }
         }
-        // decay-weighted x of this warp's channels -> high/low parts
         const float clast = sm.c2[kSsdQ - 1];
         {
             const int p = m0 + (lane >> 1);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int sc = 32 * (lane & 1) + i;
+            for (int i = 0; i < 16; i += 2) {
+                const int sc = c0 + 16 * (lane & 1) + i;
                 const float w0 = ex2_approx(clast - sm.c2[sc]) * sm.dt[sc];
                 const float w1 = ex2_approx(clast - sm.c2[sc + 1]) * sm.dt[sc + 1];
                 uint32_t hi, lo;
-                split2(swz_ld(&sm.X[s][0][0], p, sc) * w0, swz_ld(&sm.X[s][0][0], p, sc + 1) * w1, hi, lo);
-                *reinterpret_cast<uint32_t*>(&sm.Wh[p][sc]) = hi;
-                *reinterpret_cast<uint32_t*>(&sm.Wl[p][sc]) = lo;
+                split2(swz_ld(&sm.X[0][0], p, sc) * w0, swz_ld(&sm.X[0][0], p, sc + 1) * w1, hi, lo);
+                *reinterpret_cast<uint32_t*>(&sm.Oh[p][sc]) = hi;
+                *reinterpret_cast<uint32_t*>(&sm.Ol[p][sc]) = lo;
             }
         }
-        __syncthreads();  // Yt complete; Wh/Wl rows of every warp written
+        __syncthreads();  // Yt and the weighted x complete; x is consumed
+        if (tid == 0 && k + 1 < n) {
+            fence_proxy_async_smem();
+            issue(0, k + 1);
+        }
         // y rows of the head's 64 channels, 8 steps per store
 #pragma unroll
         for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
@@ -346,38 +384,46 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 for (int q = 0; q < 8 && gl + q < L; ++q) dst[q] = __float2bfloat16_rn(src[q]);
             }
         }
-        // --- state: S = e^{c_Q} S + (weighted x) B^T, rows p of this warp ---
+        // --- state: S = e^{c_Q} S + (weighted x) B^T: rows m0.., this warp's state half ---
         const float ed = ex2_approx(clast);
 #pragma unroll
-        for (int j = 0; j < kNT; ++j)
+        for (int j = 0; j < kNH; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) S[j][e] *= ed;
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
-            uint32_t ah[4], al[4];
+            uint32_t ah[4], al[4], bb[kNH / 2][4];
             const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
-            ldsm_x4(smem_u32(&sm.Wh[arow][acol]), ah);
-            ldsm_x4(smem_u32(&sm.Wl[arow][acol]), al);
+            ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
+            ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
 #pragma unroll
-            for (int j = 0; j < kNT; j += 2) {  // B = Bt^T from Bt[n][s]
-                uint32_t bb[4];
-                ldsm_x4(swz(bt, 8 * j + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bb);
-                mma_bf16(S[j], ah, bb[0], bb[1]);
-                mma_bf16(S[j + 1], ah, bb[2], bb[3]);
-                mma_bf16(S[j], al, bb[0], bb[1]);
-                mma_bf16(S[j + 1], al, bb[2], bb[3]);
+            for (int jp = 0; jp < kNH / 2; ++jp)  // B = Bt^T from Bt[n][s]
+                ldsm_x4(swz(bt, n0 + 16 * jp + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bb[jp]);
+#pragma unroll
+            for (int jp = 0; jp < kNH / 2; ++jp) {
+                mma_bf16(S[2 * jp], ah, bb[jp][0], bb[jp][1]);
+                mma_bf16(S[2 * jp + 1], ah, bb[jp][2], bb[jp][3]);
+            }
+#pragma unroll
+            for (int jp = 0; jp < kNH / 2; ++jp) {
+                mma_bf16(S[2 * jp], al, bb[jp][0], bb[jp][1]);
+                mma_bf16(S[2 * jp + 1], al, bb[jp][2], bb[jp][3]);
             }
         }
         store_state_parts();
-        __syncthreads();  // state parts complete for the next chunk; this slot free for a refill
+        __syncthreads();  // state parts complete for the next chunk; B is consumed
+        if (tid == 0 && k + 1 < n) {
+            fence_proxy_async_smem();
+            issue(1, k + 1);
+        }
     }
 
     if (a.final_state) {
 #pragma unroll
-        for (int j = 0; j < kNT; ++j) {
+        for (int j = 0; j < kNH; ++j) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const int p = m0 + g + 8 * hf, c = 8 * j + 2 * tq;
+                const int p = m0 + g + 8 * hf, c = n0 + 8 * j + 2 * tq;
                 *reinterpret_cast<float2*>(a.final_state + (head_row * kSsdP + p) * NS + c) =
                     make_float2(S[j][2 * hf], S[j][2 * hf + 1]);
             }
