@@ -654,6 +654,123 @@ def run_conv(args, w):
     return 0
 
 
+def run_ssd(args, w):
+    """One step = one mamba_ssd_fwd call (the Mamba-2 chunked form) on the workload, inputs resident in HBM."""
+    import torch
+    from selective_state_space_133_b300 import ops
+    from selective_state_space_133_b300 import synthetic as syn
+
+    ws, rank, local = dist_setup(want_nccl=True)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    x = syn.ssd_inputs(w.batch, w.nheads, w.seqlen, w.dstate, headdim=w.headdim, seed=w.seed + 7919 * rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y = torch.empty_like(d["x"])
+    work = torch.empty(max(1, ops.ssd_workspace_bytes(w.batch, w.nheads, w.seqlen, w.dstate)), dtype=torch.uint8,
+                       device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ops.mamba_ssd_fwd(d["x"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["delta_bias"], d["softplus"], y=y,
+                          stream=stream, workspace=work)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ops.check_device_error(stream)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    sampler = ClockSampler(vis.split(",")[local] if vis else str(local)) if rank == 0 else None
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 1.0:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clocks = sampler.stop() if sampler else None
+    ops.check_device_error(stream)
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / K
+    value = ws * w.elements / (ms * 1e-3)
+
+    # e2e: pinned host inputs -> device, the call, y -> pinned host, every step
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = y_host.numel() * y_host.element_size()
+    K2 = max(3, min(K, 20))
+
+    def e2e_step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                d[k].copy_(v, non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / K2
+    if rank != 0:
+        return 0
+    peak, peak_kind = hbm_peak()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tc_peak, tc_kind = float(json.load(f)["bf16_tflops"]), "measured cuBLAS bf16 burst"
+    except Exception:
+        tc_peak, tc_kind = 1800.0, "fallback"
+    gbs = w.io_bytes / (ms * 1e-3) / 1e9
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    # CPU baseline: the fp64 oracle on whole heads of batch row 0 for ~10 s
+    import oracle
+    budget = float(os.environ.get("BENCH_CPU_BASELINE_S", "10"))
+    nh, el, t_cpu = 1, 0, 0.0
+    while t_cpu < budget / 2 and nh <= w.nheads:
+        ch = slice(0, nh * w.headdim)
+        t0 = time.perf_counter()
+        oracle.ssd(x["x"][:1, ch], x["delta"][:1, :nh], x["A"][:nh], x["B"][:1], x["C"][:1],
+                   None if x["D"] is None else x["D"][:nh],
+                   None if x["delta_bias"] is None else x["delta_bias"][:nh], x["softplus"])
+        t_cpu = time.perf_counter() - t0
+        el = nh * w.headdim * w.seqlen * w.dstate
+        nh *= 2
+    line = {
+        "metric": "SSD (Mamba-2 chunked form) elems/s (B·L·D·N), 1×B300",
+        "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "nheads": w.nheads, "headdim": w.headdim,
+                   "seqlen": w.seqlen, "dstate": w.dstate, "chunk": 64, "io_dtype": "bf16", "state_dtype": "fp32",
+                   "parallelism": f"replicas x{ws}", "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB"},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "peak_source": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes,
+                     "tensor_tflops": tflops, "tensor_peak_tflops": tc_peak, "tensor_peak_source": tc_kind,
+                     "tensor_frac": tflops / tc_peak, "algorithmic_flops_per_launch": w.flops,
+                     "note": "HBM bounds the roofline time of this workload (bytes / copy peak > flops / bf16 peak)"},
+        "clocks": clocks,
+        "e2e": {"value": ws * w.elements / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": K2},
+        "cpu_baseline": {"value": el / t_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{el // (w.headdim * w.seqlen * w.dstate)} whole heads of batch row 0 "
+                                   f"({el} elements), fp64, {t_cpu:.1f} s"},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -665,6 +782,10 @@ def main():
                     help="bwd: the backward (all gradients); conv: the scan with the fused conv1d + SiLU")
     args = ap.parse_args()
     from selective_state_space_133_b300 import synthetic as syn
+    if args.workload in syn.SSD_WORKLOADS:
+        if args.impl == "reference":
+            raise SystemExit("--impl reference times the scan workload only")
+        return run_ssd(args, syn.SSD_WORKLOADS[args.workload])
     if args.workload in syn.DECODE_WORKLOADS:
         if args.impl == "reference":
             raise SystemExit("--impl reference times the scan workload only")

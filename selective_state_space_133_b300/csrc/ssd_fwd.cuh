@@ -67,8 +67,8 @@ struct SsdSmem {
     alignas(16) __nv_bfloat16 Oh[kSsdQ][kSsdQ + kSsdPad], Ol[kSsdQ][kSsdQ + kSsdPad];
     alignas(16) __nv_bfloat16 Sh[kSsdP][NS + kSsdPad], Sl[kSsdP][NS + kSsdPad];  // state [p][n]
     alignas(16) float Yt[kSsdP][kSsdQ + 4];  // the chunk's outputs [p][l], for row-contiguous stores
-    float c2[kSsdQ];                         // c_l * log2(e)
-    float dt[kSsdQ];
+    float c2[2][kSsdQ];                      // c_l * log2(e), chunk k in [k & 1]
+    float dt[2][kSsdQ];
     alignas(8) uint64_t full[3];             // x, B, C tiles
 };
 static_assert(kSsdQ == kSsdP, "the O buffers hold both Q x Q and P x Q operands");
@@ -90,11 +90,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Shared address of 16-byte unit `chunk` (0..7) of row `row` in a tile of
-// 128-byte rows written by TMA with the 128-byte swizzle (tile base 1024-aligned).
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
-    return base + row * 128 + ((chunk ^ (row & 7)) << 4);
-}
+// Element (row, col) of a tile of 128-byte rows written by TMA with the
+// 128-byte swizzle (16-byte unit u of row r stored at unit u ^ (r & 7); tile
+// base 1024-aligned).
 __device__ __forceinline__ float swz_ld(const __nv_bfloat16* tile, int row, int col) {
     const unsigned char* p = reinterpret_cast<const unsigned char*>(tile) + row * 128 +
                              ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1));
@@ -117,8 +115,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2)
 ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c) {
     extern __shared__ unsigned char ssd_smem_raw[];
-    SsdSmem<NS>& sm = *reinterpret_cast<SsdSmem<NS>*>(
-        (reinterpret_cast<uintptr_t>(ssd_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned view of the dynamic shared memory, derived from the
+    // shared array itself so that every access stays a shared-memory access
+    SsdSmem<NS>& sm = *reinterpret_cast<SsdSmem<NS>*>(ssd_smem_raw + ((1024u - (smem_u32(ssd_smem_raw) & 1023u)) & 1023u));
     constexpr int kNH = NS / 16;  // 8-column state tiles of a warp (half of the state)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, tq = lane & 3;      // accumulator row group / column pair
@@ -195,60 +194,73 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const uint32_t xt = smem_u32(&sm.X[0][0]);
     const uint32_t bt = smem_u32(&sm.Bt[0][0]);
     const uint32_t ct = smem_u32(&sm.Ct[0][0]);
+    // Loop-invariant parts of the ldmatrix addresses. Rows of the swizzled
+    // tiles advance in steps of 8, so their swizzle term (row & 7) is fixed.
+    const int ra = rr + ((mi >> 1) << 3);        // row of this lane in matrices ordered (row, row, row+8, row+8)
+    const int rc = rr + ((mi & 1) << 3);         // ... ordered (row, row+8, row, row+8)
+    const uint32_t a_c = ct + ra * 128 + ((((m0 >> 3) + (mi & 1)) ^ (ra & 7)) << 4);   // C^T rows m0.. at k0 = 0
+    uint32_t b_g[2];                             // B tile for C B^T, column pairs c0 + 16 jp, at k0 = 0
+#pragma unroll
+    for (int jp = 0; jp < 2; ++jp) b_g[jp] = bt + rc * 128 + ((((c0 >> 3) + 2 * jp + (mi >> 1)) ^ (rc & 7)) << 4);
+    const uint32_t x_row = xt + (c0 + ra) * 128;  // X rows c0 + ra (+16 jp)
+    const uint32_t b_row = bt + (n0 + ra) * 128;  // Bt rows n0 + ra (+16 jp)
+    const int sw = ra & 7;
 
+    // dt and the cumulative decay of chunk k into buffer k & 1 (warp 0);
+    // padding steps get dt = 0
+    auto decay_prefix = [&](int k) {
+        float v[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int l = 2 * lane + i, gl = k * kSsdQ + l;
+            float d = 0.f;
+            if (gl < L) {
+                d = __bfloat162float(dl[gl]) + bias;
+                if (a.softplus) d = softplus_f(d);
+            }
+            sm.dt[k & 1][l] = d;
+            v[i] = d * Ah2;
+        }
+        const float pair = v[0] + v[1];
+        float incl = pair;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const float excl = incl - pair;
+        sm.c2[k & 1][2 * lane] = excl + v[0];
+        sm.c2[k & 1][2 * lane + 1] = excl + pair;
+    };
+    if (warp == 0 && n > 0) decay_prefix(0);
+    __syncthreads();
+
+    // A wait that runs out sets `timed_out`; the chunk is finished with
+    // whatever the tiles hold and the kernel leaves at the chunk's last
+    // barrier, so that no thread is ever left waiting at a barrier.
+    bool timed_out = false;
 #pragma unroll 1
     for (int k = 0; k < n; ++k) {
         const uint32_t par = static_cast<uint32_t>(k & 1);
-        // dt and the cumulative decay of the chunk (warp 0); padding steps get dt = 0
-        if (warp == 0) {
-            float v[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int l = 2 * lane + i, gl = k * kSsdQ + l;
-                float d = 0.f;
-                if (gl < L) {
-                    d = __bfloat162float(dl[gl]) + bias;
-                    if (a.softplus) d = softplus_f(d);
-                }
-                sm.dt[l] = d;
-                v[i] = d * Ah2;
-            }
-            const float pair = v[0] + v[1];
-            float incl = pair;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const float excl = incl - pair;
-            sm.c2[2 * lane] = excl + v[0];
-            sm.c2[2 * lane + 1] = excl + pair;
-        }
-        // C and B tiles (bounded wait); the barrier also publishes dt and c2
-        {
-            const bool ok = mbar_wait_bounded(&sm.full[2], par) && mbar_wait_bounded(&sm.full[1], par);
-            if (!__syncthreads_and(ok)) {
-                if (tid == 0) { report_device_error(a.err, -6); drain(); }
-                return;
-            }
-        }
+        const float* c2 = sm.c2[k & 1];
+        const float* dtv = sm.dt[k & 1];
+        if (!mbar_wait_bounded(&sm.full[2], par)) timed_out = true;  // C
 
-        // --- C S^T (carried state) and C B^T, sharing the C fragments ---
+        // --- C S^T (carried state), then C B^T once B is in ---
         float Y[4][4], G[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) { Y[j][e] = 0.f; G[j][e] = 0.f; }
         const bool carry = have_state || k > 0;
-#pragma unroll 2
-        for (int k0 = 0; k0 < NS; k0 += 16) {
-            uint32_t af[4];  // A = C^T rows m0.., from Ct[n][l]
-            ldsm_x4_t(swz(ct, k0 + rr + ((mi >> 1) << 3), (m0 >> 3) + (mi & 1)), af);
-            if (carry) {  // B = S^T from Sh/Sl[p][n], p in this warp's column half
-                uint32_t bh[2][4], bl[2][4];
+        if (carry) {
+#pragma unroll
+            for (int k0 = 0; k0 < NS; k0 += 16) {
+                uint32_t af[4], bh[2][4], bl[2][4];  // A = C^T rows m0.. from Ct[n][l]; B = S^T from Sh/Sl[p][n]
+                ldsm_x4_t(a_c + k0 * 128, af);
 #pragma unroll
                 for (int jp = 0; jp < 2; ++jp) {
-                    const int prow = c0 + 16 * jp + rr + ((mi >> 1) << 3);
+                    const int prow = c0 + 16 * jp + ra;
                     ldsm_x4(smem_u32(&sm.Sh[prow][k0 + 8 * (mi & 1)]), bh[jp]);
                     ldsm_x4(smem_u32(&sm.Sl[prow][k0 + 8 * (mi & 1)]), bl[jp]);
                 }
@@ -263,17 +275,25 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                     mma_bf16(Y[2 * jp + 1], af, bl[jp][2], bl[jp][3]);
                 }
             }
+        }
+        if (!mbar_wait_bounded(&sm.full[1], par)) timed_out = true;  // B
+        if (2 * chalf <= rb) {  // columns s <= m0 + 15 only
 #pragma unroll
-            for (int jp = 0; jp < 2; ++jp) {  // B from Bt[n][s]: columns s <= m0 + 15 only
-                if (2 * chalf + jp <= rb) {
-                    uint32_t bf[4];
-                    ldsm_x4_t(swz(bt, k0 + rr + ((mi & 1) << 3), (c0 >> 3) + 2 * jp + (mi >> 1)), bf);
-                    mma_bf16(G[2 * jp], af, bf[0], bf[1]);
-                    mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
+            for (int k0 = 0; k0 < NS; k0 += 16) {
+                uint32_t af[4];
+                ldsm_x4_t(a_c + k0 * 128, af);
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    if (2 * chalf + jp <= rb) {
+                        uint32_t bf[4];
+                        ldsm_x4_t(b_g[jp] + k0 * 128, bf);
+                        mma_bf16(G[2 * jp], af, bf[0], bf[1]);
+                        mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
+                    }
                 }
             }
         }
-        const float cl0 = sm.c2[m0 + g], cl1 = sm.c2[m0 + g + 8];
+        const float cl0 = c2[m0 + g], cl1 = c2[m0 + g + 8];
         if (carry) {
             const float e0 = ex2_approx(cl0), e1 = ex2_approx(cl1);
 #pragma unroll
@@ -291,7 +311,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const int sc = c0 + 8 * jt + 2 * tq + c;
-                        v[c] = sc <= l ? G[jt][2 * hf + c] * ex2_approx(cl - sm.c2[sc]) * sm.dt[sc] : 0.f;
+                        v[c] = sc <= l ? G[jt][2 * hf + c] * ex2_approx(cl - c2[sc]) * dtv[sc] : 0.f;
                     }
                     uint32_t hi, lo;
                     split2(v[0], v[1], hi, lo);
@@ -300,19 +320,12 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 }
             }
         }
-        // C is consumed: load the next chunk's; wait for this chunk's x. The
-        // barrier also publishes the masked rows of both column halves.
-        if (tid == 0 && k + 1 < n) {
+        __syncthreads();  // the masked rows of both column halves are in; C is consumed
+        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
             fence_proxy_async_smem();
             issue(2, k + 1);
         }
-        {
-            const bool ok = mbar_wait_bounded(&sm.full[0], par);
-            if (!__syncthreads_and(ok)) {
-                if (tid == 0) { report_device_error(a.err, -6); drain(); }
-                return;
-            }
-        }
+        if (!mbar_wait_bounded(&sm.full[0], par)) timed_out = true;  // x
         // --- Y += (masked C B^T) X^T over s < m0 + 16 ---
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) {
@@ -323,7 +336,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
 #pragma unroll
                 for (int jp = 0; jp < 2; ++jp)  // B = X^T from X[p][s]
-                    ldsm_x4(swz(xt, c0 + 16 * jp + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bx[jp]);
+                    ldsm_x4(x_row + jp * 16 * 128 + (((2 * kb + (mi & 1)) ^ sw) << 4), bx[jp]);
 #pragma unroll
                 for (int jp = 0; jp < 2; ++jp) {
                     mma_bf16(Y[2 * jp], ah, bx[jp][0], bx[jp][1]);
@@ -346,14 +359,14 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 sm.Yt[p][l] = Y[j][e] + Dh * swz_ld(&sm.X[0][0], p, l);
             }
         }
-        const float clast = sm.c2[kSsdQ - 1];
+        const float clast = c2[kSsdQ - 1];
         {
             const int p = m0 + (lane >> 1);
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
                 const int sc = c0 + 16 * (lane & 1) + i;
-                const float w0 = ex2_approx(clast - sm.c2[sc]) * sm.dt[sc];
-                const float w1 = ex2_approx(clast - sm.c2[sc + 1]) * sm.dt[sc + 1];
+                const float w0 = ex2_approx(clast - c2[sc]) * dtv[sc];
+                const float w1 = ex2_approx(clast - c2[sc + 1]) * dtv[sc + 1];
                 uint32_t hi, lo;
                 split2(swz_ld(&sm.X[0][0], p, sc) * w0, swz_ld(&sm.X[0][0], p, sc + 1) * w1, hi, lo);
                 *reinterpret_cast<uint32_t*>(&sm.Oh[p][sc]) = hi;
@@ -361,10 +374,11 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             }
         }
         __syncthreads();  // Yt and the weighted x complete; x is consumed
-        if (tid == 0 && k + 1 < n) {
+        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
             fence_proxy_async_smem();
             issue(0, k + 1);
         }
+        if (warp == 0 && k + 1 < n) decay_prefix(k + 1);  // the next chunk's dt and decay, other buffer
         // y rows of the head's 64 channels, 8 steps per store
 #pragma unroll
         for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
@@ -398,7 +412,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
 #pragma unroll
             for (int jp = 0; jp < kNH / 2; ++jp)  // B = Bt^T from Bt[n][s]
-                ldsm_x4(swz(bt, n0 + 16 * jp + rr + ((mi >> 1) << 3), 2 * kb + (mi & 1)), bb[jp]);
+                ldsm_x4(b_row + jp * 16 * 128 + (((2 * kb + (mi & 1)) ^ sw) << 4), bb[jp]);
 #pragma unroll
             for (int jp = 0; jp < kNH / 2; ++jp) {
                 mma_bf16(S[2 * jp], ah, bb[jp][0], bb[jp][1]);
@@ -411,8 +425,12 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             }
         }
         store_state_parts();
-        __syncthreads();  // state parts complete for the next chunk; B is consumed
-        if (tid == 0 && k + 1 < n) {
+        // state parts and the next chunk's decay complete; B is consumed
+        if (__syncthreads_or(timed_out)) {
+            if (tid == 0) { report_device_error(a.err, -6); drain(); }
+            return;
+        }
+        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
             fence_proxy_async_smem();
             issue(1, k + 1);
         }

@@ -39,6 +39,12 @@ def main() -> int:
         for _ in range(args.launches):
             ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
                                d["softplus"], y=y, final_state=fs, zoh=w.zoh)
+    elif args.workload in syn.SSD_WORKLOADS:
+        w = syn.SSD_WORKLOADS[args.workload]
+        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in syn.ssd_workload_inputs(w).items()}
+        y = torch.empty_like(x["x"])
+        for _ in range(args.launches):
+            ops.mamba_ssd_fwd(x["x"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["delta_bias"], x["softplus"], y=y)
     else:
         w = syn.DECODE_WORKLOADS[args.workload]
         st = {k: v.to(dev) for k, v in syn.decode_static(w).items()}

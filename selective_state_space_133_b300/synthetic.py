@@ -126,6 +126,18 @@ class SsdWorkload:
         return self.batch * self.seqlen * self.nheads * self.headdim * self.dstate
 
     @property
+    def flops(self) -> int:
+        """Algorithmic FLOPs of the chunked form (64-step chunks) per call: per chunk of q
+        steps and head, C B^T and its masked product with x over the causal
+        triangle q(q+1)/2, the state update and C S^T over q x N x headdim."""
+        total = 0
+        for l0 in range(0, self.seqlen, 64):
+            q = min(64, self.seqlen - l0)
+            tri = q * (q + 1) // 2
+            total += 2 * (tri * (self.dstate + self.headdim) + 2 * q * self.dstate * self.headdim)
+        return total * self.batch * self.nheads
+
+    @property
     def io_bytes(self) -> int:
         """Unique bytes: x, delta, B, C read; y written (bf16)."""
         rows = 2 * self.batch * self.nheads * self.headdim * self.seqlen
