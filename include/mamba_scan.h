@@ -319,6 +319,26 @@ int mamba_ssd_fwd(const void* x, const void* delta, const float* A,
                   int io_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Single-token step of the SSD form (decode), in place on the state: for each
+ * batch row b, head h and channel p of the head,
+ *   dt = delta[b,h] + delta_bias[h];  softplus(dt) if flags & MAMBA_FLAG_SOFTPLUS
+ *   S[b,h,p,:] = exp(dt * A[h]) * S[b,h,p,:] + dt * x[b,h*64+p] * B[b,:]
+ *   y[b,h*64+p] = S[b,h,p,:] . C[b,:] + D[h] * x[b,h*64+p]
+ * (one step of mamba_ssd_fwd, so a sequence can be continued token by token
+ * from its final_state).
+ *   state   : (batch, nheads, headdim, dstate) fp32, read and overwritten, 16-byte aligned
+ *   x, y    : (batch, nheads * headdim) io_dtype;  delta : (batch, nheads) io_dtype
+ *   B, C    : (batch, dstate) io_dtype, 16-byte aligned
+ *   A       : (nheads) fp32;  D, delta_bias : (nheads) fp32 or NULL
+ * Supported: io_dtype MAMBA_F32 or MAMBA_BF16, headdim 64, dstate 64 or 128,
+ * flags MAMBA_FLAG_SOFTPLUS only. Returns MAMBA_OK or a negative mamba_status.
+ */
+int mamba_ssd_update(float* state, const void* x, const void* delta, const float* A,
+                     const void* B, const void* C, const float* D, const float* delta_bias,
+                     int flags, void* y, int batch, int nheads, int headdim, int dstate,
+                     int io_dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device error word.
  * Kernels that wait on their own asynchronous copies give up after a bounded
  * number of polls (far beyond any normal copy time), set this word and return

@@ -34,6 +34,7 @@ SIGNATURES = {
     "mamba_state_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P]),
     "mamba_ssd_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "mamba_ssd_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _Z, _P]),
+    "mamba_ssd_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "mamba_check_device_error": (_I, [_P]),
     "mamba_status_string": (ctypes.c_char_p, [_I]),
     "mamba_version": (_I, []),

@@ -173,6 +173,13 @@ void launch_update_n(const mscan::UpdateArgs& a, bool zoh, cudaStream_t stream) 
     else mscan::state_update_kernel<T, NS, false><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
 }
 
+template <typename T, int NS>
+void launch_ssd_update_n(const mscan::SsdUpdateArgs& a, cudaStream_t s) {
+    constexpr int rows = mscan::kUpdateThreads / (NS / 4);
+    const dim3 grid((a.nheads * a.headdim + rows - 1) / rows, a.batch);
+    mscan::ssd_update_kernel<T, NS><<<grid, mscan::kUpdateThreads, 0, s>>>(a);
+}
+
 template <typename T>
 int launch_update(const mscan::UpdateArgs& a, int dstate, bool zoh, cudaStream_t stream) {
     switch (dstate) {
@@ -567,6 +574,36 @@ int mamba_ssd_fwd(const void* x, const void* delta, const float* A, const void* 
     }
     return dstate == 64 ? mhost::launch_ssd_n<64>(a, x, B, C, w.pitch, s)
                         : mhost::launch_ssd_n<128>(a, x, B, C, w.pitch, s);
+}
+
+int mamba_ssd_update(float* state, const void* x, const void* delta, const float* A, const void* B, const void* C,
+                     const float* D, const float* delta_bias, int flags, void* y, int batch, int nheads, int headdim,
+                     int dstate, int io_dtype, void* stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (flags & ~MAMBA_FLAG_SOFTPLUS) return MAMBA_ERR_FLAGS;
+    if (batch < 0 || nheads < 0 || headdim != mscan::kSsdP || !ssd_dstate(dstate)) return MAMBA_ERR_SHAPE;
+    if (batch > 65535) return MAMBA_ERR_SHAPE;  // grid.y
+    if (static_cast<long long>(nheads) * headdim > (1ll << 30)) return MAMBA_ERR_SHAPE;
+    if (batch == 0 || nheads == 0) return MAMBA_OK;
+    if (!state || !x || !delta || !A || !B || !C || !y) return MAMBA_ERR_NULL;
+    const size_t es = dtype_size(io_dtype);
+    const void* p16[] = {state, B, C};
+    for (const void* p : p16)
+        if (!aligned(p, 16)) return MAMBA_ERR_ALIGN;
+    const void* pe[] = {x, delta, y};
+    for (const void* p : pe)
+        if (!aligned(p, es)) return MAMBA_ERR_ALIGN;
+    if (!aligned(A, 4) || (D && !aligned(D, 4)) || (delta_bias && !aligned(delta_bias, 4))) return MAMBA_ERR_ALIGN;
+    mscan::SsdUpdateArgs a;
+    a.state = state; a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.D = D; a.bias = delta_bias; a.y = y;
+    a.batch = batch; a.nheads = nheads; a.headdim = headdim; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (io_dtype == MAMBA_BF16) {
+        if (dstate == 64) launch_ssd_update_n<__nv_bfloat16, 64>(a, s); else launch_ssd_update_n<__nv_bfloat16, 128>(a, s);
+    } else {
+        if (dstate == 64) launch_ssd_update_n<float, 64>(a, s); else launch_ssd_update_n<float, 128>(a, s);
+    }
+    return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
 int mamba_check_device_error(void* stream) {

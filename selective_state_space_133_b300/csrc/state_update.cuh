@@ -121,4 +121,67 @@ __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const Upda
     }
 }
 
+// ---------------------------------------------------------------------------
+// Single-token step of the SSD (Mamba-2) form: per batch row b and head h the
+// state is a (headdim x N) matrix with one decay per step ("Mamba 论文精读"
+// §4.1: h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t; §5.2 the multi-head layer):
+//     dt = softplus(delta[b,h] + bias[h])   (or delta + bias)
+//     S[p,:] = exp(dt A[h]) S[p,:] + dt x[b,h*P+p] B[b,:]
+//     y[b,h*P+p] = S[p,:] . C[b,:] + D[h] x[b,h*P+p]
+// Bound by HBM like the scan's state update: each state row (4N bytes) is
+// read and written once. N/4 lanes share a row, 4 states each, and add their
+// partial C.S with xor-shuffles.
+
+struct SsdUpdateArgs {
+    float* state;        // (batch, nheads, headdim, N) fp32, in place
+    const void* x;       // (batch, nheads * headdim)
+    const void* delta;   // (batch, nheads)
+    const void* B;       // (batch, N)
+    const void* C;       // (batch, N)
+    const float* A;      // (nheads)
+    const float* D;      // (nheads) or null
+    const float* bias;   // (nheads) or null
+    void* y;             // (batch, nheads * headdim)
+    int batch, nheads, headdim;
+    int softplus;
+};
+
+template <typename T, int NS>
+__global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpdateArgs a) {
+    constexpr int kQ = NS / 4;                       // lanes per row (a power of two up to 32)
+    constexpr int kRows = kUpdateThreads / kQ;       // rows per block
+    const int b = blockIdx.y;
+    const int q = threadIdx.x % kQ;
+    const int dim = a.nheads * a.headdim;
+    const int d = blockIdx.x * kRows + threadIdx.x / kQ;
+    const int dc = d < dim ? d : dim - 1;            // padding lanes recompute the last row, store nothing
+    const int h = dc / a.headdim;
+    const size_t row = static_cast<size_t>(b) * dim + dc;
+    // all loads first
+    const float4 s4 = *reinterpret_cast<const float4*>(a.state + row * NS + 4 * q);
+    float2 B01, B23, C01, C23;
+    ldg4(static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q, B01, B23);
+    ldg4(static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q, C01, C23);
+    const float xv = Io<T>::to_f(static_cast<const T*>(a.x)[row]);
+    float dt = Io<T>::to_f(static_cast<const T*>(a.delta)[static_cast<size_t>(b) * a.nheads + h]) +
+               (a.bias ? a.bias[h] : 0.f);
+    if (a.softplus) dt = softplus_f(dt);
+    const float decay = ex2_approx(dt * a.A[h] * kLog2e);
+    const float2 ea = make_float2(decay, decay);
+    const float2 w = make_float2(dt * xv, dt * xv);
+    const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, B01));
+    const float2 h23 = __ffma2_rn(ea, make_float2(s4.z, s4.w), __fmul2_rn(w, B23));
+    const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
+    float yp = acc.x + acc.y;
+#pragma unroll
+    for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+    if (d < dim) {
+        *reinterpret_cast<float4*>(a.state + row * NS + 4 * q) = make_float4(h01.x, h01.y, h23.x, h23.y);
+        if (q == 0) {
+            const float yy = a.D ? fmaf(a.D[h], xv, yp) : yp;
+            static_cast<T*>(a.y)[row] = Io<T>::from_f(yy);
+        }
+    }
+}
+
 }  // namespace mscan

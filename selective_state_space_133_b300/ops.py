@@ -295,3 +295,34 @@ def mamba_ssd_fwd(x, delta, A, B, C, D=None, delta_bias=None, softplus=False, in
                            N, _lib.MAMBA_BF16, _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_ssd_fwd")
     return (y, final_state) if want_state else y
+
+
+def mamba_ssd_update(state, x, delta, A, B, C, D=None, delta_bias=None, softplus=False, y=None, stream=None):
+    """One decode step of the SSD form in place on ``state`` (see include/mamba_scan.h, mamba_ssd_update).
+
+    state: (batch, nheads, 64, N) fp32, N in {64, 128}; x: (batch, nheads * 64);
+    delta: (batch, nheads); B, C: (batch, N), all fp32 or all bf16; A, D,
+    delta_bias: (nheads,) fp32. Returns y (batch, nheads * 64).
+    """
+    if x.dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {x.dtype}")
+    dev = state.device
+    if dev.type != "cuda":
+        raise ValueError("mamba_ssd_update runs on CUDA tensors only")
+    batch, nheads, P, N = state.shape
+    _need(state, "state", torch.float32, (batch, nheads, P, N), dev)
+    _need(x, "x", x.dtype, (batch, nheads * P), dev)
+    _need(delta, "delta", x.dtype, (batch, nheads), dev)
+    _need(B, "B", x.dtype, (batch, N), dev)
+    _need(C, "C", x.dtype, (batch, N), dev)
+    _need(A, "A", torch.float32, (nheads,), dev)
+    _need(D, "D", torch.float32, (nheads,), dev)
+    _need(delta_bias, "delta_bias", torch.float32, (nheads,), dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", x.dtype, (batch, nheads * P), dev)
+    st = _lib.lib().mamba_ssd_update(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(delta_bias), _flags(softplus), _ptr(y), batch, nheads, P, N, _IO[x.dtype],
+                                     _stream_handle(stream, dev))
+    _lib.check(st, "mamba_ssd_update")
+    return y

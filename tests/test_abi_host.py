@@ -216,3 +216,26 @@ def test_ssd_workspace_size(L):
     assert w >= 2 * (2 * 4 * 64 + 2 * 2 * 128) * 104
     assert L.mamba_ssd_workspace_size(2, 4, 64, 100, 128, 0) == 0            # fp32 I/O is not supported
     assert L.mamba_ssd_workspace_size(2, 4, 32, 100, 128, 1) == 0
+
+
+def ssd_update(L, **kw):
+    args = dict(state=P, x=P, delta=P, A=P, B=P, C=P, D=None, bias=None, flags=1, y=P, batch=4, nheads=2, headdim=64,
+                dstate=128, dtype=1)
+    args.update(kw)
+    return L.mamba_ssd_update(args["state"], args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                              args["bias"], args["flags"], args["y"], args["batch"], args["nheads"], args["headdim"],
+                              args["dstate"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=3), -3), (dict(flags=2), -8), (dict(headdim=32), -2), (dict(dstate=16), -2), (dict(batch=-1), -2),
+    (dict(batch=70000), -2), (dict(state=None), -1), (dict(x=None), -1), (dict(delta=None), -1), (dict(C=None), -1),
+    (dict(y=None), -1), (dict(A=None), -1), (dict(state=P + 8), -4), (dict(B=P + 8), -4), (dict(x=P + 1), -4),
+    (dict(dtype=0, y=P + 2), -4), (dict(D=P + 2), -4),
+])
+def test_ssd_update_rejects(L, kw, code):
+    assert ssd_update(L, **kw) == code
+
+
+def test_ssd_update_empty_is_noop(L):
+    assert ssd_update(L, batch=0, state=None) == 0

@@ -145,3 +145,48 @@ def test_rejects_unsupported():
         ops.mamba_ssd_fwd(d["x"], d["delta"], d["A"], B32, B32)
     with pytest.raises(TypeError):
         ops.mamba_ssd_fwd(d["x"].float(), d["delta"], d["A"], d["B"], d["C"])
+
+
+def ssd_step_inputs(batch, nheads, N, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    cast = lambda t: t.to(dtype).contiguous()
+    return dict(state=(torch.randn(batch, nheads, 64, N, generator=g) * 0.2).contiguous(),
+                x=cast(torch.randn(batch, nheads * 64, generator=g)), delta=cast(torch.randn(batch, nheads, generator=g) * 0.5),
+                A=-(1.0 + 15.0 * torch.rand(nheads, generator=g)), B=cast(torch.randn(batch, N, generator=g)),
+                C=cast(torch.randn(batch, N, generator=g)), D=torch.randn(nheads, generator=g),
+                delta_bias=syn.inv_softplus(torch.full((nheads,), 0.01, dtype=torch.float64)).float())
+
+
+@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ssd_update_parity(N, dtype):
+    batch, nheads = 3, 5   # 15 (row, head) pairs of 64 channels
+    x = ssd_step_inputs(batch, nheads, N, dtype, seed=N + (1 if dtype == torch.float32 else 2))
+    st = x["state"].cuda()
+    y = ops.mamba_ssd_update(st, x["x"].cuda(), x["delta"].cuda(), x["A"].cuda(), x["B"].cuda(), x["C"].cuda(),
+                             x["D"].cuda(), x["delta_bias"].cuda(), True)
+    torch.cuda.synchronize()
+    yr, hr = oracle.ssd(x["x"][:, :, None], x["delta"][:, :, None], x["A"], x["B"][:, :, None], x["C"][:, :, None],
+                        x["D"], x["delta_bias"], True, h0=x["state"])
+    tol = TOL[str(dtype).replace("torch.", "")]
+    assert max_rel_err(y.double().cpu().numpy().reshape(-1), yr.reshape(-1)) <= tol
+    assert max_rel_err(st.double().cpu().numpy().reshape(-1, N), hr.reshape(-1, N)) <= TOL["float32"]
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_ssd_update_continues_forward(N):
+    # a chunked forward over L0 steps, then one decode step per further token
+    x = syn.ssd_inputs(2, 3, 80, N, seed=21)
+    L0 = 70
+    head = {k: (v[..., :L0].contiguous() if isinstance(v, torch.Tensor) and v.dim() == 3 else v) for k, v in x.items()}
+    _, h = gpu(head)
+    st = torch.from_numpy(h).float().cuda()
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    ys = []
+    for l in range(L0, 80):
+        ys.append(ops.mamba_ssd_update(st, d["x"][..., l].contiguous(), d["delta"][..., l].contiguous(), d["A"],
+                                       d["B"][..., l].contiguous(), d["C"][..., l].contiguous(), d["D"],
+                                       d["delta_bias"], True).double().cpu().numpy())
+    yr, hr = ref(x)
+    assert max_rel_err(np.stack(ys, axis=2).reshape(-1, 80 - L0), yr[..., L0:].reshape(-1, 80 - L0)) <= TOL_BF16
+    assert max_rel_err(st.double().cpu().numpy().reshape(-1, N), hr.reshape(-1, N)) <= TOL_BF16
