@@ -337,6 +337,18 @@ def oracle_update_rate(w, budget_s: float):
     import oracle
     from selective_state_space_133_b300 import synthetic as syn
     orc = oracle.default()
+    if isinstance(w, syn.SsdDecodeWorkload):  # one SSD step = the SSD form over one step from the state
+        st = syn.ssd_decode_static(w)
+        state = st["state"].double().numpy()
+        steps, elapsed = 0, 0.0
+        while elapsed < budget_s and steps < w.steps:
+            x = syn.ssd_decode_step(w, steps)
+            t0 = time.perf_counter()
+            _, state = orc.ssd(x["x"][:, :, None], x["delta"][:, :, None], st["A"], x["B"][:, :, None],
+                               x["C"][:, :, None], st["D"], st["delta_bias"], True, h0=state)
+            elapsed += time.perf_counter() - t0
+            steps += 1
+        return w.elements_per_step * steps / elapsed, steps, elapsed
     st = syn.decode_static(w)
     state = st["state"].double().numpy()
     steps, elapsed = 0, 0.0
@@ -360,10 +372,12 @@ def run_decode(args, w):
     ws, rank, local = dist_setup(want_nccl=True)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    st = {k: v.to(dev) for k, v in syn.decode_static(w).items()}
+    ssd = isinstance(w, syn.SsdDecodeWorkload)
+    st = {k: v.to(dev) for k, v in (syn.ssd_decode_static(w) if ssd else syn.decode_static(w)).items()}
     n_in = min(8, w.steps)
-    xs = [{k: v.to(dev) for k, v in syn.decode_step(w, i).items()} for i in range(n_in)]
-    y = torch.empty_like(xs[0]["u"])
+    xs = [{k: v.to(dev) for k, v in (syn.ssd_decode_step(w, i) if ssd else syn.decode_step(w, i)).items()}
+          for i in range(n_in)]
+    y = torch.empty_like(xs[0]["x" if ssd else "u"])
     stream = torch.cuda.current_stream(dev)
     # the state (84 MB) fits the 126 MB L2: before every timed update, read a
     # 512 MB buffer (untimed), which evicts it; reading leaves clean lines, so the
@@ -373,8 +387,12 @@ def run_decode(args, w):
 
     def step(i):
         x = xs[i % n_in]
-        ops.mamba_state_update(st["state"], x["u"], x["delta"], st["A"], x["B"], x["C"], st["D"], x["z"],
-                               st["delta_bias"], True, y=y, stream=stream)
+        if ssd:
+            ops.mamba_ssd_update(st["state"], x["x"], x["delta"], st["A"], x["B"], x["C"], st["D"], st["delta_bias"],
+                                 True, y=y, stream=stream)
+        else:
+            ops.mamba_state_update(st["state"], x["u"], x["delta"], st["A"], x["B"], x["C"], st["D"], x["z"],
+                                   st["delta_bias"], True, y=y, stream=stream)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -434,12 +452,15 @@ def run_decode(args, w):
     peak, peak_kind = hbm_peak()
     achieved = w.io_bytes_per_step / (ms * 1e-3) / 1e9
     cpu_v, cpu_steps, cpu_t = oracle_update_rate(w, float(os.environ.get("BENCH_CPU_BASELINE_S", "10")))
+    shape = ({"batch": w.batch, "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate} if ssd else
+             {"batch": w.batch, "dim": w.dim, "dstate": 16})
     line = {
-        "metric": "state-update elems/s (B·D·N per token) & achieved HBM GB/s vs roofline, 1×B300",
+        "metric": ("SSD decode" if ssd else "state-update") +
+                  " elems/s (B·D·N per token) & achieved HBM GB/s vs roofline, 1×B300",
         "value": value, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": 16, "state_dtype": "fp32",
-                   "parallelism": f"replicas x{ws}", "l2": "evicted by a 512 MB read before every timed step"},
+        "config": dict({"workload": w.name}, **shape, state_dtype="fp32", parallelism=f"replicas x{ws}",
+                       l2="evicted by a 512 MB read before every timed step"),
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "peak_source": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes_per_step},
@@ -786,10 +807,10 @@ def main():
         if args.impl == "reference":
             raise SystemExit("--impl reference times the scan workload only")
         return run_ssd(args, syn.SSD_WORKLOADS[args.workload])
-    if args.workload in syn.DECODE_WORKLOADS:
+    if args.workload in syn.DECODE_WORKLOADS or args.workload in syn.SSD_DECODE_WORKLOADS:
         if args.impl == "reference":
             raise SystemExit("--impl reference times the scan workload only")
-        return run_decode(args, syn.DECODE_WORKLOADS[args.workload])
+        return run_decode(args, syn.DECODE_WORKLOADS.get(args.workload) or syn.SSD_DECODE_WORKLOADS[args.workload])
     w = syn.SCAN_WORKLOADS.get(args.workload) or syn.VARIANT_WORKLOADS[args.workload]
     if args.pass_ in ("bwd", "conv"):
         if args.impl == "reference":

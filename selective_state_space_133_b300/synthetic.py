@@ -153,6 +153,58 @@ SSD_WORKLOADS: Dict[str, SsdWorkload] = {w.name: w for w in [
 ]}
 
 
+@dataclass(frozen=True)
+class SsdDecodeWorkload:
+    """One decode token of the SSD layer for `batch` sequences at once."""
+    name: str
+    batch: int
+    nheads: int
+    dstate: int
+    steps: int
+    dtype: torch.dtype
+    state_std: float
+    seed: int
+    headdim: int = 64
+
+    @property
+    def elements_per_step(self) -> int:
+        return self.batch * self.nheads * self.headdim * self.dstate
+
+    @property
+    def io_bytes_per_step(self) -> int:
+        es = torch.finfo(self.dtype).bits // 8
+        state = 2 * 4 * self.elements_per_step                       # fp32 state read + written
+        rows = 2 * es * self.batch * self.nheads * self.headdim       # x read, y written
+        return state + rows + es * self.batch * self.nheads + 2 * es * self.batch * self.dstate
+
+
+SSD_DECODE_WORKLOADS: Dict[str, SsdDecodeWorkload] = {w.name: w for w in [
+    SsdDecodeWorkload("ssd_decode_b64_h64_n128_bf16", 64, 64, 128, 1024, torch.bfloat16, 0.1, 11),
+]}
+
+
+def ssd_decode_static(w: SsdDecodeWorkload) -> Dict[str, torch.Tensor]:
+    """Per-run tensors of the SSD decode workload: initial state, A, D, delta_bias (draw order as listed)."""
+    g = torch.Generator().manual_seed(w.seed)
+    dt = _dt_init(g, w.nheads)
+    A = -(1.0 + 15.0 * torch.rand(w.nheads, generator=g))
+    D = torch.randn(w.nheads, generator=g)
+    state = torch.randn(w.batch, w.nheads, w.headdim, w.dstate, generator=g) * w.state_std
+    return dict(state=state.contiguous(), A=A.float().contiguous(), D=D.contiguous(),
+                delta_bias=inv_softplus(dt).float())
+
+
+def ssd_decode_step(w: SsdDecodeWorkload, step: int) -> Dict[str, torch.Tensor]:
+    """Per-token tensors of step ``step`` (own seed per step: seed*1_000_003 + step)."""
+    g = torch.Generator().manual_seed(w.seed * 1_000_003 + step)
+    x = torch.randn(w.batch, w.nheads * w.headdim, generator=g)
+    delta = torch.randn(w.batch, w.nheads, generator=g) * 0.5
+    B = torch.randn(w.batch, w.dstate, generator=g)
+    C = torch.randn(w.batch, w.dstate, generator=g)
+    cast = (lambda t: t.to(w.dtype).contiguous())
+    return dict(x=cast(x), delta=cast(delta), B=cast(B), C=cast(C))
+
+
 def ssd_inputs(batch: int, nheads: int, seqlen: int, dstate: int = 128, *, headdim: int = 64, seed: int = 0,
                with_D: bool = True, softplus_in_kernel: bool = True) -> Dict[str, Optional[torch.Tensor]]:
     """CPU tensors for one SSD call: x, delta, A, B, C, D, delta_bias, softplus.
