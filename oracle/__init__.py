@@ -145,10 +145,10 @@ class Oracle:
 
     # -- gradients ------------------------------------------------------------
     def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                 dy=None, h0=None):
+                 dy=None, h0=None, zoh=False):
         """Gradients of L = sum(dy * y) for the scan of all rows.
 
-        Same inputs as ``scan`` plus dy (batch, dim, L). Returns a dict of float64
+        Same inputs as ``scan`` (zoh included) plus dy (batch, dim, L). Returns a dict of float64
         arrays: du, ddelta (batch, dim, L); dz (batch, dim, L) or None; dA (dim, N);
         dB, dC (batch, N, L); dD, ddelta_bias (dim,) or None; dh0 (batch, dim, N).
         The C code returns per-row contributions; here they are summed over the
@@ -175,7 +175,7 @@ class Oracle:
         dA = np.empty((R, N)); dD = np.empty(R); db = np.empty(R)
         dB = np.empty((R, N, L)); dC = np.empty((R, N, L)); dh0 = np.empty((R, N))
         rc = self.lib.oracle_scan_bwd(R, L, N, _ptr(ur), _ptr(dr), _ptr(zr), _ptr(Ar), _ptr(Dr), _ptr(br),
-                                      _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0), _flags(softplus),
+                                      _ptr(Bf), _ptr(Cf), _iptr(b_idx), _ptr(hr0), _flags(softplus, zoh),
                                       _ptr(gy), _ptr(du), _ptr(dd), _ptr(dz), _ptr(dA), _ptr(dD), _ptr(db),
                                       _ptr(dB), _ptr(dC), _ptr(dh0))
         if rc != 0:

@@ -66,6 +66,17 @@ static double zoh_gain(double dt, double a)
     return x == 0.0 ? dt : expm1(x) / a;
 }
 
+/* Its derivative with respect to a: (dt e^{dt a} - gain) / a, which cancels
+ * for small dt*a; there its series dt^2 (1/2 + x/3 + x^2/8 + x^3/30), x = dt a
+ * (the next term, x^4/144, is below 1e-18 of the first for |x| < 1e-4). The
+ * derivative with respect to dt is e^{dt a}. */
+static double zoh_gain_da(double dt, double a)
+{
+    double x = dt * a;
+    if (fabs(x) < 1e-4) return dt * dt * (0.5 + x * (1.0 / 3.0 + x * (1.0 / 8.0 + x / 30.0)));
+    return (dt * exp(x) - expm1(x) / a) / a;
+}
+
 /* One time step of the selective SSM for one row.
  * h[dstate] in/out; A_row[dstate]; Bt, Ct: the step's B and C, read with
  * stride bc_stride (seqlen for the scan layout (batch, dstate, seqlen), 1 for
@@ -172,6 +183,9 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
  *   dt        : ddelta = d(dt) * sigmoid(delta + bias) with softplus, else d(dt);
  *               dbias += ddelta
  *   dh0 = g after step 0.
+ * With ORACLE_ZOH the input term is gain(dt, A[n]) u B[n] instead of dt u B[n]:
+ *               dB[n][l] = gh[n] gain u;  du += gh[n] B[n] gain;
+ *               d(dt) += gh[n] B[n] u e;  dA[n] += gh[n] B[n] u dgain/dA.
  * Outputs per row (the caller sums dA/dD/dbias over batch rows and dB/dC over
  * the channels of a batch row):
  *   du, ddelta, dz : (nrows, seqlen)          dz written only if z given
@@ -179,9 +193,8 @@ int oracle_state_update(int64_t nrows, int64_t dstate, double* state,
  *   dD, dbias      : (nrows), either may be NULL
  *   dB, dC         : (nrows, dstate, seqlen)
  *   dh0            : (nrows, dstate), may be NULL
- * h0 as in oracle_scan; flags as in the forward, where only ORACLE_SOFTPLUS
- * is differentiated here. Returns 0, -1 if dstate is out of range, -2 if the
- * work buffer cannot be allocated, -3 if flags asks for the ZOH input gain.
+ * h0 and flags as in oracle_scan. Returns 0, -1 if dstate is out of range,
+ * -2 if the work buffer cannot be allocated.
  */
 int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
                     const double* u, const double* delta, const double* z,
@@ -192,8 +205,8 @@ int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
                     double* dD, double* dbias, double* dB, double* dC, double* dh0)
 {
     const int softplus_flag = flags & ORACLE_SOFTPLUS;
+    const int zoh = flags & ORACLE_ZOH;
     if (dstate < 1 || dstate > 1024) return -1;
-    if (flags & ORACLE_ZOH) return -3;
     /* H[(l + 1) * dstate + n] = state after step l; H[n] = state before step 0 */
     double* H = (double*)malloc(sizeof(double) * (size_t)(seqlen + 1) * (size_t)dstate);
     if (!H) return -2;
@@ -209,8 +222,10 @@ int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
             const int64_t i = r * seqlen + l;
             double dt = delta[i] + (bias ? bias[r] : 0.0);
             if (softplus_flag) dt = softplus_ref(dt);
-            for (int64_t n = 0; n < dstate; ++n)
-                H[(l + 1) * dstate + n] = exp(dt * Ar[n]) * H[l * dstate + n] + dt * Bb[n * seqlen + l] * u[i];
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double gain = zoh ? zoh_gain(dt, Ar[n]) : dt;
+                H[(l + 1) * dstate + n] = exp(dt * Ar[n]) * H[l * dstate + n] + gain * Bb[n * seqlen + l] * u[i];
+            }
         }
         /* reverse */
         for (int64_t n = 0; n < dstate; ++n) { g[n] = 0.0; dA[r * dstate + n] = 0.0; }
@@ -236,8 +251,17 @@ int oracle_scan_bwd(int64_t nrows, int64_t seqlen, int64_t dstate,
                 const double e = exp(dt * Ar[n]);
                 const double gh = g[n] + dp * Cb[n * seqlen + l];
                 dC[(r * dstate + n) * seqlen + l] = dp * hl[n];
-                dB[(r * dstate + n) * seqlen + l] = gh * dt * u[i];
-                ddtu += gh * Bb[n * seqlen + l];
+                if (zoh) {
+                    const double gain = zoh_gain(dt, Ar[n]);
+                    const double ghbu = gh * Bb[n * seqlen + l] * u[i];
+                    dB[(r * dstate + n) * seqlen + l] = gh * gain * u[i];
+                    dui += gh * Bb[n * seqlen + l] * gain;
+                    ddt += ghbu * e;
+                    dA[r * dstate + n] += ghbu * zoh_gain_da(dt, Ar[n]);
+                } else {
+                    dB[(r * dstate + n) * seqlen + l] = gh * dt * u[i];
+                    ddtu += gh * Bb[n * seqlen + l];
+                }
                 const double de = gh * hp[n];
                 ddt += de * e * Ar[n];
                 dA[r * dstate + n] += de * e * dt;

@@ -19,7 +19,7 @@ from oracle_pins import rand_problem
 
 def _fwd(orc, p, h0=None):
     y, h = orc.scan(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
-                    p["softplus"], h0=h0)
+                    p["softplus"], h0=h0, zoh=p.get("zoh", False))
     return y.reshape(p["u"].shape), h
 
 
@@ -53,7 +53,7 @@ def _fd_check(orc, p, h0, seed, per_tensor=5, rtol=1e-6):
     rng = np.random.default_rng(seed)
     dy = rng.standard_normal(p["u"].shape)
     g = orc.scan_bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
-                     p["softplus"], dy=dy, h0=h0)
+                     p["softplus"], dy=dy, h0=h0, zoh=p.get("zoh", False))
     inputs = dict(p)
     inputs["h0"] = h0
     names = {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
@@ -65,7 +65,9 @@ def _fd_check(orc, p, h0, seed, per_tensor=5, rtol=1e-6):
 
     for name, gname in names.items():
         x = inputs[name]
-        if x is None:
+        if x is None or not isinstance(x, np.ndarray):
+            if x is not None:
+                continue
             if name != "h0":  # a zero initial state still has a gradient; absent tensors have none
                 assert g.get(gname) is None, f"{gname} returned for a missing input"
             continue
@@ -94,5 +96,15 @@ def check_bwd_finite_differences_plain(orc):
     _fd_check(orc, p, None, 44)
 
 
+def check_bwd_finite_differences_zoh(orc):
+    # the exact zero-order-hold gain: A with negative, tiny (series branch of
+    # d gain / dA), zero and positive entries; the forward is pinned on its own
+    p = rand_problem(45, 2, 2, 9, 4)
+    p["A"] = np.array([[-2.0, -3e-6, 0.0, 0.4], [-0.2, -7.0, 1e-5, -1.0]])
+    p["zoh"] = True
+    h0 = np.random.default_rng(45).standard_normal((2, 2, 4)) * 0.3
+    _fd_check(orc, p, h0, 45, per_tensor=6)
+
+
 ALL_CHECKS = [check_h0_decay_closed_form, check_h0_split, check_bwd_finite_differences,
-              check_bwd_finite_differences_plain]
+              check_bwd_finite_differences_plain, check_bwd_finite_differences_zoh]

@@ -15,6 +15,9 @@ The oracle's ``zoh=True`` evaluates that B_bar per diagonal state. Pins:
   bit for bit;
 * a decode step with the ZOH gain continues a ZOH scan exactly.
 
+(The gradients of the ZOH gain are pinned by finite differences in
+``oracle_pins_bwd``.)
+
 Planted mistakes in copies of the C code must each fail one of these.
 """
 import numpy as np
@@ -121,24 +124,18 @@ def test_zoh_differs_from_simplified_gain():
     assert not np.allclose(y0, y1, rtol=1e-6, atol=0.0)
 
 
-def test_backward_rejects_zoh():
-    p = _problem(66, 5)
-    lib = oracle.default().lib
-    # the C entry point refuses the ZOH flag (its gradient is not written out)
-    import ctypes
-    P = ctypes.POINTER(ctypes.c_double)
-    R, L, N = 1, 5, 4
-    buf = lambda n: np.zeros(n)
-    u, dl, dy = buf(L), buf(L) + 0.1, buf(L)
-    A = p["A"][0].copy()
-    B, C = buf(N * L), buf(N * L)
-    outs = [buf(L), buf(L), None, buf(N), buf(1), buf(1), buf(N * L), buf(N * L), buf(N)]
-    ptr = lambda a: None if a is None else a.ctypes.data_as(P)
-    bidx = np.zeros(1, np.int64)
-    rc = lib.oracle_scan_bwd(R, L, N, ptr(u), ptr(dl), None, ptr(A), None, None, ptr(B), ptr(C),
-                             bidx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), None, oracle.ZOH, ptr(dy),
-                             *[ptr(o) for o in outs])
-    assert rc == -3
+def test_backward_a_zero_limit():
+    # at A = 0 the ZOH gain is dt: the forward, and every gradient but dA
+    # (which gains the gain's own derivative, dt^2 / 2 at A = 0), agree with
+    # the simplified gain's
+    p = rand_problem(66, 2, 3, 13, 4, a_zero=True)
+    dy = np.random.default_rng(66).standard_normal(p["u"].shape)
+    args = (p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"], p["softplus"])
+    g0 = oracle.scan_bwd(*args, dy=dy)
+    g1 = oracle.scan_bwd(*args, dy=dy, zoh=True)
+    for k in ("du", "ddelta", "dz", "dB", "dC", "dD", "ddelta_bias", "dh0"):
+        np.testing.assert_allclose(g1[k], g0[k], rtol=1e-12, atol=1e-12, err_msg=k)
+    assert not np.allclose(g1["dA"], g0["dA"], rtol=1e-6, atol=0.0)
 
 
 MUTANTS = {
