@@ -476,8 +476,6 @@ def run_decode(args, w):
 
 def run_bwd(args, w):
     """One step = one mamba_scan_bwd call (all gradients) on the workload, inputs resident in HBM."""
-    if w.dstate != 16 or w.zoh:
-        raise SystemExit("the backward is built for 16 states and the dt * B gain")
     import torch
     from selective_state_space_133_b300 import ops
     from selective_state_space_133_b300 import synthetic as syn
@@ -486,24 +484,25 @@ def run_bwd(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     x = syn.scan_inputs(w.batch, w.dim, w.seqlen, w.dtype, seed=w.seed + 7919 * rank, with_D=w.with_D,
-                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise)
+                        with_z=w.with_z, softplus_in_kernel=w.softplus_in_kernel, a_noise=w.a_noise,
+                        dstate=w.dstate)
     dy = torch.randn(w.batch, w.dim, w.seqlen, generator=torch.Generator().manual_seed(w.seed + 1)).to(w.dtype)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     dyd = dy.to(dev)
-    work = torch.empty(max(1, int(ops._lib.lib().mamba_scan_bwd_workspace_size(w.batch, w.dim, w.seqlen, 16,
+    work = torch.empty(max(1, int(ops._lib.lib().mamba_scan_bwd_workspace_size(w.batch, w.dim, w.seqlen, w.dstate,
                                                                               ops._IO[w.dtype]))),
                        dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     # training: the forward stores the state before every 16-step chunk, the backward starts from them
-    ck = torch.empty(w.batch, w.dim, (w.seqlen + 15) // 16, 16, device=dev)
+    ck = torch.empty(w.batch, w.dim, (w.seqlen + 15) // 16, w.dstate, device=dev)
     ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], d["softplus"],
-                       chunk_states=ck, stream=stream)
+                       chunk_states=ck, stream=stream, zoh=w.zoh)
     use_ck = [True]
 
     def step():
         return ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dyd, d["D"], d["z"], d["delta_bias"],
                                   d["softplus"], stream=stream, workspace=work,
-                                  chunk_states=ck if use_ck[0] else None)
+                                  chunk_states=ck if use_ck[0] else None, zoh=w.zoh)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -544,7 +543,7 @@ def run_bwd(args, w):
     es = torch.finfo(w.dtype).bits // 8
     rows = w.batch * w.dim * w.seqlen
     # algorithmic bytes: u, delta, z, dy read; du, ddelta, dz written; B, C read; dB, dC written
-    io = es * (rows * (4 + 3 if w.with_z else 3 + 2) + 4 * w.batch * 16 * w.seqlen)
+    io = es * (rows * (4 + 3 if w.with_z else 3 + 2) + 4 * w.batch * w.dstate * w.seqlen)
     props = torch.cuda.get_device_properties(dev)
     sm_max = (clocks or {}).get("sm_max_mhz") or 2032.0
     # given the forward's chunk states the backward computes 2 ex2 per element
@@ -561,9 +560,10 @@ def run_bwd(args, w):
         t0 = time.perf_counter()
         oracle.scan_bwd(sl(x["u"]), sl(x["delta"]), x["A"][:nch], sb(x["B"]), sb(x["C"]),
                         None if x["D"] is None else x["D"][:nch], sl(x["z"]),
-                        None if x["delta_bias"] is None else x["delta_bias"][:nch], x["softplus"], dy=sl(dy))
+                        None if x["delta_bias"] is None else x["delta_bias"][:nch], x["softplus"], dy=sl(dy),
+                        zoh=w.zoh)
         t_cpu = time.perf_counter() - t0
-        el = nch * w.seqlen * 16
+        el = nch * w.seqlen * w.dstate
         nch *= 2
     line = {
         "metric": "selective-scan backward elems/s (B·L·D·N, all gradients), 1×B300",

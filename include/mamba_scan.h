@@ -39,8 +39,8 @@
  *     For the state update, u/delta/z/y are (batch, dim) and B/C are (batch, dstate).
  *   - u, delta, z, B, C and y share io_dtype (fp32 or bf16). A, D, delta_bias and
  *     the state are always fp32; the recurrence and all accumulation are fp32.
- *   - dstate must be 8, 16, 32 or 64 (the backward: 16); anything else is
- *     MAMBA_ERR_SHAPE.
+ *   - dstate must be 8, 16, 32 or 64 for the selective scan (forward,
+ *     backward, state update); anything else is MAMBA_ERR_SHAPE.
  *   - `flags` is a bit set of mamba_flag values; 0 and 1 keep the meaning of a
  *     plain softplus switch. An unknown bit, or a bit an entry point does not
  *     support, is MAMBA_ERR_FLAGS.
@@ -79,8 +79,8 @@ typedef enum {
 
 typedef enum {
     MAMBA_FLAG_SOFTPLUS = 1,  /* dt = softplus(delta + bias) instead of delta + bias */
-    MAMBA_FLAG_ZOH = 2        /* exact zero-order-hold input gain instead of dt * B (forward entry
-                                 points and the state update) */
+    MAMBA_FLAG_ZOH = 2        /* exact zero-order-hold input gain instead of dt * B (every selective-scan
+                                 entry point; not the SSD form) */
 } mamba_flag;
 
 /*
@@ -182,9 +182,10 @@ int mamba_conv_scan_fwd_ws(const void* x, const float* conv_weight, const float*
 /*
  * Bytes of device workspace mamba_scan_bwd needs for these sizes (0 when there
  * is nothing to compute or an argument is out of range): the packed fp32 B/C
- * rows (batch * roundup(seqlen, 16) * 128 bytes), one fp32 state per row per
- * 16 steps (batch * dim * roundup(seqlen, 16) * 4 bytes) and fp32 sums of dB
- * and dC (batch * roundup(seqlen, 16) * 128 bytes).
+ * rows (batch * roundup(seqlen, 16) * 8 * dstate bytes), one fp32 state per
+ * row per 16 steps (batch * dim * roundup(seqlen, 16) / 16 * 4 * dstate bytes)
+ * and fp32 sums of dB and dC (batch * roundup(seqlen, 16) * 8 * dstate bytes),
+ * each rounded up to 256 bytes.
  */
 size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype);
 
@@ -194,8 +195,9 @@ size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate,
  * with respect to every input. The states are recomputed from the inputs, as
  * "mamba->jamba" (blog.csdn.net) §2.3 describes for the backward pass, keeping
  * one fp32 state per row every 16 steps in the workspace in between.
- * dstate must be 16 (MAMBA_ERR_SHAPE otherwise) and MAMBA_FLAG_SOFTPLUS is the
- * only flag (the gradient of the ZOH gain is not implemented: MAMBA_ERR_FLAGS).
+ * Takes the same dstate values and flags as the forward (with MAMBA_FLAG_ZOH
+ * the exact gain is differentiated, d gain / d dt = exp(dt A) and
+ * d gain / dA = (dt exp(dt A) - gain) / A, its series near dt A = 0).
  * Inputs: as mamba_scan_fwd_ws (u, delta, A, B, C, D, z, delta_bias, flags,
  * initial_state), plus
  *   chunk_states    : the forward's chunk_states output for these same inputs,

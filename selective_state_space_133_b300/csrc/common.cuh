@@ -12,7 +12,6 @@
 
 namespace mscan {
 
-constexpr int kDState = 16;  // the state size of the backward kernel
 
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -3,7 +3,8 @@
 // The forward-scan kernels are instantiated per state size in their own files
 // (scan_fwd_n8.cu ... scan_fwd_n64.cu, compiled in parallel); each of those
 // files defines launch_scan_n for its state size and instantiates no other
-// kernel; ssd_fwd.cu does the same for the SSD kernels (launch_ssd_n).
+// kernel; scan_bwd_n*.cu do the same for the backward (launch_bwd_n) and
+// ssd_fwd.cu for the SSD kernels (launch_ssd_n).
 // Everything else (argument checks, workspace layout, the B/C pack, the row
 // copies, the backward and the state update) lives in mamba_scan.cu.
 #pragma once
@@ -13,6 +14,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "scan_bwd.cuh"
 #include "scan_fwd.cuh"
 #include "ssd_fwd.cuh"
 
@@ -45,6 +47,11 @@ struct FwdInputs {
 // convolution and z are given). Returns a mamba_status.
 template <typename T, int NS>
 int launch_scan_n(const mscan::ScanArgs& a, const FwdInputs& in, int flags, cudaStream_t stream);
+
+// Launches the backward kernel of state size NS picked by `flags` and by
+// whether z is given (defined in bwd_launch.cuh). Returns a mamba_status.
+template <typename T, int NS>
+int launch_bwd_n(const mscan::ScanBwdArgs& a, int flags, cudaStream_t stream);
 
 // Launches the SSD kernel of state size NS (64 or 128) on x, B and C at row
 // pitch `pitch` elements (defined in ssd_fwd.cu). Returns a mamba_status.

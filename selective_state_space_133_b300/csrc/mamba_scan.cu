@@ -24,7 +24,6 @@ namespace {
 
 using mhost::aligned;
 using mhost::round_up;
-using mscan::kDState;
 
 constexpr int kKnownFlags = MAMBA_FLAG_SOFTPLUS | MAMBA_FLAG_ZOH;
 
@@ -198,26 +197,26 @@ struct BwdWorkspace {
     size_t bc, hck, dbc, total;
 };
 
-BwdWorkspace bwd_workspace(long long batch, long long dim, long long L) {
+BwdWorkspace bwd_workspace(long long batch, long long dim, long long L, int dstate) {
     BwdWorkspace w;
     w.Lp = static_cast<int>(round_up(static_cast<size_t>(L), mscan::kBwdTL));
     w.n = w.Lp / mscan::kBwdTL;
     w.bc = 0;
-    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * 32 * sizeof(float), 256);
+    size_t off = round_up(static_cast<size_t>(batch) * w.Lp * 2 * dstate * sizeof(float), 256);
     w.hck = off;
-    off += round_up(static_cast<size_t>(batch) * dim * w.n * kDState * sizeof(float), 256);
+    off += round_up(static_cast<size_t>(batch) * dim * w.n * dstate * sizeof(float), 256);
     w.dbc = off;
-    off += round_up(static_cast<size_t>(batch) * 2 * kDState * w.Lp * sizeof(float), 256);
+    off += round_up(static_cast<size_t>(batch) * 2 * dstate * w.Lp * sizeof(float), 256);
     w.total = L > 0 ? off : 0;
     return w;
 }
 
 template <typename T>
-int launch_bwd(mscan::ScanBwdArgs a, const void* B, const void* C, void* dB, void* dC, char* ws,
-               cudaStream_t stream) {
-    const BwdWorkspace w = bwd_workspace(a.batch, a.dim, a.seqlen);
+int launch_bwd(mscan::ScanBwdArgs a, int flags, int dstate, const void* B, const void* C, void* dB, void* dC,
+               char* ws, cudaStream_t stream) {
+    const BwdWorkspace w = bwd_workspace(a.batch, a.dim, a.seqlen, dstate);
     a.Lp = w.Lp;
-    if (cudaMemsetAsync(a.dA, 0, static_cast<size_t>(a.dim) * kDState * sizeof(float), stream) != cudaSuccess)
+    if (cudaMemsetAsync(a.dA, 0, static_cast<size_t>(a.dim) * dstate * sizeof(float), stream) != cudaSuccess)
         return MAMBA_ERR_CUDA;
     if (a.dD && cudaMemsetAsync(a.dD, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
     if (a.dbias && cudaMemsetAsync(a.dbias, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
@@ -225,25 +224,30 @@ int launch_bwd(mscan::ScanBwdArgs a, const void* B, const void* C, void* dB, voi
         a.bc = reinterpret_cast<const float*>(ws + w.bc);
         if (!a.have_hck) a.hck = reinterpret_cast<float*>(ws + w.hck);
         a.dbc = reinterpret_cast<float*>(ws + w.dbc);
-        if (cudaMemsetAsync(a.dbc, 0, static_cast<size_t>(a.batch) * 2 * kDState * w.Lp * sizeof(float), stream) !=
+        if (cudaMemsetAsync(a.dbc, 0, static_cast<size_t>(a.batch) * 2 * dstate * w.Lp * sizeof(float), stream) !=
             cudaSuccess)
             return MAMBA_ERR_CUDA;
-        launch_pack<T, kDState>(B, C, const_cast<float*>(a.bc), a.batch, a.seqlen, w.Lp, stream);
+        float* bc = const_cast<float*>(a.bc);
+        switch (dstate) {
+            case 8: launch_pack<T, 8>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            case 16: launch_pack<T, 16>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            case 32: launch_pack<T, 32>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            default: launch_pack<T, 64>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+        }
     }
-    const dim3 grid((a.dim + mscan::kBwdCh - 1) / mscan::kBwdCh, a.batch);
-    const bool z = a.z != nullptr;
-    if (a.softplus) {
-        if (z) mscan::scan_bwd_kernel<T, true, true><<<grid, 32, 0, stream>>>(a);
-        else   mscan::scan_bwd_kernel<T, true, false><<<grid, 32, 0, stream>>>(a);
-    } else {
-        if (z) mscan::scan_bwd_kernel<T, false, true><<<grid, 32, 0, stream>>>(a);
-        else   mscan::scan_bwd_kernel<T, false, false><<<grid, 32, 0, stream>>>(a);
+    int st;
+    switch (dstate) {
+        case 8: st = mhost::launch_bwd_n<T, 8>(a, flags, stream); break;
+        case 16: st = mhost::launch_bwd_n<T, 16>(a, flags, stream); break;
+        case 32: st = mhost::launch_bwd_n<T, 32>(a, flags, stream); break;
+        default: st = mhost::launch_bwd_n<T, 64>(a, flags, stream); break;
     }
+    if (st != MAMBA_OK) return st;
     if (a.seqlen > 0) {
-        const long long total = static_cast<long long>(a.batch) * 2 * kDState * a.seqlen;
+        const long long total = static_cast<long long>(a.batch) * 2 * dstate * a.seqlen;
         const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 148ll * 32));
         mscan::dbc_unpack_kernel<T><<<blocks, 256, 0, stream>>>(a.dbc, static_cast<T*>(dB), static_cast<T*>(dC),
-                                                               a.batch, a.seqlen, w.Lp);
+                                                               a.batch, dstate, a.seqlen, w.Lp);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
@@ -417,9 +421,9 @@ extern "C" int mamba_scan_fwd_noalloc(const void* u, const void* delta, const fl
 extern "C" {
 
 size_t mamba_scan_bwd_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype) {
-    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate != kDState) return 0;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || !forward_dstate(dstate)) return 0;
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return 0;
-    return bwd_workspace(batch, dim, seqlen).total;
+    return bwd_workspace(batch, dim, seqlen, dstate).total;
 }
 
 int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -430,8 +434,6 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     int st = check_scan_args(u, delta, A, B, C, D, z, delta_bias, flags, dy, nullptr, batch, dim, seqlen, dstate, io_dtype,
                              initial_state);
     if (st != MAMBA_OK) return st;
-    if (dstate != kDState) return MAMBA_ERR_SHAPE;
-    if (flags & MAMBA_FLAG_ZOH) return MAMBA_ERR_FLAGS;
     if (batch == 0 || dim == 0) return MAMBA_OK;
     if (!dA) return MAMBA_ERR_NULL;
     if (seqlen > 0 && (!du || !ddelta || !dB || !dC)) return MAMBA_ERR_NULL;
@@ -441,7 +443,7 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     for (const void* p : p16)
         if (p && !aligned(p, 16)) return MAMBA_ERR_ALIGN;
     if ((dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4))) return MAMBA_ERR_ALIGN;
-    const size_t need = bwd_workspace(batch, dim, seqlen).total;
+    const size_t need = bwd_workspace(batch, dim, seqlen, dstate).total;
     if (need > 0) {
         if (!workspace) return MAMBA_ERR_NULL;
         if (workspace_bytes < need) return MAMBA_ERR_WORKSPACE;
@@ -454,11 +456,11 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A, const void*
     a.dh0 = dinitial_state;
     a.hck = const_cast<float*>(chunk_states);  // read only when given
     a.have_hck = chunk_states != nullptr;
-    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen;
     char* ws = static_cast<char*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return io_dtype == MAMBA_BF16 ? launch_bwd<__nv_bfloat16>(a, B, C, dB, dC, ws, s)
-                                  : launch_bwd<float>(a, B, C, dB, dC, ws, s);
+    return io_dtype == MAMBA_BF16 ? launch_bwd<__nv_bfloat16>(a, flags, dstate, B, C, dB, dC, ws, s)
+                                  : launch_bwd<float>(a, flags, dstate, B, C, dB, dC, ws, s);
 }
 
 int mamba_state_update(float* state, const void* u, const void* delta, const float* A, const void* B, const void* C,
@@ -622,7 +624,7 @@ const char* mamba_status_string(int status) {
     switch (status) {
         case MAMBA_OK: return "MAMBA_OK";
         case MAMBA_ERR_NULL: return "MAMBA_ERR_NULL: a required pointer is NULL";
-        case MAMBA_ERR_SHAPE: return "MAMBA_ERR_SHAPE: unsupported or out-of-range size (dstate 8/16/32/64; backward 16)";
+        case MAMBA_ERR_SHAPE: return "MAMBA_ERR_SHAPE: unsupported or out-of-range size";
         case MAMBA_ERR_DTYPE: return "MAMBA_ERR_DTYPE: io_dtype is not MAMBA_F32 or MAMBA_BF16";
         case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a base pointer is not aligned as required";
         case MAMBA_ERR_CUDA: return "MAMBA_ERR_CUDA: a CUDA call failed";

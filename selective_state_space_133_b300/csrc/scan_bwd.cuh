@@ -6,17 +6,23 @@
 // of storing them ("mamba->jamba", blog.csdn.net, §2.3); this kernel does the
 // same, and keeps only one fp32 state per row every 16 steps between its two
 // sweeps. Per step, with dp = dy * silu(z) (or dy) and gh the gradient
-// reaching h_l (reverse-mode differentiation of h_l = e h_{l-1} + dt u B,
-// e = exp(dt A), y = (C.h + D u) silu(z)):
-//     gh     = g + dp C                dC += dp h_l        dB += gh dt u
-//     d(dtu) = sum_n gh B              de = gh h_{l-1}     d(dt) += sum_n de e A
+// reaching h_l (reverse-mode differentiation of h_l = e h_{l-1} + gain u B,
+// e = exp(dt A), gain = dt, y = (C.h + D u) silu(z)):
+//     gh     = g + dp C                dC += dp h_l        dB += gh gain u
+//     de     = gh h_{l-1}              d(dt) += sum_n de e A
 //     dA    += de e dt                 g  = gh e           (to h_{l-1})
-//     du     = dp D + d(dtu) dt        d(dt) += d(dtu) u   ddelta = d(dt) sigmoid(x)
+//     du     = dp D + sum_n gh B gain  d(dt) += sum_n gh B u (d gain / d dt)
+//     ddelta = d(dt) sigmoid(x)
+// With the exact zero-order-hold gain (ZOH; "Mamba 论文精读" §2.2) gain =
+// (e - 1) / A, d gain / d dt = e, and dA also gains gh B u (d gain / dA),
+// d gain / dA = (dt e - gain) / A, taken from its series
+// dt^2 (1/2 + x/3 + x^2/8), x = dt A, where |x| < 1/64 (next term <= 1e-7
+// relative).
 //
-// Layout: one warp per CTA = 16 channels of one batch row, as in the forward.
-// Recurrence lanes (rh, rc) = (lane >> 4, lane & 15) own states 8rh..8rh+7 of
-// channel rc; pre-pass/epilogue lanes (ec, ej) = (lane >> 1, lane & 1) own
-// steps 8ej..8ej+7 of channel ec.
+// Layout as in the forward (FwdGeo<N>): one warp per CTA; recurrence lane
+// (rh, rc) = (lane / kCh, lane % kCh) owns states kS*rh .. kS*rh + kS - 1 of
+// channel rc; pre-pass/epilogue lanes (ec, ej) = (lane / kG, lane % kG) own
+// steps kSP*ej .. kSP*ej + kSP - 1 of channel ec.
 //   Sweep 1 (forward, chunk by chunk): dt and dt*u, the recurrence, and the
 //            state before each chunk stored to the workspace; skipped when the
 //            forward already stored them (its chunk_states output).
@@ -30,100 +36,71 @@
 // and added atomically into the caller's (zeroed) fp32 outputs.
 #pragma once
 
-#include "common.cuh"
+#include "scan_fwd.cuh"
 
 namespace mscan {
 
 constexpr int kBwdTL = 16;   // steps per chunk (the checkpoint interval)
-constexpr int kBwdCh = 16;   // channels per CTA (one warp)
 
 struct ScanBwdArgs {
     const void* u;
     const void* delta;
     const void* z;          // may be null
     const void* dy;
-    const float* bc;        // packed B/C rows, (batch, Lp, 32) fp32
+    const float* bc;        // packed B/C rows, (batch, Lp, 2N) fp32
     const float* A;
     const float* D;         // may be null
     const float* bias;      // may be null
     const float* h0;        // may be null
-    float* hck;             // (batch, dim, n_chunks, 16) fp32: the workspace, or the forward's chunk states
+    float* hck;             // (batch, dim, n_chunks, N) fp32: the workspace, or the forward's chunk states
     int have_hck;           // 1: hck already holds the states (from the forward): skip sweep 1
-    float* dbc;             // workspace: (batch, 2, 16, Lp) fp32 sums of dB, dC (zeroed by the host)
+    float* dbc;             // workspace: (batch, 2, N, Lp) fp32 sums of dB, dC (zeroed by the host)
     void* du;
     void* ddelta;
     void* dz;               // null iff z is null
-    float* dA;              // (dim, 16), zeroed by the host
+    float* dA;              // (dim, N), zeroed by the host
     float* dD;              // (dim) or null, zeroed by the host
     float* dbias;           // (dim) or null, zeroed by the host
-    float* dh0;             // (batch, dim, 16) or null
+    float* dh0;             // (batch, dim, N) or null
     int batch, dim, seqlen, Lp;
-    int softplus;
 };
 
+template <int NS>
 struct ScanBwdSmem {
-    alignas(16) float2 W[kBwdCh][kBwdTL + 1];        // {dt, dt*u}; odd row pitch: distinct banks per channel
-    alignas(16) float SG[kBwdCh][kBwdTL + 1];        // d(dt)/d(delta + bias)
-    alignas(16) float DP[kBwdCh][kBwdTL + 1];        // dp = dy * silu(z)
-    alignas(16) float U[kBwdCh][kBwdTL + 1];         // u
-    alignas(16) float4 traj[kBwdTL][2][32];          // recomputed states: [step][half of the 8][lane]
-    alignas(16) float P[2][kBwdTL / 4][kBwdCh * 4 + 8];  // partial C.h: [state half][4-step group][channel][4]
-    alignas(16) float2 Q[kBwdCh][kBwdTL + 1];        // {d(dtu), d(dt)} per (channel, step), both halves summed
-    alignas(16) float RB[kBwdCh][36];                // one step's dB (cols 0..15) and dC (16..31) per channel
-    alignas(16) float BC[kBwdTL][32];                // the chunk's packed B/C rows
+    using G = FwdGeo<NS>;
+    alignas(16) float2 W[G::kCh][kBwdTL + 1];        // {dt, dt*u} ({dt, u} with ZOH); odd row pitch
+    alignas(16) float SG[G::kCh][kBwdTL + 1];        // d(dt)/d(delta + bias)
+    alignas(16) float DP[G::kCh][kBwdTL + 1];        // dp = dy * silu(z)
+    alignas(16) float U[G::kCh][kBwdTL + 1];         // u
+    alignas(16) float4 traj[kBwdTL][G::kS / 4][32];  // recomputed states: [step][4-state group][lane]
+    alignas(16) float P[G::kG][kBwdTL / 4][G::kCh * 4 + 8];  // partial C.h: [state group][4-step group][channel][4]
+    alignas(16) float2 Q[G::kCh][kBwdTL + 1];        // per (channel, step), all state groups summed:
+                                                     // {sum gh B gain', d(dt) so far}: gain' = 1 for dt*B
+                                                     // (du and d(dt) take their dt / u factors later);
+                                                     // with ZOH gain' = gain and d(dt) is complete
+    alignas(16) float RB[G::kCh][2 * NS + 4];        // one step's dB (cols 0..N-1) and dC (N..2N-1) per channel
+    alignas(16) float BC[kBwdTL][2 * NS];            // the chunk's packed B/C rows
 };
 
-// Eight consecutive values of a row as fp32, zero where l >= L. `vec`: the 8
-// are in range and 16-byte (bf16) / 32-byte (fp32) aligned.
-__device__ __forceinline__ void ldg8(const float* p, float (&v)[8], bool vec, int valid) {
+// n consecutive values of a row in global memory as fp32, zero where past the
+// end: `vec` = all n are in range and aligned for vector loads of at most 16
+// bytes (as stg_n's stores); otherwise the first `valid` one by one.
+template <int n>
+__device__ __forceinline__ void ldg_n(const float* p, float (&v)[n], bool vec, int valid) {
     if (vec) {
-        const float4 a = reinterpret_cast<const float4*>(p)[0];
-        const float4 b = reinterpret_cast<const float4*>(p)[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        lds_n<n>(p, v);  // same vector shapes in global memory
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = i < valid ? p[i] : 0.f;
+        for (int i = 0; i < n; ++i) v[i] = i < valid ? p[i] : 0.f;
     }
 }
-__device__ __forceinline__ void ldg8(const __nv_bfloat16* p, float (&v)[8], bool vec, int valid) {
+template <int n>
+__device__ __forceinline__ void ldg_n(const __nv_bfloat16* p, float (&v)[n], bool vec, int valid) {
     if (vec) {
-        const uint4 q = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            v[2 * j + 0] = __uint_as_float(w[j] << 16);
-            v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-        }
+        lds_n<n>(p, v);
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = i < valid ? __bfloat162float(p[i]) : 0.f;
-    }
-}
-
-// Eight outputs (same rules as ldg8); reuses the forward's stores.
-__device__ __forceinline__ void stg8b(float* p, const float (&v)[8], bool vec, int valid) {
-    if (vec) {
-        reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-        reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < valid) p[i] = v[i];
-    }
-}
-__device__ __forceinline__ void stg8b(__nv_bfloat16* p, const float (&v)[8], bool vec, int valid) {
-    if (vec) {
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 q = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            w[j] = *reinterpret_cast<const uint32_t*>(&q);
-        }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < valid) p[i] = __float2bfloat16_rn(v[i]);
+        for (int i = 0; i < n; ++i) v[i] = i < valid ? __bfloat162float(p[i]) : 0.f;
     }
 }
 
@@ -134,149 +111,168 @@ __device__ __forceinline__ void red_add4(float* p, float4 v) {
                  : "memory");
 }
 
-template <typename T, bool SOFTPLUS, bool HAS_Z>
-__global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
-    __shared__ ScanBwdSmem sm;
+// d gain / dA of the ZOH gain on a pair of states, with x2 = dt*a*log2(e),
+// e = exp(dt a), gain = (e - 1)/a (zoh_gain2), dt and 1/a.
+__device__ __forceinline__ float2 zoh_dgain_da2(float2 x2, float2 e, float2 gain, float2 dt, float2 inv_a) {
     constexpr float kLn2 = 0.6931471805599453f;
+    constexpr float kSmall = 0.022542110013890053f;  // |dt a| < 1/64, as in zoh_gain2
+    const float2 x = __fmul2_rn(x2, make_float2(kLn2, kLn2));
+    float2 t = __ffma2_rn(x, make_float2(0.125f, 0.125f), make_float2(1.f / 3.f, 1.f / 3.f));
+    t = __ffma2_rn(t, x, make_float2(0.5f, 0.5f));
+    const float2 ss = __fmul2_rn(__fmul2_rn(dt, dt), t);
+    const float2 sl = __fmul2_rn(__ffma2_rn(dt, e, make_float2(-gain.x, -gain.y)), inv_a);
+    return make_float2(fabsf(x2.x) < kSmall ? ss.x : sl.x, fabsf(x2.y) < kSmall ? ss.y : sl.y);
+}
+
+template <typename T, int NS, bool SOFTPLUS, bool HAS_Z, bool ZOH>
+__global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
+    using G = FwdGeo<NS>;
+    constexpr int kS = G::kS, kG = G::kG, kCh = G::kCh, kSP = G::kSP;
+    constexpr int H = kS / 2;                              // state pairs per recurrence lane
+    constexpr int kPJ = kCh * 4 + 8;
+    constexpr int kCols = 2 * NS;                          // dB and dC columns of a step
+    constexpr int kCPL = kCols >= 32 ? kCols / 32 : 1;     // columns summed per lane
+    constexpr float kLn2 = 0.6931471805599453f;
+    __shared__ ScanBwdSmem<NS> sm;
     const int lane = threadIdx.x;
-    const int b = blockIdx.y, d0 = blockIdx.x * kBwdCh;
+    const int b = blockIdx.y, d0 = blockIdx.x * kCh;
     const int L = a.seqlen, n = (L + kBwdTL - 1) / kBwdTL;
-    const int rc = lane & 15, rh = lane >> 4;   // recurrence lanes
-    const int ec = lane >> 1, ej = lane & 1;    // pre-pass / epilogue lanes
+    const int rc = lane % kCh, rh = lane / kCh;   // recurrence lanes
+    const int ec = lane / kG, ej = lane % kG;     // pre-pass / epilogue lanes
     const bool ractive = d0 + rc < a.dim;
     const int rd = ractive ? d0 + rc : a.dim - 1;  // clamped for loads of padding channels
     const bool eactive = d0 + ec < a.dim;
     const int ed = eactive ? d0 + ec : a.dim - 1;
     const size_t rrow = static_cast<size_t>(b) * a.dim + rd;
     const size_t erow = static_cast<size_t>(b) * a.dim + ed;
-    const bool vec_ok = eactive && (L & 7) == 0;
+    const bool vec_ok = eactive && (L % G::template vec_steps<T>()) == 0;
 
-    float2 A2[4];
+    float2 A2[H], IA[H];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * kDState + 8 * rh + 2 * i);
+    for (int i = 0; i < H; ++i) {
+        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i);
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
+        if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);
     }
     const float bias = a.bias ? a.bias[ed] : 0.f;
     const float Dd = a.D ? a.D[ed] : 0.f;
-    float* const hck = a.hck + rrow * n * kDState + 8 * rh;
-    const float* const bcb = a.bc + static_cast<size_t>(b) * a.Lp * 32;
+    float* const hck = a.hck + rrow * n * NS + kS * rh;
+    const float* const bcb = a.bc + static_cast<size_t>(b) * a.Lp * kCols;
 
-    // the 8 values of the pre-pass lane's row at steps k*16 + 8ej .. +7 (zero past L)
-    auto load8 = [&](const void* base, int k, float (&v)[8]) {
-        const int l = k * kBwdTL + 8 * ej;
-        ldg8(static_cast<const T*>(base) + erow * L + l, v, vec_ok && l + 8 <= L, eactive ? L - l : 0);
+    // the kSP values of the pre-pass lane's row at steps k*16 + kSP*ej .. (zero past L)
+    auto loadN = [&](const void* base, int k, float (&v)[kSP]) {
+        const int l = k * kBwdTL + kSP * ej;
+        ldg_n<kSP>(static_cast<const T*>(base) + erow * L + l, v, vec_ok && l + kSP <= L, eactive ? L - l : 0);
     };
-    // the chunk's packed B/C rows (2 KB, contiguous) into shared memory: each
-    // 16-byte load and store of the warp covers 512 contiguous bytes
+    // the chunk's packed B/C rows (16 x 2N floats, contiguous) into shared memory
     auto stage_bc = [&](int k) {
-        const float4* src = reinterpret_cast<const float4*>(bcb + static_cast<size_t>(k) * kBwdTL * 32);
+        const float4* src = reinterpret_cast<const float4*>(bcb + static_cast<size_t>(k) * kBwdTL * kCols);
         float4* dst = reinterpret_cast<float4*>(&sm.BC[0][0]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[32 * j + lane] = src[32 * j + lane];
+        for (int j = 0; j < kBwdTL * kCols / 128; ++j) dst[32 * j + lane] = src[32 * j + lane];
     };
-    auto loadB = [&](int t, float2 (&v)[4]) {
-        const float4 p0 = *reinterpret_cast<const float4*>(&sm.BC[t][8 * rh]);
-        const float4 p1 = *reinterpret_cast<const float4*>(&sm.BC[t][8 * rh + 4]);
-        v[0] = make_float2(p0.x, p0.y); v[1] = make_float2(p0.z, p0.w);
-        v[2] = make_float2(p1.x, p1.y); v[3] = make_float2(p1.z, p1.w);
-    };
-    auto loadC = [&](int t, float2 (&v)[4]) {
-        const float4 p0 = *reinterpret_cast<const float4*>(&sm.BC[t][kDState + 8 * rh]);
-        const float4 p1 = *reinterpret_cast<const float4*>(&sm.BC[t][kDState + 8 * rh + 4]);
-        v[0] = make_float2(p0.x, p0.y); v[1] = make_float2(p0.z, p0.w);
-        v[2] = make_float2(p1.x, p1.y); v[3] = make_float2(p1.z, p1.w);
+    auto loadBC = [&](int t, int off, float2 (&v)[H]) {  // off = 0: B, NS: C
+#pragma unroll
+        for (int q = 0; q < kS / 4; ++q) {
+            const float4 p = *reinterpret_cast<const float4*>(&sm.BC[t][off + kS * rh + 4 * q]);
+            v[2 * q] = make_float2(p.x, p.y);
+            v[2 * q + 1] = make_float2(p.z, p.w);
+        }
     };
     auto ex2_pair = [](float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); };
+    // the input term of one step on pair j: dt*u*B, or the ZOH gain times u*B (du holds u then)
+    auto input_term = [&](float2 x2, float2 e, float2 dd, float2 du, float2 Bj, int j) {
+        const float2 t = __fmul2_rn(du, Bj);
+        return ZOH ? __fmul2_rn(zoh_gain2(x2, e, dd, IA[j]), t) : t;
+    };
+    // pre-pass of chunk k: dt and its second operand (dt*u, or u with ZOH) per (channel, step)
+    auto prepass = [&](int k, bool full) {
+        float uv[kSP], dv[kSP];
+        loadN(a.u, k, uv);
+        loadN(a.delta, k, dv);
+        const int le = k * kBwdTL + kSP * ej;
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) {
+            const float x = dv[i] + bias;
+            float dt = x, sg = 1.f;
+            if (SOFTPLUS) {
+                dt = softplus_f(x);
+                if (full) sg = rcp_approx(1.f + ex2_approx(-x * kLog2e));  // softplus'(x) = sigmoid(x)
+            }
+            if (le + i >= L) dt = 0.f;   // padding steps leave the state unchanged
+            sm.W[ec][kSP * ej + i] = make_float2(dt, ZOH ? uv[i] : dt * uv[i]);
+            if (full) {
+                sm.SG[ec][kSP * ej + i] = sg;
+                sm.U[ec][kSP * ej + i] = uv[i];
+            }
+        }
+    };
+    auto store_h = [&](float* p, const float2 (&v)[H]) {
+#pragma unroll
+        for (int q = 0; q < kS / 4; ++q)
+            reinterpret_cast<float4*>(p)[q] = make_float4(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
+    };
+    auto load_h = [&](const float* p, float2 (&v)[H]) {
+#pragma unroll
+        for (int q = 0; q < kS / 4; ++q) {
+            const float4 t = reinterpret_cast<const float4*>(p)[q];
+            v[2 * q] = make_float2(t.x, t.y);
+            v[2 * q + 1] = make_float2(t.z, t.w);
+        }
+    };
 
     // ---------------------------------------------------- sweep 1: forward ----
-    float2 h[4];
+    float2 h[H];
     if (a.h0) {
-        const float4* hp = reinterpret_cast<const float4*>(a.h0 + rrow * kDState + 8 * rh);
-        const float4 p0 = hp[0], p1 = hp[1];
-        h[0] = make_float2(p0.x, p0.y); h[1] = make_float2(p0.z, p0.w);
-        h[2] = make_float2(p1.x, p1.y); h[3] = make_float2(p1.z, p1.w);
+        load_h(a.h0 + rrow * NS + kS * rh, h);
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < H; ++i) h[i] = make_float2(0.f, 0.f);
     }
 #pragma unroll 1
     for (int k = 0; k < (a.have_hck ? 0 : n); ++k) {
-        {
-            float uv[8], dv[8];
-            load8(a.u, k, uv);
-            load8(a.delta, k, dv);
-            const int l = k * kBwdTL + 8 * ej;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float dt = dv[i] + bias;
-                if (SOFTPLUS) dt = softplus_f(dt);
-                if (l + i >= L) dt = 0.f;   // padding steps leave the state unchanged
-                sm.W[ec][8 * ej + i] = make_float2(dt, dt * uv[i]);
-            }
-        }
+        prepass(k, false);
         stage_bc(k);
         __syncwarp();
-        if (ractive) {
-            float4* hp = reinterpret_cast<float4*>(hck + k * kDState);
-            hp[0] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-            hp[1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
-        }
+        if (ractive) store_h(hck + static_cast<size_t>(k) * NS, h);
 #pragma unroll
         for (int t = 0; t < kBwdTL; ++t) {
             const float2 w = sm.W[rc][t];
-            float2 Bv[4];
-            loadB(t, Bv);
+            float2 Bv[H];
+            loadBC(t, 0, Bv);
             const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) h[j] = __ffma2_rn(ex2_pair(__fmul2_rn(dd, A2[j])), h[j], __fmul2_rn(du, Bv[j]));
+            for (int j = 0; j < H; ++j) {
+                const float2 x2 = __fmul2_rn(dd, A2[j]);
+                const float2 e = ex2_pair(x2);
+                h[j] = __ffma2_rn(e, h[j], input_term(x2, e, dd, du, Bv[j], j));
+            }
         }
         __syncwarp();
     }
 
     // ---------------------------------------------------- sweep 2: reverse ----
-    float2 g[4], dAacc[4];
+    float2 g[H], dAacc[H];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) { g[i] = make_float2(0.f, 0.f); dAacc[i] = make_float2(0.f, 0.f); }
+    for (int i = 0; i < H; ++i) { g[i] = make_float2(0.f, 0.f); dAacc[i] = make_float2(0.f, 0.f); }
     float dDacc = 0.f, dbacc = 0.f;
-    const int col_which = lane >> 4, col_n = lane & 15;  // the dB/dC column this lane sums
 #pragma unroll 1
     for (int k = n - 1; k >= 0; --k) {
         const int l0 = k * kBwdTL;
-        const int le = l0 + 8 * ej;  // first step of the pre-pass lane's eight
+        const int le = l0 + kSP * ej;  // first step of the pre-pass lane's kSP
         // the chunk's checkpoint (issued first: its latency overlaps the pre-pass)
-        float2 hs[4];
-        {
-            const float4* hp = reinterpret_cast<const float4*>(hck + k * kDState);
-            const float4 p0 = hp[0], p1 = hp[1];
-            hs[0] = make_float2(p0.x, p0.y); hs[1] = make_float2(p0.z, p0.w);
-            hs[2] = make_float2(p1.x, p1.y); hs[3] = make_float2(p1.z, p1.w);
-        }
-        // (i) dt, dt*u, d(dt)/dx and u per (channel, step), into shared memory
-        {
-            float uv[8], dv[8];
-            load8(a.u, k, uv);
-            load8(a.delta, k, dv);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x = dv[i] + bias;
-                float dt = x, sg = 1.f;
-                if (SOFTPLUS) {
-                    dt = softplus_f(x);
-                    sg = rcp_approx(1.f + ex2_approx(-x * kLog2e));  // softplus'(x) = sigmoid(x)
-                }
-                if (le + i >= L) dt = 0.f;
-                sm.W[ec][8 * ej + i] = make_float2(dt, dt * uv[i]);
-                sm.SG[ec][8 * ej + i] = sg;
-                sm.U[ec][8 * ej + i] = uv[i];
-            }
-        }
+        float2 hs[H];
+        load_h(hck + static_cast<size_t>(k) * NS, hs);
+        // (i) dt, its second operand, d(dt)/dx and u per (channel, step), into shared memory
+        prepass(k, true);
         stage_bc(k);
         __syncwarp();
 
         // (ii) the chunk's states, recomputed from its checkpoint, and C.h
         {
-            float2 hc[4] = {hs[0], hs[1], hs[2], hs[3]};
+            float2 hc[H];
+#pragma unroll
+            for (int j = 0; j < H; ++j) hc[j] = hs[j];
             float* Pw = &sm.P[rh][0][4 * rc];
 #pragma unroll 1
             for (int t0 = 0; t0 < kBwdTL; t0 += 4) {
@@ -285,42 +281,60 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                 for (int i = 0; i < 4; ++i) {
                     const int t = t0 + i;
                     const float2 w = sm.W[rc][t];
-                    float2 Bv[4], Cv[4];
-                    loadB(t, Bv);
-                    loadC(t, Cv);
+                    float2 Bv[H], Cv[H];
+                    loadBC(t, 0, Bv);
+                    loadBC(t, NS, Cv);
                     const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        hc[j] = __ffma2_rn(ex2_pair(__fmul2_rn(dd, A2[j])), hc[j], __fmul2_rn(du, Bv[j]));
-                    sm.traj[t][0][lane] = make_float4(hc[0].x, hc[0].y, hc[1].x, hc[1].y);
-                    sm.traj[t][1][lane] = make_float4(hc[2].x, hc[2].y, hc[3].x, hc[3].y);
+                    for (int j = 0; j < H; ++j) {
+                        const float2 x2 = __fmul2_rn(dd, A2[j]);
+                        const float2 e = ex2_pair(x2);
+                        hc[j] = __ffma2_rn(e, hc[j], input_term(x2, e, dd, du, Bv[j], j));
+                    }
+#pragma unroll
+                    for (int q = 0; q < kS / 4; ++q)
+                        sm.traj[t][q][lane] = make_float4(hc[2 * q].x, hc[2 * q].y, hc[2 * q + 1].x, hc[2 * q + 1].y);
                     float2 acc = __fmul2_rn(Cv[0], hc[0]);
-                    acc = __ffma2_rn(Cv[1], hc[1], acc);
-                    acc = __ffma2_rn(Cv[2], hc[2], acc);
-                    acc = __ffma2_rn(Cv[3], hc[3], acc);
+#pragma unroll
+                    for (int j = 1; j < H; ++j) acc = __ffma2_rn(Cv[j], hc[j], acc);
                     p[i] = acc.x + acc.y;
                 }
-                *reinterpret_cast<float4*>(Pw + (t0 / 4) * (kBwdCh * 4 + 8)) = make_float4(p[0], p[1], p[2], p[3]);
+                *reinterpret_cast<float4*>(Pw + (t0 / 4) * kPJ) = make_float4(p[0], p[1], p[2], p[3]);
             }
         }
         __syncwarp();
 
         // (iii) dp = dy * silu(z) and dz = dy * (C.h + D u) * silu'(z)
         {
-            float gy[8], zv[8], pre[8];
-            load8(a.dy, k, gy);
-            if (HAS_Z) load8(a.z, k, zv);
+            float gy[kSP], zv[kSP], pre[kSP];
+            loadN(a.dy, k, gy);
+            if (HAS_Z) loadN(a.z, k, zv);
+            if constexpr (kSP >= 4) {
 #pragma unroll
-            for (int gq = 0; gq < 2; ++gq) {
-                const float4 x0 = *reinterpret_cast<const float4*>(&sm.P[0][2 * ej + gq][4 * ec]);
-                const float4 x1 = *reinterpret_cast<const float4*>(&sm.P[1][2 * ej + gq][4 * ec]);
-                pre[4 * gq + 0] = x0.x + x1.x; pre[4 * gq + 1] = x0.y + x1.y;
-                pre[4 * gq + 2] = x0.z + x1.z; pre[4 * gq + 3] = x0.w + x1.w;
+                for (int gq = 0; gq < kSP / 4; ++gq) {
+                    const int grp = (kSP / 4) * ej + gq;
+                    float4 s = *reinterpret_cast<const float4*>(&sm.P[0][grp][4 * ec]);
+#pragma unroll
+                    for (int r = 1; r < kG; ++r) {
+                        const float4 x = *reinterpret_cast<const float4*>(&sm.P[r][grp][4 * ec]);
+                        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+                    }
+                    pre[4 * gq] = s.x; pre[4 * gq + 1] = s.y; pre[4 * gq + 2] = s.z; pre[4 * gq + 3] = s.w;
+                }
+            } else {  // two steps: half of a 4-step group
+                const int grp = ej / 2, off = 2 * (ej % 2);
+                float2 s = *reinterpret_cast<const float2*>(&sm.P[0][grp][4 * ec + off]);
+#pragma unroll
+                for (int r = 1; r < kG; ++r) {
+                    const float2 x = *reinterpret_cast<const float2*>(&sm.P[r][grp][4 * ec + off]);
+                    s.x += x.x; s.y += x.y;
+                }
+                pre[0] = s.x; pre[1] = s.y;
             }
-            float dzv[8];
+            float dzv[kSP];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float uu = sm.U[ec][8 * ej + i];
+            for (int i = 0; i < kSP; ++i) {
+                const float uu = sm.U[ec][kSP * ej + i];
                 const float p = fmaf(Dd, uu, pre[i]);
                 float dp = gy[i];
                 if (HAS_Z) {
@@ -329,116 +343,149 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                     dp = gy[i] * zv[i] * s;
                 }
                 dDacc = fmaf(dp, uu, dDacc);
-                sm.DP[ec][8 * ej + i] = dp;
+                sm.DP[ec][kSP * ej + i] = dp;
             }
             if (HAS_Z) {
                 T* dzp = static_cast<T*>(a.dz) + erow * L + le;
-                if (eactive && le < L) stg8b(dzp, dzv, vec_ok && le + 8 <= L, L - le);
+                if (eactive && le < L) stg_n<kSP>(dzp, dzv, vec_ok && le + kSP <= L, L - le);
             }
         }
         __syncwarp();
 
         // (iv) the reverse recurrence over the chunk's 16 steps; this lane's
-        // dB/dC column (the channel sum) goes to the fp32 sums 4 steps at a time
-        float* const dcol = a.dbc + ((static_cast<size_t>(b) * 2 + col_which) * kDState + col_n) * a.Lp + l0;
+        // dB/dC columns (channel sums) go to the fp32 sums 4 steps at a time
 #pragma unroll 1
         for (int t0 = kBwdTL - 4; t0 >= 0; t0 -= 4) {
-          float accBC[4];
+          float accBC[kCPL][4];
 #pragma unroll
           for (int ti = 3; ti >= 0; --ti) {
             const int t = t0 + ti;
             const float2 w = sm.W[rc][t];
             const float dp = sm.DP[rc][t];
-            float2 Bv[4], Cv[4], hT[4], hP[4];
-            loadB(t, Bv);
-            loadC(t, Cv);
-            {
-                const float4 q0 = sm.traj[t][0][lane], q1 = sm.traj[t][1][lane];
-                hT[0] = make_float2(q0.x, q0.y); hT[1] = make_float2(q0.z, q0.w);
-                hT[2] = make_float2(q1.x, q1.y); hT[3] = make_float2(q1.z, q1.w);
+            float2 Bv[H], Cv[H], hT[H], hP[H];
+            loadBC(t, 0, Bv);
+            loadBC(t, NS, Cv);
+#pragma unroll
+            for (int q = 0; q < kS / 4; ++q) {
+                const float4 v = sm.traj[t][q][lane];
+                hT[2 * q] = make_float2(v.x, v.y);
+                hT[2 * q + 1] = make_float2(v.z, v.w);
             }
             if (t > 0) {
-                const float4 q0 = sm.traj[t - 1][0][lane], q1 = sm.traj[t - 1][1][lane];
-                hP[0] = make_float2(q0.x, q0.y); hP[1] = make_float2(q0.z, q0.w);
-                hP[2] = make_float2(q1.x, q1.y); hP[3] = make_float2(q1.z, q1.w);
+#pragma unroll
+                for (int q = 0; q < kS / 4; ++q) {
+                    const float4 v = sm.traj[t - 1][q][lane];
+                    hP[2 * q] = make_float2(v.x, v.y);
+                    hP[2 * q + 1] = make_float2(v.z, v.w);
+                }
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) hP[j] = hs[j];
+                for (int j = 0; j < H; ++j) hP[j] = hs[j];
             }
             const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y), dpp = make_float2(dp, dp);
-            float2 sdtu = make_float2(0.f, 0.f), sdt = make_float2(0.f, 0.f);
-            float2 dBv[4], dCv[4];
+            float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f), sc = make_float2(0.f, 0.f);
+            float2 dBv[H], dCv[H];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 e = ex2_pair(__fmul2_rn(dd, A2[j]));
+            for (int j = 0; j < H; ++j) {
+                const float2 x2 = __fmul2_rn(dd, A2[j]);
+                const float2 e = ex2_pair(x2);
                 const float2 gh = __ffma2_rn(dpp, Cv[j], g[j]);
                 dCv[j] = __fmul2_rn(dpp, hT[j]);
-                dBv[j] = __fmul2_rn(gh, du);
-                sdtu = __ffma2_rn(gh, Bv[j], sdtu);
+                if (ZOH) {  // du holds u
+                    const float2 gain = zoh_gain2(x2, e, dd, IA[j]);
+                    const float2 ghB = __fmul2_rn(gh, Bv[j]);
+                    dBv[j] = __fmul2_rn(__fmul2_rn(gh, gain), du);
+                    sa = __ffma2_rn(ghB, gain, sa);
+                    sc = __ffma2_rn(ghB, e, sc);
+                    dAacc[j] = __ffma2_rn(__fmul2_rn(ghB, du), zoh_dgain_da2(x2, e, gain, dd, IA[j]), dAacc[j]);
+                } else {    // du holds dt*u
+                    dBv[j] = __fmul2_rn(gh, du);
+                    sa = __ffma2_rn(gh, Bv[j], sa);
+                }
                 const float2 dee = __fmul2_rn(__fmul2_rn(gh, hP[j]), e);
-                sdt = __ffma2_rn(dee, A2[j], sdt);
+                sb = __ffma2_rn(dee, A2[j], sb);
                 dAacc[j] = __ffma2_rn(dee, dd, dAacc[j]);
                 g[j] = __fmul2_rn(gh, e);
             }
-            {   // both state halves of the channel: lanes rc and rc + 16
-                float qa = sdtu.x + sdtu.y, qb = sdt.x + sdt.y;
-                qa += __shfl_xor_sync(0xffffffffu, qa, 16);
-                qb += __shfl_xor_sync(0xffffffffu, qb, 16);
-                if (rh == 0) sm.Q[rc][t] = make_float2(qa, qb * kLn2);
+            {   // all state groups of the channel: lanes rc + kCh * m
+                float qa = sa.x + sa.y, qb = sb.x + sb.y, qc = sc.x + sc.y;
+#pragma unroll
+                for (int o = kCh; o < 32; o <<= 1) {
+                    qa += __shfl_xor_sync(0xffffffffu, qa, o);
+                    qb += __shfl_xor_sync(0xffffffffu, qb, o);
+                    if (ZOH) qc += __shfl_xor_sync(0xffffffffu, qc, o);
+                }
+                // with ZOH the term sum_n gh B u e (d gain / d dt = e) completes d(dt) here
+                if (rh == 0) sm.Q[rc][t] = make_float2(qa, ZOH ? fmaf(qc, sm.U[rc][t], qb * kLn2) : qb * kLn2);
             }
             // channel sums of this step's dB and dC
-            float4* rb = reinterpret_cast<float4*>(&sm.RB[rc][0]);
-            rb[2 * rh] = make_float4(dBv[0].x, dBv[0].y, dBv[1].x, dBv[1].y);
-            rb[2 * rh + 1] = make_float4(dBv[2].x, dBv[2].y, dBv[3].x, dBv[3].y);
-            rb[4 + 2 * rh] = make_float4(dCv[0].x, dCv[0].y, dCv[1].x, dCv[1].y);
-            rb[4 + 2 * rh + 1] = make_float4(dCv[2].x, dCv[2].y, dCv[3].x, dCv[3].y);
-            __syncwarp();
-            float2 sacc = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < kBwdCh; c += 2) sacc = __fadd2_rn(sacc, make_float2(sm.RB[c][lane], sm.RB[c + 1][lane]));
-            accBC[ti] = sacc.x + sacc.y;
+            for (int q = 0; q < kS / 4; ++q) {
+                reinterpret_cast<float4*>(&sm.RB[rc][kS * rh])[q] =
+                    make_float4(dBv[2 * q].x, dBv[2 * q].y, dBv[2 * q + 1].x, dBv[2 * q + 1].y);
+                reinterpret_cast<float4*>(&sm.RB[rc][NS + kS * rh])[q] =
+                    make_float4(dCv[2 * q].x, dCv[2 * q].y, dCv[2 * q + 1].x, dCv[2 * q + 1].y);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < kCPL; ++c) {
+                const int col = lane + 32 * c;
+                float2 sacc = make_float2(0.f, 0.f);
+                if (col < kCols) {
+#pragma unroll
+                    for (int ch = 0; ch < kCh; ch += 2)
+                        sacc = __fadd2_rn(sacc, make_float2(sm.RB[ch][col], sm.RB[ch + 1][col]));
+                }
+                accBC[c][ti] = sacc.x + sacc.y;
+            }
             __syncwarp();
           }
-          red_add4(dcol + t0, make_float4(accBC[0], accBC[1], accBC[2], accBC[3]));
+#pragma unroll
+          for (int c = 0; c < kCPL; ++c) {
+              const int col = lane + 32 * c;
+              if (col < kCols) {
+                  float* dcol = a.dbc + ((static_cast<size_t>(b) * 2 + col / NS) * NS + col % NS) * a.Lp + l0;
+                  red_add4(dcol + t0, make_float4(accBC[c][0], accBC[c][1], accBC[c][2], accBC[c][3]));
+              }
+          }
         }
 
         // (v) du and ddelta per (channel, step)
         {
-            float duv[8], dxv[8];
+            float duv[kSP], dxv[kSP];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = 8 * ej + i;
+            for (int i = 0; i < kSP; ++i) {
+                const int t = kSP * ej + i;
                 const float2 q = sm.Q[ec][t];
-                const float sdtu = q.x;
-                const float sdt = fmaf(sdtu, sm.U[ec][t], q.y);
-                duv[i] = fmaf(sm.DP[ec][t], Dd, sdtu * sm.W[ec][t].x);
+                const float dsum = ZOH ? q.x : q.x * sm.W[ec][t].x;      // sum_n gh B gain
+                const float sdt = ZOH ? q.y : fmaf(q.x, sm.U[ec][t], q.y);  // d(dt)
+                duv[i] = fmaf(sm.DP[ec][t], Dd, dsum);
                 dxv[i] = le + i < L ? sdt * sm.SG[ec][t] : 0.f;
                 dbacc += dxv[i];
             }
             if (eactive && le < L) {
-                stg8b(static_cast<T*>(a.du) + erow * L + le, duv, vec_ok && le + 8 <= L, L - le);
-                stg8b(static_cast<T*>(a.ddelta) + erow * L + le, dxv, vec_ok && le + 8 <= L, L - le);
+                stg_n<kSP>(static_cast<T*>(a.du) + erow * L + le, duv, vec_ok && le + kSP <= L, L - le);
+                stg_n<kSP>(static_cast<T*>(a.ddelta) + erow * L + le, dxv, vec_ok && le + kSP <= L, L - le);
             }
         }
         __syncwarp();
     }
 
     // the gradient of the initial state, dA, dD and the bias's gradient
-    if (a.dh0 && ractive) {
-        float4* p = reinterpret_cast<float4*>(a.dh0 + rrow * kDState + 8 * rh);
-        p[0] = make_float4(g[0].x, g[0].y, g[1].x, g[1].y);
-        p[1] = make_float4(g[2].x, g[2].y, g[3].x, g[3].y);
-    }
+    if (a.dh0 && ractive) store_h(a.dh0 + rrow * NS + kS * rh, g);
     if (ractive) {
-        float* p = a.dA + static_cast<size_t>(rd) * kDState + 8 * rh;
+        float* p = a.dA + static_cast<size_t>(rd) * NS + kS * rh;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < H; ++j) {
             atomicAdd(p + 2 * j, dAacc[j].x);
             atomicAdd(p + 2 * j + 1, dAacc[j].y);
         }
     }
-    dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 1);
-    dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 1);
+#pragma unroll
+    for (int o = 1; o < kG; o <<= 1) {   // the kG pre-pass lanes of a channel
+        dDacc += __shfl_xor_sync(0xffffffffu, dDacc, o);
+        dbacc += __shfl_xor_sync(0xffffffffu, dbacc, o);
+    }
     if (eactive && ej == 0) {
         if (a.dD) atomicAdd(a.dD + ed, dDacc);
         if (a.dbias) atomicAdd(a.dbias + ed, dbacc);
@@ -448,18 +495,19 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
 // dB and dC in the I/O dtype from the fp32 sums: out[b][n][l] = dbc[b][which][n][l].
 template <typename T>
 __global__ void __launch_bounds__(256)
-dbc_unpack_kernel(const float* __restrict__ dbc, T* __restrict__ dB, T* __restrict__ dC, int batch, int L, int Lp) {
-    const long long total = static_cast<long long>(batch) * 2 * kDState * L;
+dbc_unpack_kernel(const float* __restrict__ dbc, T* __restrict__ dB, T* __restrict__ dC, int batch, int ns, int L,
+                  int Lp) {
+    const long long total = static_cast<long long>(batch) * 2 * ns * L;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int l = static_cast<int>(i % L);
         const long long r = i / L;  // (b, which, n)
-        const int nn = static_cast<int>(r % kDState);
-        const int which = static_cast<int>((r / kDState) % 2);
-        const int bb = static_cast<int>(r / (2 * kDState));
+        const int nn = static_cast<int>(r % ns);
+        const int which = static_cast<int>((r / ns) % 2);
+        const int bb = static_cast<int>(r / (2 * ns));
         const float v = dbc[r * Lp + l];
         T* out = which ? dC : dB;
-        out[(static_cast<size_t>(bb) * kDState + nn) * L + l] = Io<T>::from_f(v);
+        out[(static_cast<size_t>(bb) * ns + nn) * L + l] = Io<T>::from_f(v);
     }
 }
 

@@ -162,13 +162,13 @@ def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bi
 
 def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
                    initial_state=None, want_initial_state_grad=False, stream=None, workspace=None,
-                   chunk_states=None):
+                   chunk_states=None, zoh=False):
     """Gradients of sum(dy * y) for the scan (see include/mamba_scan.h, mamba_scan_bwd).
 
-    Inputs as mamba_scan_fwd (N = 16, no ZOH gain) plus dy (batch, dim, L) in the I/O dtype. Returns a
-    dict with du, ddelta, dz (or None), dA (dim, 16) fp32, dB, dC (batch, 16, L),
-    dD and ddelta_bias (dim,) fp32 (or None when the input is absent) and dh0
-    (batch, dim, 16) fp32 when ``want_initial_state_grad``.
+    Inputs as mamba_scan_fwd (zoh included) plus dy (batch, dim, L) in the I/O
+    dtype. Returns a dict with du, ddelta, dz (or None), dA (dim, N) fp32, dB,
+    dC (batch, N, L), dD and ddelta_bias (dim,) fp32 (or None when the input is
+    absent) and dh0 (batch, dim, N) fp32 when ``want_initial_state_grad``.
     """
     if u.dtype not in _IO:
         raise TypeError(f"unsupported io dtype {u.dtype}")
@@ -197,7 +197,7 @@ def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softp
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     st = lib.mamba_scan_bwd(
-        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _flags(softplus),
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _flags(softplus, zoh),
         _ptr(initial_state), _ptr(chunk_states), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
         _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(out["dh0"]),
         batch, dim, L, N, _IO[u.dtype], _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))

@@ -168,7 +168,8 @@ def scan_bwd(L, **kw):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(dstate=8), -2), (dict(dstate=64), -2), (dict(sp=2), -8), (dict(sp=3), -8), (dict(sp=4), -8),
+    (dict(dstate=12), -2), (dict(dstate=128), -2), (dict(sp=4), -8), (dict(sp=-1), -8),
+    (dict(dstate=8, du=P + 4), -4), (dict(dstate=64, sp=3, dA=None), -1),
     (dict(dA=None), -1), (dict(z=P, dz=None), -1), (dict(dD=P), -1), (dict(du=P + 4), -4),
     (dict(ws_bytes=100), -7),
 ])
@@ -176,10 +177,12 @@ def test_scan_bwd_rejects(L, kw, code):
     assert scan_bwd(L, **kw) == code
 
 
-def test_bwd_workspace_size_only_for_16_states(L):
-    assert L.mamba_scan_bwd_workspace_size(2, 32, 64, 16, 1) > 0
-    for n in (8, 32, 64):
-        assert L.mamba_scan_bwd_workspace_size(2, 32, 64, n, 1) == 0
+def test_bwd_workspace_size(L):
+    # packed B/C rows + one state per 16 steps + fp32 dB/dC sums, each rounded to 256 bytes
+    for n in (8, 16, 32, 64):
+        want = 2 * 64 * 2 * n * 4 + 2 * 32 * 4 * n * 4 + 2 * 2 * n * 64 * 4
+        assert L.mamba_scan_bwd_workspace_size(2, 32, 64, n, 1) == want
+    assert L.mamba_scan_bwd_workspace_size(2, 32, 64, 24, 1) == 0
 
 
 def ssd(L, **kw):

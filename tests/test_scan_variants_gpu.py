@@ -213,11 +213,3 @@ def test_update_continues_zoh_scan(dstate):
     tol = tol_of(torch.float32)
     assert max_rel_err(np.stack(ys, axis=1), yr[:, L0:]) <= tol
     assert max_rel_err(st.double().cpu().numpy().reshape(-1, dstate), hr) <= tol
-
-
-def test_backward_rejects_other_state_sizes():
-    x = syn.scan_inputs(1, 16, 32, torch.float32, seed=91, dstate=32)
-    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    dy = torch.ones_like(d["u"])
-    with pytest.raises(Exception, match="MAMBA_ERR_SHAPE"):
-        ops.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"], True)
