@@ -36,11 +36,10 @@ METRIC = "selective-scan elems/s (B·L·D·N) & achieved HBM GB/s vs roofline, 1
 UNIT = "elem/s"
 DEFAULT_WORKLOAD = "scan_b8_d2048_l4096_bf16"
 FALLBACK_HBM_GBS = 6400.0
+# the files that define the scan kernel's device code and its launch (grid, TMA boxes)
 KERNEL_SOURCES = ["selective_state_space_133_b300/csrc/scan_fwd.cuh",
                   "selective_state_space_133_b300/csrc/common.cuh",
-                  "selective_state_space_133_b300/csrc/fwd_launch.cuh",
-                  "selective_state_space_133_b300/csrc/host.h",
-                  "selective_state_space_133_b300/csrc/mamba_scan.cu"]
+                  "selective_state_space_133_b300/csrc/fwd_launch.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_fwd_traffic.json")
 
 
