@@ -27,7 +27,7 @@
 //            state before each chunk stored to the workspace; skipped when the
 //            forward already stored them (its chunk_states output).
 //   Sweep 2 (reverse, chunk by chunk): reload the chunk's starting state,
-//            recompute its 16 states into shared memory with C.h; form dp and
+//            recompute the states of its 16 steps into shared memory with C.h; form dp and
 //            dz; run the reverse recurrence over the 16 steps; per step, the
 //            channel sums of dB and dC are formed in shared memory and added
 //            into an fp32 buffer (vector atomics, one per 4 steps); finally
