@@ -83,6 +83,10 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
 }
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
 // D += A B, A 16x16 (row), B 16x8 (col), bf16 operands, fp32 accumulators
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
@@ -198,13 +202,19 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     // tiles advance in steps of 8, so their swizzle term (row & 7) is fixed.
     const int ra = rr + ((mi >> 1) << 3);        // row of this lane in matrices ordered (row, row, row+8, row+8)
     const int rc = rr + ((mi & 1) << 3);         // ... ordered (row, row+8, row, row+8)
-    const uint32_t a_c = ct + ra * 128 + ((((m0 >> 3) + (mi & 1)) ^ (ra & 7)) << 4);   // C^T rows m0.. at k0 = 0
-    uint32_t b_g[2];                             // B tile for C B^T, column pairs c0 + 16 jp, at k0 = 0
+    // Outputs (C S^T, the masked product, y): two row blocks of equal causal
+    // work, {0, 3} or {1, 2}, and one quarter (16) of the head's channels.
+    const int yrb[2] = {(warp & 1) ? 1 : 0, (warp & 1) ? 2 : 3};
+    const int pq = warp >> 1;
+    uint32_t a_y[2];                             // C^T rows of the two output row blocks, at k0 = 0
 #pragma unroll
-    for (int jp = 0; jp < 2; ++jp) b_g[jp] = bt + rc * 128 + ((((c0 >> 3) + 2 * jp + (mi >> 1)) ^ (rc & 7)) << 4);
-    const uint32_t x_row = xt + (c0 + ra) * 128;  // X rows c0 + ra (+16 jp)
-    const uint32_t b_row = bt + (n0 + ra) * 128;  // Bt rows n0 + ra (+16 jp)
+    for (int r = 0; r < 2; ++r) a_y[r] = ct + ra * 128 + (((2 * yrb[r] + (mi & 1)) ^ (ra & 7)) << 4);
+    const uint32_t x_q = xt + (16 * pq + ra) * 128;  // X rows of the channel quarter
     const int sw = ra & 7;
+    // C B^T: the 20 (row block, column block, 8-column half) units of the causal
+    // triangle, dealt round-robin: units warp, warp + 8, warp + 16
+    const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix.x2 row of this lane
+    const uint32_t b_row = bt + (n0 + ra) * 128;  // Bt rows n0 + ra (+16 jp)
 
     // dt and the cumulative decay of chunk k into buffer k & 1 (warp 0);
     // padding steps get dt = 0
@@ -246,117 +256,125 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         const float* dtv = sm.dt[k & 1];
         if (!mbar_wait_bounded(&sm.full[2], par)) timed_out = true;  // C
 
-        // --- C S^T (carried state), then C B^T once B is in ---
-        float Y[4][4], G[4][4];
+        // --- C S^T (carried state) for this warp's two row blocks and channel quarter ---
+        float Y[2][2][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) { Y[j][e] = 0.f; G[j][e] = 0.f; }
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Y[r][j][e] = 0.f;
         const bool carry = have_state || k > 0;
         if (carry) {
 #pragma unroll
             for (int k0 = 0; k0 < NS; k0 += 16) {
-                uint32_t af[4], bh[2][4], bl[2][4];  // A = C^T rows m0.. from Ct[n][l]; B = S^T from Sh/Sl[p][n]
-                ldsm_x4_t(a_c + k0 * 128, af);
+                uint32_t af[2][4], bh[4], bl[4];  // A = C^T rows from Ct[n][l]; B = S^T from Sh/Sl[p][n]
+                ldsm_x4_t(a_y[0] + k0 * 128, af[0]);
+                ldsm_x4_t(a_y[1] + k0 * 128, af[1]);
+                ldsm_x4(smem_u32(&sm.Sh[16 * pq + ra][k0 + 8 * (mi & 1)]), bh);
+                ldsm_x4(smem_u32(&sm.Sl[16 * pq + ra][k0 + 8 * (mi & 1)]), bl);
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    const int prow = c0 + 16 * jp + ra;
-                    ldsm_x4(smem_u32(&sm.Sh[prow][k0 + 8 * (mi & 1)]), bh[jp]);
-                    ldsm_x4(smem_u32(&sm.Sl[prow][k0 + 8 * (mi & 1)]), bl[jp]);
+                for (int r = 0; r < 2; ++r) {
+                    mma_bf16(Y[r][0], af[r], bh[0], bh[1]);
+                    mma_bf16(Y[r][1], af[r], bh[2], bh[3]);
                 }
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    mma_bf16(Y[2 * jp], af, bh[jp][0], bh[jp][1]);
-                    mma_bf16(Y[2 * jp + 1], af, bh[jp][2], bh[jp][3]);
+                for (int r = 0; r < 2; ++r) {
+                    mma_bf16(Y[r][0], af[r], bl[0], bl[1]);
+                    mma_bf16(Y[r][1], af[r], bl[2], bl[3]);
                 }
+            }
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    mma_bf16(Y[2 * jp], af, bl[jp][0], bl[jp][1]);
-                    mma_bf16(Y[2 * jp + 1], af, bl[jp][2], bl[jp][3]);
-                }
+            for (int r = 0; r < 2; ++r) {
+                const float e0 = ex2_approx(c2[16 * yrb[r] + g]), e1 = ex2_approx(c2[16 * yrb[r] + g + 8]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) { Y[r][j][0] *= e0; Y[r][j][1] *= e0; Y[r][j][2] *= e1; Y[r][j][3] *= e1; }
             }
         }
         if (!mbar_wait_bounded(&sm.full[1], par)) timed_out = true;  // B
-        if (2 * chalf <= rb) {  // columns s <= m0 + 15 only
+        // --- C B^T over this warp's units of the causal triangle, masked and weighted ---
+        {
+            float G[3][4];
+            int urb[3], ucol[3];  // row block and first column of each unit
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                // unit u -> (row block, column block, half): u = rb (rb + 1) + 2 sb + nt
+                const int u = warp + 8 * i;
+                const int rbu = u < 2 ? 0 : (u < 6 ? 1 : (u < 12 ? 2 : 3));
+                const int rem = u - rbu * (rbu + 1);
+                urb[i] = rbu;
+                ucol[i] = 8 * rem;            // 16 sb + 8 nt
+#pragma unroll
+                for (int e = 0; e < 4; ++e) G[i][e] = 0.f;
+            }
 #pragma unroll
             for (int k0 = 0; k0 < NS; k0 += 16) {
-                uint32_t af[4];
-                ldsm_x4_t(a_c + k0 * 128, af);
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    if (2 * chalf + jp <= rb) {
-                        uint32_t bf[4];
-                        ldsm_x4_t(b_g[jp] + k0 * 128, bf);
-                        mma_bf16(G[2 * jp], af, bf[0], bf[1]);
-                        mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
+                for (int i = 0; i < 3; ++i) {
+                    if (warp + 8 * i < 20) {
+                        uint32_t af[4], bf[2];
+                        ldsm_x4_t(ct + (k0 + ra) * 128 + (((2 * urb[i] + (mi & 1)) ^ (ra & 7)) << 4), af);
+                        ldsm_x2_t(bt + (k0 + krow) * 128 + (((ucol[i] >> 3) ^ (krow & 7)) << 4), bf);
+                        mma_bf16(G[i], af, bf[0], bf[1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                if (warp + 8 * i < 20) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int l = 16 * urb[i] + g + 8 * hf;
+                        const float cl = c2[l];
+                        float v[2];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int sc = ucol[i] + 2 * tq + c;
+                            v[c] = sc <= l ? G[i][2 * hf + c] * ex2_approx(cl - c2[sc]) * dtv[sc] : 0.f;
+                        }
+                        uint32_t hi, lo;
+                        split2(v[0], v[1], hi, lo);
+                        *reinterpret_cast<uint32_t*>(&sm.Oh[l][ucol[i] + 2 * tq]) = hi;
+                        *reinterpret_cast<uint32_t*>(&sm.Ol[l][ucol[i] + 2 * tq]) = lo;
                     }
                 }
             }
         }
-        const float cl0 = c2[m0 + g], cl1 = c2[m0 + g + 8];
-        if (carry) {
-            const float e0 = ex2_approx(cl0), e1 = ex2_approx(cl1);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) { Y[j][0] *= e0; Y[j][1] *= e0; Y[j][2] *= e1; Y[j][3] *= e1; }
-        }
-        // masked, decay-weighted C B^T -> high/low parts (rows m0.., this warp's columns)
-#pragma unroll
-        for (int jt = 0; jt < 4; ++jt) {
-            if (2 * chalf + (jt >> 1) <= rb) {
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int l = m0 + g + 8 * hf;
-                    const float cl = hf ? cl1 : cl0;
-                    float v[2];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int sc = c0 + 8 * jt + 2 * tq + c;
-                        v[c] = sc <= l ? G[jt][2 * hf + c] * ex2_approx(cl - c2[sc]) * dtv[sc] : 0.f;
-                    }
-                    uint32_t hi, lo;
-                    split2(v[0], v[1], hi, lo);
-                    *reinterpret_cast<uint32_t*>(&sm.Oh[l][c0 + 8 * jt + 2 * tq]) = hi;
-                    *reinterpret_cast<uint32_t*>(&sm.Ol[l][c0 + 8 * jt + 2 * tq]) = lo;
-                }
-            }
-        }
-        __syncthreads();  // the masked rows of both column halves are in; C is consumed
+        __syncthreads();  // every unit of the triangle is in; C is consumed
         if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
             fence_proxy_async_smem();
             issue(2, k + 1);
         }
         if (!mbar_wait_bounded(&sm.full[0], par)) timed_out = true;  // x
-        // --- Y += (masked C B^T) X^T over s < m0 + 16 ---
+        // --- Y += (masked C B^T) X^T over s < 16 (row block + 1) ---
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            if (kb <= rb) {
-                uint32_t ah[4], al[4], bx[2][4];
-                const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
-                ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
-                ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
+        for (int r = 0; r < 2; ++r) {
 #pragma unroll
-                for (int jp = 0; jp < 2; ++jp)  // B = X^T from X[p][s]
-                    ldsm_x4(x_row + jp * 16 * 128 + (((2 * kb + (mi & 1)) ^ sw) << 4), bx[jp]);
-#pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    mma_bf16(Y[2 * jp], ah, bx[jp][0], bx[jp][1]);
-                    mma_bf16(Y[2 * jp + 1], ah, bx[jp][2], bx[jp][3]);
-                }
-#pragma unroll
-                for (int jp = 0; jp < 2; ++jp) {
-                    mma_bf16(Y[2 * jp], al, bx[jp][0], bx[jp][1]);
-                    mma_bf16(Y[2 * jp + 1], al, bx[jp][2], bx[jp][3]);
+            for (int kb = 0; kb < 4; ++kb) {
+                if (kb <= yrb[r]) {
+                    uint32_t ah[4], al[4], bx[4];
+                    const int arow = 16 * yrb[r] + rc, acol = 16 * kb + 8 * (mi >> 1);
+                    ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
+                    ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
+                    ldsm_x4(x_q + (((2 * kb + (mi & 1)) ^ sw) << 4), bx);  // B = X^T from X[p][s]
+                    mma_bf16(Y[r][0], ah, bx[0], bx[1]);
+                    mma_bf16(Y[r][1], ah, bx[2], bx[3]);
+                    mma_bf16(Y[r][0], al, bx[0], bx[1]);
+                    mma_bf16(Y[r][1], al, bx[2], bx[3]);
                 }
             }
         }
         __syncthreads();  // every warp is done with the masked rows: the O buffers take the weighted x
         // --- outputs (+ D x) into Yt; decay-weighted x into the O buffers ---
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int r = 0; r < 2; ++r) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int l = m0 + g + 8 * (e >> 1), p = c0 + 8 * j + 2 * tq + (e & 1);
-                sm.Yt[p][l] = Y[j][e] + Dh * swz_ld(&sm.X[0][0], p, l);
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int l = 16 * yrb[r] + g + 8 * (e >> 1), p = 16 * pq + 8 * j + 2 * tq + (e & 1);
+                    sm.Yt[p][l] = Y[r][j][e] + Dh * swz_ld(&sm.X[0][0], p, l);
+                }
             }
         }
         const float clast = c2[kSsdQ - 1];
