@@ -1,4 +1,4 @@
-// State-space dual (SSD) layer, chunked form on the tensor cores, sm_103a.
+// State-space dual (SSD) layer, chunked form on the 5th-generation tensor cores, sm_103a.
 //
 // The Mamba-2 form of the selective SSM ("Mamba 论文精读", youngju.dev, §4.1:
 // the recurrence h_t = A_t h_{t-1} + B_t x_t, y_t = C_t h_t is dual to the
@@ -11,37 +11,47 @@
 //         + e^{c_l} S_prev C_l                                    (carried state)
 //         + D_h x_l
 //     S_new = e^{c_Q} S_prev + sum_s x_s (e^{c_Q - c_s} dt_s) B_s^T.
-// The four contractions (C B^T, its masked product with X, the state update
-// and C S^T) run on the tensor cores: bf16 operands, fp32 accumulation.
-// Three operands are not bf16 inputs but values computed in fp32 (the masked
-// C B^T, the decay-weighted x and the carried state); each is split into a
-// bf16 high part and a bf16 remainder and multiplied twice, which keeps them
-// to ~2^-17 relative (one bf16 rounding of those operands alone costs up to
-// 1e-2 relative error in y at N = 128, over the bf16 I/O tolerance).
+// Four contractions per chunk, all `tcgen05.mma` (bf16 operands from shared
+// memory, fp32 accumulators in tensor memory), issued by one thread:
+//     G  = C^T B            M = 64 (l), N = 64 (s), K = N      -> TMEM cols   0..63
+//     Y1 = C^T S_prev^T     M = 64 (l), N = 64 (p), K = N      -> TMEM cols  64..127
+//     Y2 = Gm X^T           M = 64 (l), N = 64 (p), K = 64 (s) -> TMEM cols 128..191
+//     U  = B W^T            M = N (n),  N = 64 (p), K = 64 (s) -> TMEM cols 192..255
+// with Gm the causally masked, decay-weighted G and W the decay-weighted x
+// (W[p][s] = x[p][s] e^{c_Q - c_s} dt_s). C and B are used straight from their
+// TMA tiles ([n][l] rows): as MN-major operands where the contraction runs over
+// n, as a K-major one (B in U) where it runs over s. Three operands are not bf16
+// inputs but values computed in fp32 (Gm, W and the carried state); each is
+// split into a bf16 high part and a bf16 remainder and multiplied twice, which
+// keeps them to ~2^-17 relative (one bf16 rounding of those operands alone
+// costs up to 1e-2 relative error in y at N = 128, over the bf16 tolerance).
 //
 // One CTA (8 warps) per (head, batch row) walks the chunks in order; the fp32
-// state never leaves the registers (it is the state-update product's
-// accumulator). Warp w owns row block w & 3 (16 rows: steps l of the outputs
-// and of C B^T, channels p of the state) and column half w >> 2 of every
-// per-chunk product, so that two CTAs (16 warps) fit on an SM and hide each
-// other's latencies. The x, B and C tiles arrive by 3-D TMA (128-byte swizzled
-// rows), each on its own barrier and refilled for the next chunk as soon as
-// its last reader is done (C after C S^T and C B^T, x after the outputs, B
-// after the state update); the operands the CTA writes itself use padded
-// rows. Within each product the high-part MMAs of all column tiles are issued
-// before the low-part ones, so no two consecutive MMAs share an accumulator.
-// Steps past the end of the sequence get dt = 0, so they leave the state
-// unchanged.
+// state stays in registers (a thread holds one state column n for 32 of the
+// channels), updated from U as S = e^{c_Q} S + U and written back, split, as
+// the next chunk's operand. Two CTAs share an SM (104 KB of shared memory and
+// 256 TMEM columns each), so one's elementwise work overlaps the other's
+// contractions and loads. Per chunk: thread 0 issues G and Y1 as soon as C and
+// B are in; meanwhile every thread forms W; then Gm from G (tcgen05.ld, mask,
+// weights, split); barrier; thread 0 issues Y2 and U; every thread forms the
+// outputs y = e^{c_l} Y1 + Y2 + D x (staged in shared memory for 16-byte row
+// stores) and the new state. The x, B and C tiles arrive by 3-D TMA (128-byte
+// swizzle) on their own barriers and are refilled for the next chunk as soon
+// as the contractions reading them are done. Steps past the end of the
+// sequence get dt = 0, so they leave the state unchanged. Every wait is
+// bounded: a wait that runs out is reported through the device error word,
+// the chunk finishes and the kernel leaves with its tensor memory freed.
 #pragma once
 
 #include "common.cuh"
 
 namespace mscan {
 
-constexpr int kSsdQ = 64;         // chunk length
-constexpr int kSsdP = 64;         // head dimension
-constexpr int kSsdThreads = 256;  // 8 warps
-constexpr int kSsdPad = 8;        // row padding (bf16) of the operands written in shared memory
+constexpr int kSsdQ = 64;          // chunk length
+constexpr int kSsdP = 64;          // head dimension
+constexpr int kSsdThreads = 256;   // 8 warps
+constexpr int kSsdTmemCols = 256;  // G, Y1, Y2, U: 64 fp32 columns each
+constexpr int kSsdYPitch = 72;     // row pitch (bf16) of the output staging tile
 
 struct SsdArgs {
     const void* delta;   // (batch, nheads, L) bf16
@@ -56,51 +66,41 @@ struct SsdArgs {
     int softplus;
 };
 
+// All tiles are rows of 64 bf16 (128 bytes) in the 128-byte swizzle (16-byte
+// unit u of row r stored at unit u ^ (r & 7), tiles 1024-aligned): the layout
+// TMA writes and the tensor cores read.
 template <int NS>
 struct SsdSmem {
-    // TMA tiles: rows of 64 bf16 (128 bytes), 128-byte swizzle
-    alignas(1024) __nv_bfloat16 X[kSsdP][kSsdQ];   // x   [p][s]
-    alignas(1024) __nv_bfloat16 Bt[NS][kSsdQ];     // B   [n][s]
-    alignas(1024) __nv_bfloat16 Ct[NS][kSsdQ];     // C   [n][l]
-    // operands computed here, high and low bf16 parts: the masked C B^T [l][s]
-    // until its product with x is done, then the decay-weighted x [p][s]
-    alignas(16) __nv_bfloat16 Oh[kSsdQ][kSsdQ + kSsdPad], Ol[kSsdQ][kSsdQ + kSsdPad];
-    alignas(16) __nv_bfloat16 Sh[kSsdP][NS + kSsdPad], Sl[kSsdP][NS + kSsdPad];  // state [p][n]
-    alignas(16) float Yt[kSsdP][kSsdQ + 4];  // the chunk's outputs [p][l], for row-contiguous stores
-    float c2[2][kSsdQ];                      // c_l * log2(e), chunk k in [k & 1]
-    float dt[2][kSsdQ];
-    alignas(8) uint64_t full[3];             // x, B, C tiles
+    alignas(1024) __nv_bfloat16 X[kSsdP][kSsdQ];   // x [p][s]            (TMA)
+    alignas(1024) __nv_bfloat16 Bt[NS][kSsdQ];     // B [n][s]            (TMA)
+    alignas(1024) __nv_bfloat16 Ct[NS][kSsdQ];     // C [n][l]            (TMA)
+    alignas(1024) __nv_bfloat16 Gh[kSsdQ][kSsdQ];  // Gm [l][s], high part
+    alignas(1024) __nv_bfloat16 Gl[kSsdQ][kSsdQ];  //            low part
+    // W [p][s] high and low parts; once the U product is done, the staging
+    // tile of the chunk's outputs y [p][l] (bf16, pitch kSsdYPitch)
+    alignas(1024) __nv_bfloat16 Wh[kSsdP][kSsdQ];
+    alignas(1024) __nv_bfloat16 Wl[kSsdP][kSsdQ];
+    // carried state [p][n] high and low parts, in 64-column blocks [n / 64][p][n % 64]
+    alignas(1024) __nv_bfloat16 Sh[NS / 64][kSsdP][64];
+    alignas(1024) __nv_bfloat16 Sl[NS / 64][kSsdP][64];
+    alignas(16) float c2[2][kSsdQ];  // c_l * log2(e), chunk k in [k & 1]
+    alignas(16) float dt[2][kSsdQ];
+    alignas(16) float wq[2][kSsdQ];  // e^{c_Q - c_s} dt_s
+    alignas(8) uint64_t full[3];     // TMA: x, B, C
+    alignas(8) uint64_t done[4];     // MMA completion: G, Y1, Y2, U
+    uint32_t tmem;                   // base address of this CTA's tensor memory
 };
-static_assert(kSsdQ == kSsdP, "the O buffers hold both Q x Q and P x Q operands");
+static_assert(kSsdP * kSsdYPitch * 2 <= 2 * kSsdP * kSsdQ * 2, "the y staging tile fits in the W buffers");
 
 // ------------------------------------------------------------ helpers ------
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+// Byte offset of element (row, col) in a swizzled tile of 128-byte rows.
+__device__ __forceinline__ int swz(int row, int col) {
+    return row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t (&r)[2]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
-                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
-// D += A B, A 16x16 (row), B 16x8 (col), bf16 operands, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-                 "{%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// Element (row, col) of a tile of 128-byte rows written by TMA with the
-// 128-byte swizzle (16-byte unit u of row r stored at unit u ^ (r & 7); tile
-// base 1024-aligned).
 __device__ __forceinline__ float swz_ld(const __nv_bfloat16* tile, int row, int col) {
-    const unsigned char* p = reinterpret_cast<const unsigned char*>(tile) + row * 128 +
-                             ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1));
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+    return __bfloat162float(
+        *reinterpret_cast<const __nv_bfloat16*>(reinterpret_cast<const unsigned char*>(tile) + swz(row, col)));
 }
 // v as a bf16 pair hi + lo: hi = bf16(v), lo = bf16(v - hi).
 __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
@@ -110,7 +110,61 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_
     hi = *reinterpret_cast<const uint32_t*>(&h);
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+}
 
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
+// byte offsets, descriptor version 1 (bit 46), 128-byte swizzle (2 << 61).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+// K-major operand: rows (M or N) of 128 bytes along K, groups of 8 rows 1024
+// bytes apart; one K16 step is a 32-byte offset inside the swizzled rows.
+__device__ __forceinline__ uint64_t desc_k(uint32_t saddr) { return umma_desc(saddr, 16, 1024); }
+// MN-major operand of one 64-wide block along M (or N): rows along K, 128
+// bytes each, groups of 8 rows 1024 bytes apart; one K16 step is 2048 bytes.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t saddr) { return umma_desc(saddr, 1024, 1024); }
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A/B
+// MN-major (transposed) flags, N / 8 and M / 16.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D (tensor memory) = A B (+ D if acc); issued by one thread.
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+        : "memory");
+}
+// `bar` receives one arrival once every MMA this thread has issued is done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 lanes x 256 bits: thread t gets rows t/4 and t/4 + 8 (from the lane base),
+// columns 2(t%4) and 2(t%4) + 1 of the 8 at `taddr`: r = {(r0,c0), (r0,c1), (r8,c0), (r8,c1)}.
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+// 32 lanes x 32 bits, 16 columns: thread t gets lane (base + t), columns c..c+15.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------- kernel ------
 
@@ -118,28 +172,31 @@ template <int NS>
 __global__ void __launch_bounds__(kSsdThreads, 2)
 ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c) {
+    static_assert(NS == 64 || NS == 128, "state sizes 64 and 128 are compiled");
     extern __shared__ unsigned char ssd_smem_raw[];
     // 1024-byte aligned view of the dynamic shared memory, derived from the
     // shared array itself so that every access stays a shared-memory access
     SsdSmem<NS>& sm = *reinterpret_cast<SsdSmem<NS>*>(ssd_smem_raw + ((1024u - (smem_u32(ssd_smem_raw) & 1023u)) & 1023u));
-    constexpr int kNH = NS / 16;  // 8-column state tiles of a warp (half of the state)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, tq = lane & 3;      // accumulator row group / column pair
-    const int mi = lane >> 3, rr = lane & 7;     // ldmatrix: which 8x8 matrix, which row of it
-    const int rb = warp & 3, chalf = warp >> 2;
-    const int m0 = 16 * rb;                      // this warp's rows
-    const int c0 = 32 * chalf;                   // its half of the 64 columns (channels p, or steps s of C B^T)
-    const int n0 = chalf * (NS / 2);             // its half of the state columns
+    const int q = warp & 3;      // the TMEM lane quarter this warp may access
+    const int half = warp >> 2;  // its half (32 columns) of every per-chunk product
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = a.seqlen;
     const int n = (L + kSsdQ - 1) / kSsdQ;
     const int dim = a.nheads * kSsdP;
-    const int ch0 = h * kSsdP;                   // first channel of the head
+    const int ch0 = h * kSsdP;  // first channel of the head
     const float Ah2 = a.A[h] * kLog2e;
     const float bias = a.bias ? a.bias[h] : 0.f;
     const float Dh = a.D ? a.D[h] : 0.f;
     const size_t head_row = static_cast<size_t>(b) * a.nheads + h;
 
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
+                     "n"(kSsdTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
     // tile loads of chunk k (thread 0): barrier 0 = x, 1 = B, 2 = C; parity k & 1
     int last[3] = {-1, -1, -1};
     auto issue = [&](int which, int k) {
@@ -161,75 +218,57 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     };
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&sm.full[i], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&sm.done[i], 1);
         fence_barrier_init();
         if (n > 0) { issue(2, 0); issue(1, 0); issue(0, 0); }
     }
+    __syncwarp();
 
-    // The state: rows m0 + g (+8), columns n0 + 8j + 2tq (+1).
-    float S[kNH][4];
+    // The state: this thread holds column sn of it for channels p = 32 half + j.
+    // U's row n lies in TMEM lane n at N = 128 (M = 128) and in lane
+    // 32 (n / 16) + n % 16 at N = 64 (M = 64), where lanes 16..31 of a warp hold none.
+    const bool sact = NS == 128 || lane < 16;
+    const int sn = NS == 128 ? 32 * q + lane : 16 * q + (lane & 15);
     const bool have_state = a.h0 != nullptr;
+    float S[32];
 #pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int p = m0 + g + 8 * (e >> 1), c = n0 + 8 * j + 2 * tq + (e & 1);
-            S[j][e] = have_state ? a.h0[(head_row * kSsdP + p) * NS + c] : 0.f;
-        }
-    }
+    for (int j = 0; j < 32; ++j)
+        S[j] = (have_state && sact) ? a.h0[(head_row * kSsdP + 32 * half + j) * NS + sn] : 0.f;
     auto store_state_parts = [&]() {
+        if (!sact) return;
+        unsigned char* hb = reinterpret_cast<unsigned char*>(&sm.Sh[sn >> 6][0][0]);
+        unsigned char* lb = reinterpret_cast<unsigned char*>(&sm.Sl[sn >> 6][0][0]);
+        const int c = sn & 63;
 #pragma unroll
-        for (int j = 0; j < kNH; ++j) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t hi, lo;
-                split2(S[j][2 * hf], S[j][2 * hf + 1], hi, lo);
-                const int p = m0 + g + 8 * hf, c = n0 + 8 * j + 2 * tq;
-                *reinterpret_cast<uint32_t*>(&sm.Sh[p][c]) = hi;
-                *reinterpret_cast<uint32_t*>(&sm.Sl[p][c]) = lo;
-            }
+        for (int j = 0; j < 32; ++j) {
+            const int o = swz(32 * half + j, c);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(S[j]);
+            *reinterpret_cast<__nv_bfloat16*>(hb + o) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(lb + o) = __float2bfloat16_rn(S[j] - __bfloat162float(hi));
         }
     };
     if (have_state) store_state_parts();
-    __syncthreads();
+    // Gm is zero above the diagonal; those blocks are never written again
+    for (int i = tid; i < kSsdQ * kSsdQ * 2 / 16; i += kSsdThreads) {
+        reinterpret_cast<uint4*>(&sm.Gh[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(&sm.Gl[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
 
+    // dt, the cumulative decay and the state-update weights of chunk k into
+    // buffer k & 1 (warp 0); padding steps get dt = 0
     const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(a.delta) + head_row * L;
-    __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
-    const bool vec_ok = (L & 7) == 0;
-    const uint32_t xt = smem_u32(&sm.X[0][0]);
-    const uint32_t bt = smem_u32(&sm.Bt[0][0]);
-    const uint32_t ct = smem_u32(&sm.Ct[0][0]);
-    // Loop-invariant parts of the ldmatrix addresses. Rows of the swizzled
-    // tiles advance in steps of 8, so their swizzle term (row & 7) is fixed.
-    const int ra = rr + ((mi >> 1) << 3);        // row of this lane in matrices ordered (row, row, row+8, row+8)
-    const int rc = rr + ((mi & 1) << 3);         // ... ordered (row, row+8, row, row+8)
-    // Outputs (C S^T, the masked product, y): two row blocks of equal causal
-    // work, {0, 3} or {1, 2}, and one quarter (16) of the head's channels.
-    const int yrb[2] = {(warp & 1) ? 1 : 0, (warp & 1) ? 2 : 3};
-    const int pq = warp >> 1;
-    uint32_t a_y[2];                             // C^T rows of the two output row blocks, at k0 = 0
-#pragma unroll
-    for (int r = 0; r < 2; ++r) a_y[r] = ct + ra * 128 + (((2 * yrb[r] + (mi & 1)) ^ (ra & 7)) << 4);
-    const uint32_t x_q = xt + (16 * pq + ra) * 128;  // X rows of the channel quarter
-    const int sw = ra & 7;
-    // C B^T: the 20 (row block, column block, 8-column half) units of the causal
-    // triangle, dealt round-robin: units warp, warp + 8, warp + 16
-    const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);  // ldmatrix.x2 row of this lane
-    const uint32_t b_row = bt + (n0 + ra) * 128;  // Bt rows n0 + ra (+16 jp)
-
-    // dt and the cumulative decay of chunk k into buffer k & 1 (warp 0);
-    // padding steps get dt = 0
     auto decay_prefix = [&](int k) {
-        float v[2];
+        float v[2], d[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int l = 2 * lane + i, gl = k * kSsdQ + l;
-            float d = 0.f;
+            d[i] = 0.f;
             if (gl < L) {
-                d = __bfloat162float(dl[gl]) + bias;
-                if (a.softplus) d = softplus_f(d);
+                d[i] = __bfloat162float(dl[gl]) + bias;
+                if (a.softplus) d[i] = softplus_f(d[i]);
             }
-            sm.dt[k & 1][l] = d;
-            v[i] = d * Ah2;
+            sm.dt[k & 1][l] = d[i];
+            v[i] = d[i] * Ah2;
         }
         const float pair = v[0] + v[1];
         float incl = pair;
@@ -239,11 +278,36 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             if (lane >= o) incl += t;
         }
         const float excl = incl - pair;
-        sm.c2[k & 1][2 * lane] = excl + v[0];
-        sm.c2[k & 1][2 * lane + 1] = excl + pair;
+        const float cq = __shfl_sync(0xffffffffu, incl, 31);
+        const float c0 = excl + v[0], c1 = excl + pair;
+        sm.c2[k & 1][2 * lane] = c0;
+        sm.c2[k & 1][2 * lane + 1] = c1;
+        sm.wq[k & 1][2 * lane] = ex2_approx(cq - c0) * d[0];
+        sm.wq[k & 1][2 * lane + 1] = ex2_approx(cq - c1) * d[1];
     };
     if (warp == 0 && n > 0) decay_prefix(0);
+    fence_proxy_async_smem();  // the state parts and the zeros, for the tensor cores
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem = sm.tmem;
+    const uint32_t tG = tmem, tY1 = tmem + 64, tY2 = tmem + 128, tU = tmem + 192;
+    const uint32_t xs = smem_u32(&sm.X[0][0]), bs = smem_u32(&sm.Bt[0][0]), cs = smem_u32(&sm.Ct[0][0]);
+    const uint32_t ghs = smem_u32(&sm.Gh[0][0]), gls = smem_u32(&sm.Gl[0][0]);
+    const uint32_t whs = smem_u32(&sm.Wh[0][0]), wls = smem_u32(&sm.Wl[0][0]);
+    const uint32_t shs = smem_u32(&sm.Sh[0][0][0]), sls = smem_u32(&sm.Sl[0][0][0]);
+    constexpr uint32_t kIdG = umma_idesc(64, 64, true, true);     // C^T (MN-major) x B (MN-major)
+    constexpr uint32_t kIdY1 = umma_idesc(64, 64, true, false);   // C^T (MN-major) x S^T (K-major)
+    constexpr uint32_t kIdY2 = umma_idesc(64, 64, false, false);  // Gm x X^T
+    constexpr uint32_t kIdU = umma_idesc(NS, 64, false, false);   // B x W^T
+    constexpr uint32_t kSBlk = kSsdP * 128;                       // bytes of one 64-column state block
+
+    __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
+    __nv_bfloat16* yt = &sm.Wh[0][0];  // output staging [p][kSsdYPitch], over the W buffers
+    const bool vec_ok = (L & 7) == 0;
+    const int l0 = 16 * q + (lane >> 2), l1 = l0 + 8;  // this thread's rows in the M = 64 products
+    const int cp = 2 * (lane & 3);                     // and its column pair in each group of 8
 
     // A wait that runs out sets `timed_out`; the chunk is finished with
     // whatever the tiles hold and the kernel leaves at the chunk's last
@@ -254,217 +318,203 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         const uint32_t par = static_cast<uint32_t>(k & 1);
         const float* c2 = sm.c2[k & 1];
         const float* dtv = sm.dt[k & 1];
-        if (!mbar_wait_bounded(&sm.full[2], par)) timed_out = true;  // C
-
-        // --- C S^T (carried state) for this warp's two row blocks and channel quarter ---
-        float Y[2][2][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) Y[r][j][e] = 0.f;
+        const float* wq = sm.wq[k & 1];
         const bool carry = have_state || k > 0;
-        if (carry) {
+
+        // --- G = C^T B and Y1 = C^T S^T as soon as C and B are in ---
+        if (tid == 0) {
+            if (!mbar_wait_bounded(&sm.full[2], par)) timed_out = true;
+            if (!mbar_wait_bounded(&sm.full[1], par)) timed_out = true;
+            tc_fence_after();
 #pragma unroll
-            for (int k0 = 0; k0 < NS; k0 += 16) {
-                uint32_t af[2][4], bh[4], bl[4];  // A = C^T rows from Ct[n][l]; B = S^T from Sh/Sl[p][n]
-                ldsm_x4_t(a_y[0] + k0 * 128, af[0]);
-                ldsm_x4_t(a_y[1] + k0 * 128, af[1]);
-                ldsm_x4(smem_u32(&sm.Sh[16 * pq + ra][k0 + 8 * (mi & 1)]), bh);
-                ldsm_x4(smem_u32(&sm.Sl[16 * pq + ra][k0 + 8 * (mi & 1)]), bl);
+            for (int kk = 0; kk < NS / 16; ++kk) umma(tG, desc_mn(cs + kk * 2048), desc_mn(bs + kk * 2048), kIdG, kk > 0);
+            umma_commit(&sm.done[0]);
+            if (carry) {
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    mma_bf16(Y[r][0], af[r], bh[0], bh[1]);
-                    mma_bf16(Y[r][1], af[r], bh[2], bh[3]);
-                }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    mma_bf16(Y[r][0], af[r], bl[0], bl[1]);
-                    mma_bf16(Y[r][1], af[r], bl[2], bl[3]);
+                for (int kk = 0; kk < NS / 16; ++kk) {
+                    const uint32_t so = (kk >> 2) * kSBlk + (kk & 3) * 32;
+                    umma(tY1, desc_mn(cs + kk * 2048), desc_k(shs + so), kIdY1, kk > 0);
+                    umma(tY1, desc_mn(cs + kk * 2048), desc_k(sls + so), kIdY1, true);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const float e0 = ex2_approx(c2[16 * yrb[r] + g]), e1 = ex2_approx(c2[16 * yrb[r] + g + 8]);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) { Y[r][j][0] *= e0; Y[r][j][1] *= e0; Y[r][j][2] *= e1; Y[r][j][3] *= e1; }
-            }
+            umma_commit(&sm.done[1]);
         }
-        if (!mbar_wait_bounded(&sm.full[1], par)) timed_out = true;  // B
-        // --- C B^T over this warp's units of the causal triangle, masked and weighted ---
+        __syncwarp();
+
+        // --- W = x e^{c_Q - c_s} dt_s, split: thread = channel p, 16 steps ---
+        if (!mbar_wait_bounded(&sm.full[0], par)) timed_out = true;
         {
-            float G[3][4];
-            int urb[3], ucol[3];  // row block and first column of each unit
+            const int p = tid >> 2;
+            const unsigned char* xb = reinterpret_cast<const unsigned char*>(&sm.X[0][0]);
+            unsigned char* whb = reinterpret_cast<unsigned char*>(&sm.Wh[0][0]);
+            unsigned char* wlb = reinterpret_cast<unsigned char*>(&sm.Wl[0][0]);
 #pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                // unit u -> (row block, column block, half): u = rb (rb + 1) + 2 sb + nt
-                const int u = warp + 8 * i;
-                const int rbu = u < 2 ? 0 : (u < 6 ? 1 : (u < 12 ? 2 : 3));
-                const int rem = u - rbu * (rbu + 1);
-                urb[i] = rbu;
-                ucol[i] = 8 * rem;            // 16 sb + 8 nt
-#pragma unroll
-                for (int e = 0; e < 4; ++e) G[i][e] = 0.f;
-            }
-#pragma unroll
-            for (int k0 = 0; k0 < NS; k0 += 16) {
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    if (warp + 8 * i < 20) {
-                        uint32_t af[4], bf[2];
-                        ldsm_x4_t(ct + (k0 + ra) * 128 + (((2 * urb[i] + (mi & 1)) ^ (ra & 7)) << 4), af);
-                        ldsm_x2_t(bt + (k0 + krow) * 128 + (((ucol[i] >> 3) ^ (krow & 7)) << 4), bf);
-                        mma_bf16(G[i], af, bf[0], bf[1]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                if (warp + 8 * i < 20) {
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int l = 16 * urb[i] + g + 8 * hf;
-                        const float cl = c2[l];
-                        float v[2];
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int sc = ucol[i] + 2 * tq + c;
-                            v[c] = sc <= l ? G[i][2 * hf + c] * ex2_approx(cl - c2[sc]) * dtv[sc] : 0.f;
-                        }
-                        uint32_t hi, lo;
-                        split2(v[0], v[1], hi, lo);
-                        *reinterpret_cast<uint32_t*>(&sm.Oh[l][ucol[i] + 2 * tq]) = hi;
-                        *reinterpret_cast<uint32_t*>(&sm.Ol[l][ucol[i] + 2 * tq]) = lo;
-                    }
-                }
+            for (int i = 0; i < 2; ++i) {
+                const int u = 2 * (tid & 3) + i;  // 16-byte unit: steps 8u .. 8u + 7
+                const int off = p * 128 + ((u ^ (p & 7)) << 4);
+                const uint4 xv = *reinterpret_cast<const uint4*>(xb + off);
+                const float4 w0 = *reinterpret_cast<const float4*>(&wq[8 * u]);
+                const float4 w1 = *reinterpret_cast<const float4*>(&wq[8 * u + 4]);
+                const float2 x0 = bf2_to_f2(xv.x), x1 = bf2_to_f2(xv.y), x2 = bf2_to_f2(xv.z), x3 = bf2_to_f2(xv.w);
+                uint4 hi, lo;
+                split2(x0.x * w0.x, x0.y * w0.y, hi.x, lo.x);
+                split2(x1.x * w0.z, x1.y * w0.w, hi.y, lo.y);
+                split2(x2.x * w1.x, x2.y * w1.y, hi.z, lo.z);
+                split2(x3.x * w1.z, x3.y * w1.w, hi.w, lo.w);
+                *reinterpret_cast<uint4*>(whb + off) = hi;
+                *reinterpret_cast<uint4*>(wlb + off) = lo;
             }
         }
-        __syncthreads();  // every unit of the triangle is in; C is consumed
-        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
-            fence_proxy_async_smem();
-            issue(2, k + 1);
-        }
-        if (!mbar_wait_bounded(&sm.full[0], par)) timed_out = true;  // x
-        // --- Y += (masked C B^T) X^T over s < 16 (row block + 1) ---
+
+        // --- Gm = G e^{c_l - c_s} dt_s on and below the diagonal, split ---
+        if (!mbar_wait_bounded(&sm.done[0], par)) timed_out = true;
+        tc_fence_after();
+        if (32 * half <= 16 * q + 15) {  // (the warp's block has steps s <= l)
+            uint32_t g[4][4];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+            for (int j = 0; j < 4; ++j) tmem_ld_16x256b(tG + lane_base + 32 * half + 8 * j, g[j]);
+            tmem_wait_ld();
+            const float cl0 = c2[l0], cl1 = c2[l1];
+            unsigned char* ghb = reinterpret_cast<unsigned char*>(&sm.Gh[0][0]);
+            unsigned char* glb = reinterpret_cast<unsigned char*>(&sm.Gl[0][0]);
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-                if (kb <= yrb[r]) {
-                    uint32_t ah[4], al[4], bx[4];
-                    const int arow = 16 * yrb[r] + rc, acol = 16 * kb + 8 * (mi >> 1);
-                    ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
-                    ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
-                    ldsm_x4(x_q + (((2 * kb + (mi & 1)) ^ sw) << 4), bx);  // B = X^T from X[p][s]
-                    mma_bf16(Y[r][0], ah, bx[0], bx[1]);
-                    mma_bf16(Y[r][1], ah, bx[2], bx[3]);
-                    mma_bf16(Y[r][0], al, bx[0], bx[1]);
-                    mma_bf16(Y[r][1], al, bx[2], bx[3]);
-                }
-            }
-        }
-        __syncthreads();  // every warp is done with the masked rows: the O buffers take the weighted x
-        // --- outputs (+ D x) into Yt; decay-weighted x into the O buffers ---
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int l = 16 * yrb[r] + g + 8 * (e >> 1), p = 16 * pq + 8 * j + 2 * tq + (e & 1);
-                    sm.Yt[p][l] = Y[r][j][e] + Dh * swz_ld(&sm.X[0][0], p, l);
-                }
-            }
-        }
-        const float clast = c2[kSsdQ - 1];
-        {
-            const int p = m0 + (lane >> 1);
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const int sc = c0 + 16 * (lane & 1) + i;
-                const float w0 = ex2_approx(clast - c2[sc]) * dtv[sc];
-                const float w1 = ex2_approx(clast - c2[sc + 1]) * dtv[sc + 1];
+            for (int j = 0; j < 4; ++j) {
+                const int s = 32 * half + 8 * j + cp;
+                const float2 cs2 = *reinterpret_cast<const float2*>(&c2[s]);
+                const float2 ds = *reinterpret_cast<const float2*>(&dtv[s]);
+                const float v00 = s <= l0 ? __uint_as_float(g[j][0]) * ex2_approx(cl0 - cs2.x) * ds.x : 0.f;
+                const float v01 = s + 1 <= l0 ? __uint_as_float(g[j][1]) * ex2_approx(cl0 - cs2.y) * ds.y : 0.f;
+                const float v10 = s <= l1 ? __uint_as_float(g[j][2]) * ex2_approx(cl1 - cs2.x) * ds.x : 0.f;
+                const float v11 = s + 1 <= l1 ? __uint_as_float(g[j][3]) * ex2_approx(cl1 - cs2.y) * ds.y : 0.f;
                 uint32_t hi, lo;
-                split2(swz_ld(&sm.X[0][0], p, sc) * w0, swz_ld(&sm.X[0][0], p, sc + 1) * w1, hi, lo);
-                *reinterpret_cast<uint32_t*>(&sm.Oh[p][sc]) = hi;
-                *reinterpret_cast<uint32_t*>(&sm.Ol[p][sc]) = lo;
+                split2(v00, v01, hi, lo);
+                *reinterpret_cast<uint32_t*>(ghb + swz(l0, s)) = hi;
+                *reinterpret_cast<uint32_t*>(glb + swz(l0, s)) = lo;
+                split2(v10, v11, hi, lo);
+                *reinterpret_cast<uint32_t*>(ghb + swz(l1, s)) = hi;
+                *reinterpret_cast<uint32_t*>(glb + swz(l1, s)) = lo;
             }
         }
-        __syncthreads();  // Yt and the weighted x complete; x is consumed
-        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
-            fence_proxy_async_smem();
-            issue(0, k + 1);
+        fence_proxy_async_smem();  // W and Gm, for the tensor cores
+        tc_fence_before();
+        __syncthreads();
+
+        // --- Y2 = Gm X^T and U = B W^T; C is reloaded once G and Y1 are done ---
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kSsdQ / 16; ++kk) {
+                umma(tY2, desc_k(ghs + kk * 32), desc_k(xs + kk * 32), kIdY2, kk > 0);
+                umma(tY2, desc_k(gls + kk * 32), desc_k(xs + kk * 32), kIdY2, true);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kSsdQ / 16; ++kk) {
+                umma(tU, desc_k(bs + kk * 32), desc_k(whs + kk * 32), kIdU, kk > 0);
+                umma(tU, desc_k(bs + kk * 32), desc_k(wls + kk * 32), kIdU, true);
+            }
+            umma_commit(&sm.done[2]);
+            if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;
+            if (k + 1 < n && !timed_out) issue(2, k + 1);
         }
-        if (warp == 0 && k + 1 < n) decay_prefix(k + 1);  // the next chunk's dt and decay, other buffer
+        __syncwarp();
+
+        // --- outputs y = e^{c_l} Y1 + Y2 + D x, staged as bf16 [p][l] over W ---
+        if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;
+        if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // Y2 and U (W is free)
+        tc_fence_after();
+        {
+            uint32_t y1[4][4], y2[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld_16x256b(tY2 + lane_base + 32 * half + 8 * j, y2[j]);
+            if (carry) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld_16x256b(tY1 + lane_base + 32 * half + 8 * j, y1[j]);
+            }
+            tmem_wait_ld();
+            const float e0 = carry ? ex2_approx(c2[l0]) : 0.f, e1 = carry ? ex2_approx(c2[l1]) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = 32 * half + 8 * j + cp;
+                float v00 = __uint_as_float(y2[j][0]) + Dh * swz_ld(&sm.X[0][0], p, l0);
+                float v01 = __uint_as_float(y2[j][1]) + Dh * swz_ld(&sm.X[0][0], p + 1, l0);
+                float v10 = __uint_as_float(y2[j][2]) + Dh * swz_ld(&sm.X[0][0], p, l1);
+                float v11 = __uint_as_float(y2[j][3]) + Dh * swz_ld(&sm.X[0][0], p + 1, l1);
+                if (carry) {
+                    v00 = fmaf(e0, __uint_as_float(y1[j][0]), v00);
+                    v01 = fmaf(e0, __uint_as_float(y1[j][1]), v01);
+                    v10 = fmaf(e1, __uint_as_float(y1[j][2]), v10);
+                    v11 = fmaf(e1, __uint_as_float(y1[j][3]), v11);
+                }
+                yt[p * kSsdYPitch + l0] = __float2bfloat16_rn(v00);
+                yt[(p + 1) * kSsdYPitch + l0] = __float2bfloat16_rn(v01);
+                yt[p * kSsdYPitch + l1] = __float2bfloat16_rn(v10);
+                yt[(p + 1) * kSsdYPitch + l1] = __float2bfloat16_rn(v11);
+            }
+        }
+
+        // --- state: S = e^{c_Q} S + U, split into the next chunk's operand ---
+        {
+            uint32_t u[2][16];
+            tmem_ld_32x32b_x16(tU + lane_base + 32 * half, u[0]);
+            tmem_ld_32x32b_x16(tU + lane_base + 32 * half + 16, u[1]);
+            tmem_wait_ld();
+            const float ed = ex2_approx(c2[kSsdQ - 1]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[j] = fmaf(ed, S[j], __uint_as_float(u[j >> 4][j & 15]));
+        }
+        store_state_parts();  // (the Y1 product, the parts' last reader, is done)
+        tc_fence_before();
+        __syncthreads();  // the staging tile is complete
+
         // y rows of the head's 64 channels, 8 steps per store
 #pragma unroll
         for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
             const int p = v >> 3, lc = (v & 7) * 8, gl = k * kSsdQ + lc;
             if (gl >= L) continue;
             __nv_bfloat16* dst = yb + static_cast<size_t>(p) * L + gl;
-            const float* src = &sm.Yt[p][lc];
+            const __nv_bfloat16* src = yt + p * kSsdYPitch + lc;
             if (vec_ok && gl + 8 <= L) {
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const __nv_bfloat162 o = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
-                    w[q] = *reinterpret_cast<const uint32_t*>(&o);
-                }
-                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
             } else {
-                for (int q = 0; q < 8 && gl + q < L; ++q) dst[q] = __float2bfloat16_rn(src[q]);
+                for (int i = 0; i < 8 && gl + i < L; ++i) dst[i] = src[i];
             }
         }
-        // --- state: S = e^{c_Q} S + (weighted x) B^T: rows m0.., this warp's state half ---
-        const float ed = ex2_approx(clast);
-#pragma unroll
-        for (int j = 0; j < kNH; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) S[j][e] *= ed;
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-            uint32_t ah[4], al[4], bb[kNH / 2][4];
-            const int arow = m0 + rr + ((mi & 1) << 3), acol = 16 * kb + 8 * (mi >> 1);
-            ldsm_x4(smem_u32(&sm.Oh[arow][acol]), ah);
-            ldsm_x4(smem_u32(&sm.Ol[arow][acol]), al);
-#pragma unroll
-            for (int jp = 0; jp < kNH / 2; ++jp)  // B = Bt^T from Bt[n][s]
-                ldsm_x4(b_row + jp * 16 * 128 + (((2 * kb + (mi & 1)) ^ sw) << 4), bb[jp]);
-#pragma unroll
-            for (int jp = 0; jp < kNH / 2; ++jp) {
-                mma_bf16(S[2 * jp], ah, bb[jp][0], bb[jp][1]);
-                mma_bf16(S[2 * jp + 1], ah, bb[jp][2], bb[jp][3]);
-            }
-#pragma unroll
-            for (int jp = 0; jp < kNH / 2; ++jp) {
-                mma_bf16(S[2 * jp], al, bb[jp][0], bb[jp][1]);
-                mma_bf16(S[2 * jp + 1], al, bb[jp][2], bb[jp][3]);
-            }
-        }
-        store_state_parts();
-        // state parts and the next chunk's decay complete; B is consumed
+        if (warp == 0 && k + 1 < n) decay_prefix(k + 1);  // the next chunk's dt and decay, other buffer
+        fence_proxy_async_smem();  // the state parts, for the next chunk's Y1 product
+        tc_fence_before();
+        // the staging tile is read out; x and B are consumed
         if (__syncthreads_or(timed_out)) {
-            if (tid == 0) { report_device_error(a.err, -6); drain(); }
+            if (tid == 0) {
+                report_device_error(a.err, -6);
+                drain();
+                for (int i = 0; i < 3; ++i) mbar_wait_bounded(&sm.done[i], par);  // this chunk's products
+            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (warp == 0)
+                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kSsdTmemCols)
+                             : "memory");
             return;
         }
-        if (tid == 0 && k + 1 < n && !timed_out) {  // (never refill a tile whose load may be in flight)
+        tc_fence_after();
+        if (tid == 0 && k + 1 < n) {
             fence_proxy_async_smem();
             issue(1, k + 1);
+            issue(0, k + 1);
         }
+        __syncwarp();
     }
 
-    if (a.final_state) {
+    if (a.final_state && sact) {
 #pragma unroll
-        for (int j = 0; j < kNH; ++j) {
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int p = m0 + g + 8 * hf, c = n0 + 8 * j + 2 * tq;
-                *reinterpret_cast<float2*>(a.final_state + (head_row * kSsdP + p) * NS + c) =
-                    make_float2(S[j][2 * hf], S[j][2 * hf + 1]);
-            }
-        }
+        for (int j = 0; j < 32; ++j) a.final_state[(head_row * kSsdP + 32 * half + j) * NS + sn] = S[j];
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kSsdTmemCols) : "memory");
 }
 
 }  // namespace mscan
