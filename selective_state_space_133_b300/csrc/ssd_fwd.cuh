@@ -32,12 +32,15 @@
 // the next chunk's operand. Two CTAs share an SM (104 KB of shared memory and
 // 256 TMEM columns each), so one's elementwise work overlaps the other's
 // contractions and loads. Per chunk: thread 0 issues G and Y1 as soon as C and
-// B are in; meanwhile every thread forms W; then Gm from G (tcgen05.ld, mask,
-// weights, split); barrier; thread 0 issues Y2 and U; every thread forms the
-// outputs y = e^{c_l} Y1 + Y2 + D x (staged in shared memory for 16-byte row
-// stores) and the new state. The x, B and C tiles arrive by 3-D TMA (128-byte
-// swizzle) on their own barriers and are refilled for the next chunk as soon
-// as the contractions reading them are done. Steps past the end of the
+// B are in; every thread forms W; barrier; thread 0 issues U while every
+// thread forms Gm from G (tcgen05.ld, mask, decay weights, split), with D_h
+// added on its diagonal so that Y2 = Gm X^T carries the skip term D x;
+// barrier; thread 0 issues Y2 and reloads the B, C and x tiles for the next
+// chunk as soon as the products reading them are done; every thread forms the
+// outputs y = e^{c_l} Y1 + Y2 (staged in shared memory and stored, 16 bytes a
+// row piece, at the start of the next chunk) and the new state; barrier. The
+// tiles arrive by 3-D TMA (128-byte swizzle) on their own barriers, so their
+// loads overlap the second half of the previous chunk. Steps past the end of the
 // sequence get dt = 0, so they leave the state unchanged. Every wait is
 // bounded: a wait that runs out is reported through the device error word,
 // the chunk finishes and the kernel leaves with its tensor memory freed.
@@ -74,12 +77,12 @@ struct SsdSmem {
     alignas(1024) __nv_bfloat16 X[kSsdP][kSsdQ];   // x [p][s]            (TMA)
     alignas(1024) __nv_bfloat16 Bt[NS][kSsdQ];     // B [n][s]            (TMA)
     alignas(1024) __nv_bfloat16 Ct[NS][kSsdQ];     // C [n][l]            (TMA)
-    alignas(1024) __nv_bfloat16 Gh[kSsdQ][kSsdQ];  // Gm [l][s], high part
-    alignas(1024) __nv_bfloat16 Gl[kSsdQ][kSsdQ];  //            low part
-    // W [p][s] high and low parts; once the U product is done, the staging
+    // Gm [l][s] high and low parts; once the Y2 product is done, the staging
     // tile of the chunk's outputs y [p][l] (bf16, pitch kSsdYPitch)
-    alignas(1024) __nv_bfloat16 Wh[kSsdP][kSsdQ];
-    alignas(1024) __nv_bfloat16 Wl[kSsdP][kSsdQ];
+    alignas(1024) __nv_bfloat16 Gh[kSsdQ][kSsdQ];
+    alignas(1024) __nv_bfloat16 Gl[kSsdQ][kSsdQ];
+    alignas(1024) __nv_bfloat16 Wh[kSsdP][kSsdQ];  // W [p][s], high part
+    alignas(1024) __nv_bfloat16 Wl[kSsdP][kSsdQ];  //           low part
     // carried state [p][n] high and low parts, in 64-column blocks [n / 64][p][n % 64]
     alignas(1024) __nv_bfloat16 Sh[NS / 64][kSsdP][64];
     alignas(1024) __nv_bfloat16 Sl[NS / 64][kSsdP][64];
@@ -87,10 +90,10 @@ struct SsdSmem {
     alignas(16) float dt[2][kSsdQ];
     alignas(16) float wq[2][kSsdQ];  // e^{c_Q - c_s} dt_s
     alignas(8) uint64_t full[3];     // TMA: x, B, C
-    alignas(8) uint64_t done[4];     // MMA completion: G, Y1, Y2, U
+    alignas(8) uint64_t done[4];     // MMA completion: G, Y1, U, Y2 (each also covers the earlier ones)
     uint32_t tmem;                   // base address of this CTA's tensor memory
 };
-static_assert(kSsdP * kSsdYPitch * 2 <= 2 * kSsdP * kSsdQ * 2, "the y staging tile fits in the W buffers");
+static_assert(kSsdP * kSsdYPitch * 2 <= 2 * kSsdQ * kSsdQ * 2, "the y staging tile fits in the Gm buffers");
 
 // ------------------------------------------------------------ helpers ------
 
@@ -218,7 +221,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     };
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&sm.full[i], 1);
-        for (int i = 0; i < 3; ++i) mbar_init(&sm.done[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.done[i], 1);
         fence_barrier_init();
         if (n > 0) { issue(2, 0); issue(1, 0); issue(0, 0); }
     }
@@ -248,12 +251,6 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         }
     };
     if (have_state) store_state_parts();
-    // Gm is zero above the diagonal; those blocks are never written again
-    for (int i = tid; i < kSsdQ * kSsdQ * 2 / 16; i += kSsdThreads) {
-        reinterpret_cast<uint4*>(&sm.Gh[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(&sm.Gl[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
-
     // dt, the cumulative decay and the state-update weights of chunk k into
     // buffer k & 1 (warp 0); padding steps get dt = 0
     const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(a.delta) + head_row * L;
@@ -286,7 +283,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         sm.wq[k & 1][2 * lane + 1] = ex2_approx(cq - c1) * d[1];
     };
     if (warp == 0 && n > 0) decay_prefix(0);
-    fence_proxy_async_smem();  // the state parts and the zeros, for the tensor cores
+    fence_proxy_async_smem();  // the state parts, for the tensor cores
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -303,11 +300,29 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     constexpr uint32_t kIdU = umma_idesc(NS, 64, false, false);   // B x W^T
     constexpr uint32_t kSBlk = kSsdP * 128;                       // bytes of one 64-column state block
 
+
     __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
-    __nv_bfloat16* yt = &sm.Wh[0][0];  // output staging [p][kSsdYPitch], over the W buffers
+    // Output staging [p][kSsdYPitch] over the Gm buffers: written once the
+    // masked product is done, stored to HBM at the start of the next chunk.
+    __nv_bfloat16* yt = &sm.Gh[0][0];
     const bool vec_ok = (L & 7) == 0;
     const int l0 = 16 * q + (lane >> 2), l1 = l0 + 8;  // this thread's rows in the M = 64 products
     const int cp = 2 * (lane & 3);                     // and its column pair in each group of 8
+    // y rows of the head's 64 channels for chunk k, 8 steps per store
+    auto store_y = [&](int k) {
+#pragma unroll
+        for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
+            const int p = v >> 3, lc = (v & 7) * 8, gl = k * kSsdQ + lc;
+            if (gl >= L) continue;
+            __nv_bfloat16* dst = yb + static_cast<size_t>(p) * L + gl;
+            const __nv_bfloat16* src = yt + p * kSsdYPitch + lc;
+            if (vec_ok && gl + 8 <= L) {
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+            } else {
+                for (int i = 0; i < 8 && gl + i < L; ++i) dst[i] = src[i];
+            }
+        }
+    };
 
     // A wait that runs out sets `timed_out`; the chunk is finished with
     // whatever the tiles hold and the kernel leaves at the chunk's last
@@ -340,6 +355,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             umma_commit(&sm.done[1]);
         }
         __syncwarp();
+        if (k > 0) store_y(k - 1);
 
         // --- W = x e^{c_Q - c_s} dt_s, split: thread = channel p, 16 steps ---
         if (!mbar_wait_bounded(&sm.full[0], par)) timed_out = true;
@@ -365,41 +381,72 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 *reinterpret_cast<uint4*>(wlb + off) = lo;
             }
         }
+        fence_proxy_async_smem();  // W, for the tensor cores
+        tc_fence_before();
+        __syncthreads();  // W is complete; the staging tile is read out
 
-        // --- Gm = G e^{c_l - c_s} dt_s on and below the diagonal, split ---
+        // --- U = B W^T, while the masked operand is formed ---
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kSsdQ / 16; ++kk) {
+                umma(tU, desc_k(bs + kk * 32), desc_k(whs + kk * 32), kIdU, kk > 0);
+                umma(tU, desc_k(bs + kk * 32), desc_k(wls + kk * 32), kIdU, true);
+            }
+            umma_commit(&sm.done[2]);
+        }
+        __syncwarp();
+
+        // --- Gm = G e^{c_l - c_s} dt_s for s <= l, plus D on the diagonal
+        //     (so that Y2 carries the skip term D x), split ---
         if (!mbar_wait_bounded(&sm.done[0], par)) timed_out = true;
         tc_fence_after();
-        if (32 * half <= 16 * q + 15) {  // (the warp's block has steps s <= l)
-            uint32_t g[4][4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_16x256b(tG + lane_base + 32 * half + 8 * j, g[j]);
-            tmem_wait_ld();
-            const float cl0 = c2[l0], cl1 = c2[l1];
+        {
             unsigned char* ghb = reinterpret_cast<unsigned char*>(&sm.Gh[0][0]);
             unsigned char* glb = reinterpret_cast<unsigned char*>(&sm.Gl[0][0]);
+            if (32 * half <= 16 * q + 15) {  // (the warp's block has steps s <= l)
+                uint32_t g[4][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int s = 32 * half + 8 * j + cp;
-                const float2 cs2 = *reinterpret_cast<const float2*>(&c2[s]);
-                const float2 ds = *reinterpret_cast<const float2*>(&dtv[s]);
-                const float v00 = s <= l0 ? __uint_as_float(g[j][0]) * ex2_approx(cl0 - cs2.x) * ds.x : 0.f;
-                const float v01 = s + 1 <= l0 ? __uint_as_float(g[j][1]) * ex2_approx(cl0 - cs2.y) * ds.y : 0.f;
-                const float v10 = s <= l1 ? __uint_as_float(g[j][2]) * ex2_approx(cl1 - cs2.x) * ds.x : 0.f;
-                const float v11 = s + 1 <= l1 ? __uint_as_float(g[j][3]) * ex2_approx(cl1 - cs2.y) * ds.y : 0.f;
-                uint32_t hi, lo;
-                split2(v00, v01, hi, lo);
-                *reinterpret_cast<uint32_t*>(ghb + swz(l0, s)) = hi;
-                *reinterpret_cast<uint32_t*>(glb + swz(l0, s)) = lo;
-                split2(v10, v11, hi, lo);
-                *reinterpret_cast<uint32_t*>(ghb + swz(l1, s)) = hi;
-                *reinterpret_cast<uint32_t*>(glb + swz(l1, s)) = lo;
+                for (int j = 0; j < 4; ++j) tmem_ld_16x256b(tG + lane_base + 32 * half + 8 * j, g[j]);
+                tmem_wait_ld();
+                const float cl0 = c2[l0], cl1 = c2[l1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int s = 32 * half + 8 * j + cp;
+                    const float2 cs2 = *reinterpret_cast<const float2*>(&c2[s]);
+                    const float2 ds = *reinterpret_cast<const float2*>(&dtv[s]);
+                    float v00 = s <= l0 ? __uint_as_float(g[j][0]) * ex2_approx(cl0 - cs2.x) * ds.x : 0.f;
+                    float v01 = s + 1 <= l0 ? __uint_as_float(g[j][1]) * ex2_approx(cl0 - cs2.y) * ds.y : 0.f;
+                    float v10 = s <= l1 ? __uint_as_float(g[j][2]) * ex2_approx(cl1 - cs2.x) * ds.x : 0.f;
+                    float v11 = s + 1 <= l1 ? __uint_as_float(g[j][3]) * ex2_approx(cl1 - cs2.y) * ds.y : 0.f;
+                    if (s == l0) v00 += Dh;
+                    if (s + 1 == l0) v01 += Dh;
+                    if (s == l1) v10 += Dh;
+                    if (s + 1 == l1) v11 += Dh;
+                    uint32_t hi, lo;
+                    split2(v00, v01, hi, lo);
+                    *reinterpret_cast<uint32_t*>(ghb + swz(l0, s)) = hi;
+                    *reinterpret_cast<uint32_t*>(glb + swz(l0, s)) = lo;
+                    split2(v10, v11, hi, lo);
+                    *reinterpret_cast<uint32_t*>(ghb + swz(l1, s)) = hi;
+                    *reinterpret_cast<uint32_t*>(glb + swz(l1, s)) = lo;
+                }
+            } else {  // above the diagonal (the staging tile overwrote it)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int s = 32 * half + 8 * j + cp;
+                    *reinterpret_cast<uint32_t*>(ghb + swz(l0, s)) = 0u;
+                    *reinterpret_cast<uint32_t*>(glb + swz(l0, s)) = 0u;
+                    *reinterpret_cast<uint32_t*>(ghb + swz(l1, s)) = 0u;
+                    *reinterpret_cast<uint32_t*>(glb + swz(l1, s)) = 0u;
+                }
             }
         }
-        fence_proxy_async_smem();  // W and Gm, for the tensor cores
+        fence_proxy_async_smem();  // Gm, for the tensor cores
         tc_fence_before();
         __syncthreads();
 
-        // --- Y2 = Gm X^T and U = B W^T; C is reloaded once G and Y1 are done ---
+        // --- Y2 = Gm X^T; B and C are reloaded for the next chunk once free ---
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -407,21 +454,24 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 umma(tY2, desc_k(ghs + kk * 32), desc_k(xs + kk * 32), kIdY2, kk > 0);
                 umma(tY2, desc_k(gls + kk * 32), desc_k(xs + kk * 32), kIdY2, true);
             }
-#pragma unroll
-            for (int kk = 0; kk < kSsdQ / 16; ++kk) {
-                umma(tU, desc_k(bs + kk * 32), desc_k(whs + kk * 32), kIdU, kk > 0);
-                umma(tU, desc_k(bs + kk * 32), desc_k(wls + kk * 32), kIdU, true);
+            umma_commit(&sm.done[3]);
+            if (k + 1 < n) {
+                if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // G and U: B is free
+                if (!timed_out) issue(1, k + 1);
+                if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;  // G and Y1: C is free
+                if (!timed_out) issue(2, k + 1);
             }
-            umma_commit(&sm.done[2]);
-            if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;
-            if (k + 1 < n && !timed_out) issue(2, k + 1);
         }
         __syncwarp();
 
-        // --- outputs y = e^{c_l} Y1 + Y2 + D x, staged as bf16 [p][l] over W ---
-        if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;
-        if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // Y2 and U (W is free)
+        // --- outputs y = e^{c_l} Y1 + Y2, staged as bf16 [p][l] over Gm ---
+        if (!mbar_wait_bounded(&sm.done[3], par)) timed_out = true;  // every product of the chunk
         tc_fence_after();
+        if (tid == 0 && k + 1 < n && !timed_out) {  // x is free
+            fence_proxy_async_smem();
+            issue(0, k + 1);
+        }
+        __syncwarp();
         {
             uint32_t y1[4][4], y2[4][4];
 #pragma unroll
@@ -435,10 +485,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int p = 32 * half + 8 * j + cp;
-                float v00 = __uint_as_float(y2[j][0]) + Dh * swz_ld(&sm.X[0][0], p, l0);
-                float v01 = __uint_as_float(y2[j][1]) + Dh * swz_ld(&sm.X[0][0], p + 1, l0);
-                float v10 = __uint_as_float(y2[j][2]) + Dh * swz_ld(&sm.X[0][0], p, l1);
-                float v11 = __uint_as_float(y2[j][3]) + Dh * swz_ld(&sm.X[0][0], p + 1, l1);
+                float v00 = __uint_as_float(y2[j][0]), v01 = __uint_as_float(y2[j][1]);
+                float v10 = __uint_as_float(y2[j][2]), v11 = __uint_as_float(y2[j][3]);
                 if (carry) {
                     v00 = fmaf(e0, __uint_as_float(y1[j][0]), v00);
                     v01 = fmaf(e0, __uint_as_float(y1[j][1]), v01);
@@ -463,31 +511,15 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             for (int j = 0; j < 32; ++j) S[j] = fmaf(ed, S[j], __uint_as_float(u[j >> 4][j & 15]));
         }
         store_state_parts();  // (the Y1 product, the parts' last reader, is done)
-        tc_fence_before();
-        __syncthreads();  // the staging tile is complete
-
-        // y rows of the head's 64 channels, 8 steps per store
-#pragma unroll
-        for (int v = tid; v < kSsdP * (kSsdQ / 8); v += kSsdThreads) {
-            const int p = v >> 3, lc = (v & 7) * 8, gl = k * kSsdQ + lc;
-            if (gl >= L) continue;
-            __nv_bfloat16* dst = yb + static_cast<size_t>(p) * L + gl;
-            const __nv_bfloat16* src = yt + p * kSsdYPitch + lc;
-            if (vec_ok && gl + 8 <= L) {
-                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-            } else {
-                for (int i = 0; i < 8 && gl + i < L; ++i) dst[i] = src[i];
-            }
-        }
         if (warp == 0 && k + 1 < n) decay_prefix(k + 1);  // the next chunk's dt and decay, other buffer
         fence_proxy_async_smem();  // the state parts, for the next chunk's Y1 product
         tc_fence_before();
-        // the staging tile is read out; x and B are consumed
+        // the staging tile, the state parts and the next chunk's decay are complete
         if (__syncthreads_or(timed_out)) {
             if (tid == 0) {
                 report_device_error(a.err, -6);
                 drain();
-                for (int i = 0; i < 3; ++i) mbar_wait_bounded(&sm.done[i], par);  // this chunk's products
+                for (int i = 0; i < 4; ++i) mbar_wait_bounded(&sm.done[i], par);  // this chunk's products
             }
             tc_fence_before();
             __syncthreads();
@@ -498,13 +530,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             return;
         }
         tc_fence_after();
-        if (tid == 0 && k + 1 < n) {
-            fence_proxy_async_smem();
-            issue(1, k + 1);
-            issue(0, k + 1);
-        }
-        __syncwarp();
     }
+    if (n > 0) store_y(n - 1);
 
     if (a.final_state && sact) {
 #pragma unroll
