@@ -31,11 +31,11 @@
 // channels), updated from U as S = e^{c_Q} S + U and written back, split, as
 // the next chunk's operand. Two CTAs share an SM (104 KB of shared memory and
 // 256 TMEM columns each), so one's elementwise work overlaps the other's
-// contractions and loads. Per chunk: thread 0 issues G and Y1 as soon as C and
-// B are in; every thread forms W; barrier; thread 0 issues U while every
+// contractions and loads. Per chunk: one thread issues G and Y1 as soon as C and
+// B are in; every thread forms W; barrier; it issues U while every
 // thread forms Gm from G (tcgen05.ld, mask, decay weights, split), with D_h
 // added on its diagonal so that Y2 = Gm X^T carries the skip term D x;
-// barrier; thread 0 issues Y2 and reloads the B, C and x tiles for the next
+// barrier; it issues Y2 and reloads the B, C and x tiles for the next
 // chunk as soon as the products reading them are done; every thread forms the
 // outputs y = e^{c_l} Y1 + Y2 (staged in shared memory and stored, 16 bytes a
 // row piece, at the start of the next chunk) and the new state; barrier. The
@@ -184,6 +184,10 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const int q = warp & 3;      // the TMEM lane quarter this warp may access
     const int half = warp >> 2;  // its half (32 columns) of every per-chunk product
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    // Warps 4 and 5 own blocks of Gm that lie above the diagonal (no TMEM
+    // read, no mask arithmetic), so they take the serial work: thread 0 of
+    // warp 4 issues the loads and the MMAs, warp 5 forms each chunk's decay.
+    constexpr int kIssuer = 128, kDecayWarp = 5;
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = a.seqlen;
     const int n = (L + kSsdQ - 1) / kSsdQ;
@@ -200,7 +204,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // tile loads of chunk k (thread 0): barrier 0 = x, 1 = B, 2 = C; parity k & 1
+    // tile loads of chunk k (the issuing thread): barrier 0 = x, 1 = B, 2 = C; parity k & 1
     int last[3] = {-1, -1, -1};
     auto issue = [&](int which, int k) {
         uint64_t* bar = &sm.full[which];
@@ -219,7 +223,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         for (int i = 0; i < 3; ++i)
             if (last[i] >= 0) mbar_wait_bounded(&sm.full[i], static_cast<uint32_t>(last[i] & 1));
     };
-    if (tid == 0) {
+    if (tid == kIssuer) {
         for (int i = 0; i < 3; ++i) mbar_init(&sm.full[i], 1);
         for (int i = 0; i < 4; ++i) mbar_init(&sm.done[i], 1);
         fence_barrier_init();
@@ -252,16 +256,24 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     };
     if (have_state) store_state_parts();
     // dt, the cumulative decay and the state-update weights of chunk k into
-    // buffer k & 1 (warp 0); padding steps get dt = 0
+    // buffer k & 1 (one warp); padding steps get dt = 0
     const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(a.delta) + head_row * L;
-    auto decay_prefix = [&](int k) {
+    // Δ of chunk k (steps 2 lane, 2 lane + 1), loaded a chunk ahead of its use
+    auto load_delta = [&](int k, float (&r)[2]) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int gl = k * kSsdQ + 2 * lane + i;
+            r[i] = gl < L ? __bfloat162float(dl[gl]) : 0.f;
+        }
+    };
+    auto decay_prefix = [&](int k, const float (&r)[2]) {
         float v[2], d[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int l = 2 * lane + i, gl = k * kSsdQ + l;
             d[i] = 0.f;
             if (gl < L) {
-                d[i] = __bfloat162float(dl[gl]) + bias;
+                d[i] = r[i] + bias;
                 if (a.softplus) d[i] = softplus_f(d[i]);
             }
             sm.dt[k & 1][l] = d[i];
@@ -282,7 +294,11 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         sm.wq[k & 1][2 * lane] = ex2_approx(cq - c0) * d[0];
         sm.wq[k & 1][2 * lane + 1] = ex2_approx(cq - c1) * d[1];
     };
-    if (warp == 0 && n > 0) decay_prefix(0);
+    if (warp == kDecayWarp && n > 0) {
+        float r[2];
+        load_delta(0, r);
+        decay_prefix(0, r);
+    }
     fence_proxy_async_smem();  // the state parts, for the tensor cores
     tc_fence_before();
     __syncthreads();
@@ -335,9 +351,11 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         const float* dtv = sm.dt[k & 1];
         const float* wq = sm.wq[k & 1];
         const bool carry = have_state || k > 0;
+        float dnext[2] = {0.f, 0.f};
+        if (warp == kDecayWarp && k + 1 < n) load_delta(k + 1, dnext);
 
         // --- G = C^T B and Y1 = C^T S^T as soon as C and B are in ---
-        if (tid == 0) {
+        if (tid == kIssuer) {
             if (!mbar_wait_bounded(&sm.full[2], par)) timed_out = true;
             if (!mbar_wait_bounded(&sm.full[1], par)) timed_out = true;
             tc_fence_after();
@@ -386,7 +404,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         __syncthreads();  // W is complete; the staging tile is read out
 
         // --- U = B W^T, while the masked operand is formed ---
-        if (tid == 0) {
+        if (tid == kIssuer) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kSsdQ / 16; ++kk) {
@@ -394,6 +412,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 umma(tU, desc_k(bs + kk * 32), desc_k(wls + kk * 32), kIdU, true);
             }
             umma_commit(&sm.done[2]);
+            if (k + 1 < n && !timed_out && mbar_try_wait(&sm.done[1], par)) issue(2, k + 1);  // C is free already
         }
         __syncwarp();
 
@@ -447,7 +466,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         __syncthreads();
 
         // --- Y2 = Gm X^T; B and C are reloaded for the next chunk once free ---
-        if (tid == 0) {
+        if (tid == kIssuer) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kSsdQ / 16; ++kk) {
@@ -458,16 +477,33 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             if (k + 1 < n) {
                 if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // G and U: B is free
                 if (!timed_out) issue(1, k + 1);
-                if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;  // G and Y1: C is free
-                if (!timed_out) issue(2, k + 1);
+                if (last[2] != k + 1) {  // C not reloaded yet
+                    if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;  // G and Y1: C is free
+                    if (!timed_out) issue(2, k + 1);
+                }
             }
         }
         __syncwarp();
 
+        // --- state: S = e^{c_Q} S + U, split into the next chunk's operand ---
+        if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // U
+        tc_fence_after();
+        {
+            uint32_t u[2][16];
+            tmem_ld_32x32b_x16(tU + lane_base + 32 * half, u[0]);
+            tmem_ld_32x32b_x16(tU + lane_base + 32 * half + 16, u[1]);
+            tmem_wait_ld();
+            const float ed = ex2_approx(c2[kSsdQ - 1]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[j] = fmaf(ed, S[j], __uint_as_float(u[j >> 4][j & 15]));
+        }
+        if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;  // Y1, the parts' last reader, is done
+        store_state_parts();
+
         // --- outputs y = e^{c_l} Y1 + Y2, staged as bf16 [p][l] over Gm ---
         if (!mbar_wait_bounded(&sm.done[3], par)) timed_out = true;  // every product of the chunk
         tc_fence_after();
-        if (tid == 0 && k + 1 < n && !timed_out) {  // x is free
+        if (tid == kIssuer && k + 1 < n && !timed_out) {  // x is free
             fence_proxy_async_smem();
             issue(0, k + 1);
         }
@@ -500,23 +536,12 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             }
         }
 
-        // --- state: S = e^{c_Q} S + U, split into the next chunk's operand ---
-        {
-            uint32_t u[2][16];
-            tmem_ld_32x32b_x16(tU + lane_base + 32 * half, u[0]);
-            tmem_ld_32x32b_x16(tU + lane_base + 32 * half + 16, u[1]);
-            tmem_wait_ld();
-            const float ed = ex2_approx(c2[kSsdQ - 1]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = fmaf(ed, S[j], __uint_as_float(u[j >> 4][j & 15]));
-        }
-        store_state_parts();  // (the Y1 product, the parts' last reader, is done)
-        if (warp == 0 && k + 1 < n) decay_prefix(k + 1);  // the next chunk's dt and decay, other buffer
+        if (warp == kDecayWarp && k + 1 < n) decay_prefix(k + 1, dnext);  // the next chunk's dt and decay, other buffer
         fence_proxy_async_smem();  // the state parts, for the next chunk's Y1 product
         tc_fence_before();
         // the staging tile, the state parts and the next chunk's decay are complete
         if (__syncthreads_or(timed_out)) {
-            if (tid == 0) {
+            if (tid == kIssuer) {
                 report_device_error(a.err, -6);
                 drain();
                 for (int i = 0; i < 4; ++i) mbar_wait_bounded(&sm.done[i], par);  // this chunk's products
