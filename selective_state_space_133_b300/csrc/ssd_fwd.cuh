@@ -20,7 +20,8 @@
 // with Gm the causally masked, decay-weighted G and W the decay-weighted x
 // (W[p][s] = x[p][s] e^{c_Q - c_s} dt_s). C and B are used straight from their
 // TMA tiles ([n][l] rows): as MN-major operands where the contraction runs over
-// n, as a K-major one (B in U) where it runs over s. Three operands are not bf16
+// n, as a K-major one (B in U) where it runs over s; the carried state is
+// written in the same [n][p] form (16-byte row pieces). Three operands are not bf16
 // inputs but values computed in fp32 (Gm, W and the carried state); each is
 // split into a bf16 high part and a bf16 remainder and multiplied twice, which
 // keeps them to ~2^-17 relative (one bf16 rounding of those operands alone
@@ -83,9 +84,8 @@ struct SsdSmem {
     alignas(1024) __nv_bfloat16 Gl[kSsdQ][kSsdQ];
     alignas(1024) __nv_bfloat16 Wh[kSsdP][kSsdQ];  // W [p][s], high part
     alignas(1024) __nv_bfloat16 Wl[kSsdP][kSsdQ];  //           low part
-    // carried state [p][n] high and low parts, in 64-column blocks [n / 64][p][n % 64]
-    alignas(1024) __nv_bfloat16 Sh[NS / 64][kSsdP][64];
-    alignas(1024) __nv_bfloat16 Sl[NS / 64][kSsdP][64];
+    alignas(1024) __nv_bfloat16 Sh[NS][kSsdP];     // carried state [n][p], high part
+    alignas(1024) __nv_bfloat16 Sl[NS][kSsdP];     //                       low part
     alignas(16) float c2[2][kSsdQ];  // c_l * log2(e), chunk k in [k & 1]
     alignas(16) float dt[2][kSsdQ];
     alignas(16) float wq[2][kSsdQ];  // e^{c_Q - c_s} dt_s
@@ -241,17 +241,22 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 #pragma unroll
     for (int j = 0; j < 32; ++j)
         S[j] = (have_state && sact) ? a.h0[(head_row * kSsdP + 32 * half + j) * NS + sn] : 0.f;
+    // the state's high and low parts as the Y1 product's operand: row n, this
+    // thread's 32 channels as four 16-byte units of each part
     auto store_state_parts = [&]() {
         if (!sact) return;
-        unsigned char* hb = reinterpret_cast<unsigned char*>(&sm.Sh[sn >> 6][0][0]);
-        unsigned char* lb = reinterpret_cast<unsigned char*>(&sm.Sl[sn >> 6][0][0]);
-        const int c = sn & 63;
+        unsigned char* hb = reinterpret_cast<unsigned char*>(&sm.Sh[sn][0]);
+        unsigned char* lb = reinterpret_cast<unsigned char*>(&sm.Sl[sn][0]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int o = swz(32 * half + j, c);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(S[j]);
-            *reinterpret_cast<__nv_bfloat16*>(hb + o) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(lb + o) = __float2bfloat16_rn(S[j] - __bfloat162float(hi));
+        for (int c = 0; c < 4; ++c) {
+            uint4 hi, lo;
+            split2(S[8 * c], S[8 * c + 1], hi.x, lo.x);
+            split2(S[8 * c + 2], S[8 * c + 3], hi.y, lo.y);
+            split2(S[8 * c + 4], S[8 * c + 5], hi.z, lo.z);
+            split2(S[8 * c + 6], S[8 * c + 7], hi.w, lo.w);
+            const int off = ((4 * half + c) ^ (sn & 7)) << 4;
+            *reinterpret_cast<uint4*>(hb + off) = hi;
+            *reinterpret_cast<uint4*>(lb + off) = lo;
         }
     };
     if (have_state) store_state_parts();
@@ -309,12 +314,11 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const uint32_t xs = smem_u32(&sm.X[0][0]), bs = smem_u32(&sm.Bt[0][0]), cs = smem_u32(&sm.Ct[0][0]);
     const uint32_t ghs = smem_u32(&sm.Gh[0][0]), gls = smem_u32(&sm.Gl[0][0]);
     const uint32_t whs = smem_u32(&sm.Wh[0][0]), wls = smem_u32(&sm.Wl[0][0]);
-    const uint32_t shs = smem_u32(&sm.Sh[0][0][0]), sls = smem_u32(&sm.Sl[0][0][0]);
+    const uint32_t shs = smem_u32(&sm.Sh[0][0]), sls = smem_u32(&sm.Sl[0][0]);
     constexpr uint32_t kIdG = umma_idesc(64, 64, true, true);     // C^T (MN-major) x B (MN-major)
-    constexpr uint32_t kIdY1 = umma_idesc(64, 64, true, false);   // C^T (MN-major) x S^T (K-major)
+    constexpr uint32_t kIdY1 = umma_idesc(64, 64, true, true);    // C^T (MN-major) x S^T (MN-major)
     constexpr uint32_t kIdY2 = umma_idesc(64, 64, false, false);  // Gm x X^T
     constexpr uint32_t kIdU = umma_idesc(NS, 64, false, false);   // B x W^T
-    constexpr uint32_t kSBlk = kSsdP * 128;                       // bytes of one 64-column state block
 
 
     __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
@@ -365,9 +369,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             if (carry) {
 #pragma unroll
                 for (int kk = 0; kk < NS / 16; ++kk) {
-                    const uint32_t so = (kk >> 2) * kSBlk + (kk & 3) * 32;
-                    umma(tY1, desc_mn(cs + kk * 2048), desc_k(shs + so), kIdY1, kk > 0);
-                    umma(tY1, desc_mn(cs + kk * 2048), desc_k(sls + so), kIdY1, true);
+                    umma(tY1, desc_mn(cs + kk * 2048), desc_mn(shs + kk * 2048), kIdY1, kk > 0);
+                    umma(tY1, desc_mn(cs + kk * 2048), desc_mn(sls + kk * 2048), kIdY1, true);
                 }
             }
             umma_commit(&sm.done[1]);
