@@ -320,7 +320,6 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     constexpr uint32_t kIdY2 = umma_idesc(64, 64, false, false);  // Gm x X^T
     constexpr uint32_t kIdU = umma_idesc(NS, 64, false, false);   // B x W^T
 
-
     __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
     // Output staging [p][kSsdYPitch] over the Gm buffers: written once the
     // masked product is done, stored to HBM at the start of the next chunk.
