@@ -91,6 +91,25 @@ def test_initial_state_and_pieces(N):
     assert max_rel_err(h2.reshape(-1, N), hr.reshape(-1, N)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("N", [64, 128])
+def test_strong_decay(N):
+    # dt near 1 and A down to -32: the decay sum of a chunk runs to thousands
+    # (log2 units), so e^{c_l}, the state-update weights and every off-diagonal
+    # weight underflow to zero; above the diagonal the kernel's e^{c_l - c_s}
+    # overflows and must be masked, not multiplied by zero
+    x = syn.ssd_inputs(2, 3, 200, N, seed=31)
+    x["A"] = -torch.tensor([8.0, 16.0, 32.0])
+    x["delta_bias"] = torch.full((3,), 0.5)
+    compare(x, "strong decay")
+
+
+def test_no_decay():
+    # A = 0: every decay factor is 1 and the state is the running sum of dt x B^T
+    x = syn.ssd_inputs(1, 2, 300, 128, seed=32)
+    x["A"] = torch.zeros(2)
+    compare(x, "A = 0")
+
+
 def test_zero_length_keeps_state():
     x = syn.ssd_inputs(2, 3, 0, 128, seed=12)
     h0 = torch.randn(2, 3, 64, 128, generator=torch.Generator().manual_seed(4))
