@@ -13,7 +13,8 @@ M[l, s] = (C_l . B_s) * prod_{r=s+1..l} a_r * dt_s. Pins:
   channels) gives the same outputs and final state;
 * the chunked form (masked products inside each chunk, the state passed from
   chunk to chunk) at chunk sizes 1, 7, 16 and 64, the decomposition a chunked
-  GPU kernel computes;
+  GPU kernel computes, and the same with D x taken as D on the diagonal of the
+  masked matrix;
 * a sequence split in two and continued from the first part's final state.
 
 Planted mistakes in copies of the C code must each fail one of these.
@@ -120,6 +121,33 @@ def check_chunked_form(orc):
         np.testing.assert_allclose(hc, hl, rtol=1e-10, atol=1e-11)
 
 
+def check_skip_in_the_diagonal(orc):
+    # the skip term D x_l as D on the diagonal of the masked intra-chunk matrix
+    # (the GPU kernel's form): Y = (T o M + D I) X over each chunk, nothing added after
+    p = problem(105, L=70)
+    y, hl = run(orc, p)
+    x, B, C, A = p["x"], p["B"], p["C"], p["A"]
+    batch, dim, L = x.shape
+    H = A.shape[0]
+    P = dim // H
+    dt = eff_dt(p)
+    for b in range(batch):
+        for h in range(H):
+            S = np.zeros((P, B.shape[1]))
+            for l0 in range(0, L, 32):
+                sl = slice(l0, min(L, l0 + 32))
+                d = dt[b, h, sl]
+                cum = np.cumsum(d * A[h])
+                X = x[b, h * P:(h + 1) * P, sl].T
+                Cc, Bc = C[b][:, sl], B[b][:, sl]
+                G = np.tril((Cc.T @ Bc) * np.exp(cum[:, None] - cum[None, :]) * d[None, :])
+                G = G + p["D"][h] * np.eye(len(d))
+                Y = G @ X + np.exp(cum)[:, None] * (Cc.T @ S.T)
+                np.testing.assert_allclose(Y.T, y[b, h * P:(h + 1) * P, sl], rtol=1e-10, atol=1e-11)
+                S = np.exp(cum[-1]) * S + (X * (np.exp(cum[-1] - cum) * d)[:, None]).T @ Bc.T
+            np.testing.assert_allclose(S, hl[b, h], rtol=1e-10, atol=1e-11)
+
+
 def check_split_continuation(orc):
     p = problem(104, L=41)
     y, hl = run(orc, p)
@@ -132,7 +160,8 @@ def check_split_continuation(orc):
         np.testing.assert_allclose(h2, hl, rtol=1e-12, atol=1e-13)
 
 
-CHECKS = [check_matrix_form, check_scan_equivalence, check_chunked_form, check_split_continuation]
+CHECKS = [check_matrix_form, check_scan_equivalence, check_chunked_form, check_skip_in_the_diagonal,
+          check_split_continuation]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
