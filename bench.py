@@ -41,11 +41,16 @@ KERNEL_SOURCES = ["selective_state_space_133_b300/csrc/scan_fwd.cuh",
                   "selective_state_space_133_b300/csrc/common.cuh",
                   "selective_state_space_133_b300/csrc/fwd_launch.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_fwd_traffic.json")
+# the same for the SSD kernel
+SSD_KERNEL_SOURCES = ["selective_state_space_133_b300/csrc/ssd_fwd.cuh",
+                      "selective_state_space_133_b300/csrc/ssd_fwd.cu",
+                      "selective_state_space_133_b300/csrc/common.cuh"]
+SSD_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ssd_fwd_traffic.json")
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -59,12 +64,12 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_per_launch(workload: str):
+def traffic_per_launch(workload: str, path=TRAFFIC_FILE, sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu capture of this workload, if the kernel is unchanged since."""
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             t = json.load(f)
-        if t.get("kernel_hash") == kernel_hash() and t.get("workload") == workload:
+        if t.get("kernel_hash") == kernel_hash(sources) and t.get("workload") == workload:
             return float(t["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -776,7 +781,8 @@ def run_ssd(args, w):
                    "parallelism": f"replicas x{ws}", "l2": f"no flush: inputs {w.io_bytes / 1e6:.0f} MB"},
         "gpu_launches": K,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "traffic": None, "peak_source": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes,
+                     "traffic": traffic_per_launch(w.name, SSD_TRAFFIC_FILE, SSD_KERNEL_SOURCES),
+                     "peak_source": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes,
                      "tensor_tflops": tflops, "tensor_peak_tflops": tc_peak, "tensor_peak_source": tc_kind,
                      "tensor_frac": tflops / tc_peak, "algorithmic_flops_per_launch": w.flops,
                      "note": "HBM bounds the roofline time of this workload (bytes / copy peak > flops / bf16 peak)"},
