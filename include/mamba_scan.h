@@ -25,11 +25,11 @@
  * written; no (batch, L, D, N) intermediate ever reaches device memory.
  *
  * Conventions shared by every entry point
- *   - Pointers are DEVICE pointers owned by the caller. The library keeps no
- *     state between calls (apart from one device error word, see
- *     mamba_check_device_error). Only mamba_scan_fwd allocates: a stream-ordered
- *     workspace (cudaMallocAsync / cudaFreeAsync on `stream`); callers that
- *     manage memory themselves pass the workspace to mamba_scan_fwd_ws.
+ *   - Pointers are DEVICE pointers owned by the caller. The library allocates
+ *     nothing and keeps no state between calls (apart from one device error
+ *     word, see mamba_check_device_error). Scratch memory, where an entry point
+ *     uses any, is a caller workspace (the *_ws entry points and the backward)
+ *     or, for mamba_scan_fwd_noalloc, a fixed array the library reserves.
  *   - All tensors are dense, row-major, contiguous:
  *       u, delta, z, y : (batch, dim, seqlen)
  *       B, C           : (batch, dstate, seqlen)   -- one group, shared by all channels
@@ -98,9 +98,9 @@ typedef enum {
  * Any of batch, dim, seqlen may be 0 (nothing to compute; final_state, if given,
  * is zero-filled). When seqlen == 0, u, delta, B, C, z and y may be NULL (an
  * empty tensor's data pointer). y must not alias an input.
- * The call launches one small kernel that packs B and C into a device workspace
- * (fp32, one row of B then C per step) and then the scan kernel; the workspace
- * is allocated and freed stream-ordered on `stream`.
+ * Allocates nothing and launches one kernel, which reads B and C in their own
+ * layout. (A long sequence over few channels runs faster through
+ * mamba_scan_fwd_ws with a workspace: see mamba_scan_workspace_size.)
  * Returns MAMBA_OK or a negative mamba_status.
  */
 int mamba_scan_fwd(const void* u, const void* delta, const float* A,
@@ -112,11 +112,21 @@ int mamba_scan_fwd(const void* u, const void* delta, const float* A,
                    int io_dtype, void* stream);
 
 /*
- * Bytes of device workspace mamba_scan_fwd_ws needs for these sizes (0 when
- * there is nothing to compute or an argument is out of range): the packed
- * fp32 B/C rows, batch * roundup(seqlen, 16) * 8 * dstate bytes, plus, only when
- * seqlen * sizeof(io type) is not a multiple of 16 bytes, copies of u, delta
- * and z at a row pitch that is.
+ * Bytes of device workspace mamba_scan_fwd_ws (and mamba_conv_scan_fwd_ws)
+ * can use for these sizes on the current device; 0 when it needs none (the
+ * usual case), when there is nothing to compute, an argument is out of range
+ * or no device is current.
+ * The workspace holds the carries of a sequence split: when batch *
+ * ceil(dim / channels per warp) (16 channels a warp for dstate 8 and 16, 8 for
+ * 32, 4 for 64) is below four warps per streaming multiprocessor, i.e. a long
+ * sequence over few channels, the 16-step chunks are cut into S segments of at
+ * least 64 chunks (S about 12 warps per scheduler over the warps of one pass,
+ * at most 32): one kernel finds every segment's end state from zero (from
+ * initial_state for the first) and the sum of dt over it, and the scan kernel
+ * starts each segment from the state these give. The size is
+ * (S - 1) * batch * dim * (dstate + 1) * 4 bytes, each part rounded up to 256.
+ * The results are the same as in one pass up to the rounding of the state at
+ * the segment boundaries.
  */
 size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int io_dtype);
 
@@ -134,12 +144,14 @@ size_t mamba_scan_workspace_size(int batch, int dim, int seqlen, int dstate, int
  *                     chunk (the first is initial_state), which mamba_scan_bwd
  *                     can take instead of recomputing it (training)
  *   workspace       : device buffer, 256-byte aligned, owned by the caller, of
- *                     at least mamba_scan_workspace_size(...) bytes (may be NULL
- *                     when that size is 0); its contents are scratch, needed
- *                     only until the call's kernels on `stream` have finished
+ *                     at least mamba_scan_workspace_size(...) bytes, or NULL;
+ *                     with NULL (or a size of 0) the scan runs in one pass,
+ *                     otherwise split as mamba_scan_workspace_size describes;
+ *                     its contents are scratch, needed only until the call's
+ *                     kernels on `stream` have finished
  *   workspace_bytes : its size
- * Allocates nothing. Returns MAMBA_ERR_WORKSPACE if the buffer is too small,
- * MAMBA_ERR_NULL if it is NULL while needed, MAMBA_ERR_ALIGN if misaligned.
+ * Allocates nothing. Returns MAMBA_ERR_WORKSPACE if a non-NULL buffer is too
+ * small, MAMBA_ERR_ALIGN if it is misaligned.
  */
 int mamba_scan_fwd_ws(const void* u, const void* delta, const float* A,
                       const void* B, const void* C,
@@ -237,22 +249,24 @@ int mamba_scan_bwd(const void* u, const void* delta, const float* A,
  * memory at start-up, plugins inside a framework that owns every device
  * allocation, programs with no allocator to provide a workspace).
  *
- * Same arguments, semantics and checks as mamba_scan_fwd. The scratch that
- * mamba_scan_fwd_ws takes from the caller lives instead in a fixed 16 MiB
- * array in device memory that the library reserves on every GPU that loads
- * it, until the process exits.
- *   - Sizes whose workspace (mamba_scan_workspace_size) exceeds 16 MiB are
- *     rejected with MAMBA_ERR_WORKSPACE before anything is launched. For
- *     lengths whose rows are whole 16-byte units that allows
- *     batch * roundup(seqlen, 16) * dstate <= 2097152 (e.g. 8 x 4096 or
- *     1 x 131072 at dstate 16).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current and caches it: make that
- *     first call before any stream capture is under way.
+ * Same arguments, semantics and checks as mamba_scan_fwd, but a long sequence
+ * over few channels is split as by mamba_scan_fwd_ws with a workspace (see
+ * mamba_scan_workspace_size). The split's carries live in a fixed 1 MiB array
+ * in device memory that the library reserves on every GPU that loads it, until
+ * the process exits.
+ *   - When the carries of the split mamba_scan_fwd_ws would take exceed 1 MiB,
+ *     this call cuts fewer segments, the most whose carries fit (on a 148-SM
+ *     GPU: 4 segments of 1 x 5120 channels at dstate 16, against 22), or none;
+ *     it never needs more memory, so no size is rejected for lack of it.
+ *   - The first call on a device that splits looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current and caches it:
+ *     make that first call before any stream capture is under way.
+ *   - `stream` must belong to the current device (MAMBA_ERR_CUDA otherwise):
+ *     the array's address is per device.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, or other host threads) race on it and must be serialised by the
- *     caller. Nothing needs clearing between calls: each call writes all the
- *     scratch it reads.
+ *     caller. Nothing needs clearing between calls: the first kernel of a
+ *     split writes every carry the second reads.
  * Returns MAMBA_OK or a negative mamba_status (MAMBA_ERR_CUDA if the address
  * lookup fails).
  */

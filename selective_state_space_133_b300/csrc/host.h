@@ -5,8 +5,8 @@
 // files defines launch_scan_n for its state size and instantiates no other
 // kernel; scan_bwd_n*.cu do the same for the backward (launch_bwd_n) and
 // ssd_fwd.cu for the SSD kernels (launch_ssd_n).
-// Everything else (argument checks, workspace layout, the B/C pack, the row
-// copies, the backward and the state update) lives in mamba_scan.cu.
+// Everything else (argument checks, workspace layouts, the backward's B/C
+// pack, the row copies of the SSD and the state update) lives in mamba_scan.cu.
 #pragma once
 
 #include <cuda.h>
@@ -31,22 +31,14 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const void* b
                  uint64_t e2, uint64_t pitch0, uint32_t b0, uint32_t b1,
                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
-// Inputs of one forward launch after the call's preparation: u/delta/z at row
-// pitch `pitch` (the caller's tensors, or copies in the workspace), and the
-// packed B/C rows (batch, Lp, 2N) fp32.
-struct FwdInputs {
-    const void* u;
-    const void* delta;
-    const void* z;   // may be null
-    const float* bc;
-    int pitch, Lp;
-};
-
 // Encodes the tensor maps and launches the forward kernel of state size NS
 // (the instantiation picked by `flags`, bits MAMBA_FLAG_*, and by whether the
-// convolution and z are given). Returns a mamba_status.
+// convolution and z are given) on the inputs named in `a`, over `nseg`
+// segments of a.seg_chunks chunks (nseg = 1, a.seg_chunks = 0: no split);
+// `state_pass` launches the state-only pass of a split sequence instead.
+// Returns a mamba_status.
 template <typename T, int NS>
-int launch_scan_n(const mscan::ScanArgs& a, const FwdInputs& in, int flags, cudaStream_t stream);
+int launch_scan_n(const mscan::ScanArgs& a, int flags, int nseg, bool state_pass, cudaStream_t stream);
 
 // Launches the backward kernel of state size NS picked by `flags` and by
 // whether z is given (defined in bwd_launch.cuh). Returns a mamba_status.

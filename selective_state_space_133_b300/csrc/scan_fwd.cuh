@@ -29,13 +29,19 @@
 //    per step (16-byte broadcast loads), and share the per-(channel, step)
 //    values dt and dt*u. At N = 16 that is 16 channels per CTA.
 //  * The sequence is cut into 16-step chunks. Lane 0 issues 3-D TMA loads of
-//    a chunk's u/delta/z tiles (kCh channels x 16 steps) and of the chunk's
-//    packed B/C rows (fp32, [step][B0..N-1 C0..N-1], written once per call by
-//    bc_pack_kernel) into a ring of kStages slots with one "full" mbarrier per
-//    slot (TMA transaction count); a slot is refilled as soon as the warp is
-//    done with it, and the waits for data are bounded and report a timeout
-//    instead of hanging.
-//  * Per chunk there are three phases, run in order:
+//    a chunk's u/delta/z tiles (kCh channels x 16 steps) and of its B and C
+//    tiles in their own (batch, N, L) layout (N rows x 16 steps each) into a
+//    ring of kStages slots with one "full" mbarrier per slot (TMA transaction
+//    count); a slot is refilled as soon as the warp is done with it, and the
+//    waits for data are bounded and report a timeout instead of hanging. When
+//    a row of L elements is not a whole number of 16-byte units (a TMA stride
+//    rule) the warp loads each chunk's tiles itself with plain loads instead.
+//    Nothing but the caller's tensors is read or written: the kernel needs no
+//    workspace.
+//  * Per chunk there are four phases, run in order:
+//      transpose  the chunk's B and C tiles, converted to fp32, into one row
+//                 per step [B0..N-1 C0..N-1] (ldmatrix.trans for bf16, a lane
+//                 per tile row for fp32), shared by every channel of the CTA;
 //      pre-pass   once per (channel, step), lane (c, j) = (lane / kG, lane % kG)
 //                 taking steps kSP*j .. kSP*j + kSP - 1 of channel c: dt and
 //                 dt*u, stored as float2 pairs that the recurrence uses as
@@ -69,14 +75,15 @@ struct FwdGeo {
     static constexpr int kG = NS / kS;            // lanes per channel
     static constexpr int kCh = 32 / kG;           // channels per CTA (one warp)
     static constexpr int kSP = kTL / kG;          // steps per lane in the pre-pass and epilogue
-    static constexpr int kBCW = 2 * NS;           // floats per step in the packed B/C buffer
+    static constexpr int kBCW = 2 * NS + 8;       // row stride (floats) of the transposed B/C tile: 16-byte
+                                                  // rows whose 8-byte stores by a half-warp hit distinct banks
     static constexpr int kWP = kTL + 2;           // W row stride (float2): 16-byte rows
     // P row strides: a quarter-warp's 16-byte stores of the recurrence land in
     // distinct banks (kPH = 16 mod 32 words when two state groups share a
     // quarter-warp), and so do the epilogue's loads of 4-step groups.
     static constexpr int kPJ = kCh * 4 + (kG == 8 ? 4 : 8);  // stride between 4-step groups (floats)
     static constexpr int kPH = (kTL / 4) * kPJ;              // stride between state groups (floats)
-    static constexpr int kStages = NS == 64 ? 3 : 4;         // TMA ring depth (N = 64: B/C rows are 8 KB a chunk)
+    static constexpr int kStages = NS == 64 ? 3 : 4;         // TMA ring depth (N = 64: B/C tiles are 4 KB a chunk)
     // y is stored kSP steps at a time in vectors of at most 16 bytes; whole
     // vectors need the row length to be a multiple of this many steps
     template <typename T>
@@ -86,6 +93,13 @@ struct FwdGeo {
 };
 
 struct ScanArgs {
+    // the inputs, read with plain loads when `plain` (rows not TMA-strideable)
+    const void* u;
+    const void* delta;
+    const void* z;       // may be null
+    const void* B;
+    const void* C;
+    int plain;
     const float* A;
     const float* D;      // may be null
     const float* bias;   // may be null
@@ -100,6 +114,15 @@ struct ScanArgs {
     const float* conv_w;     // (dim, kConvW) fp32
     const float* conv_b;     // (dim) fp32, may be null
     const void* conv_state;  // (batch, dim, kConvW - 1) io dtype: x before step 0, oldest first; may be null
+    // Sequence split (long sequences with few channels): the chunks are cut
+    // into segments of seg_chunks chunks, grid.z = segment. The state-only
+    // pass (STATE instantiation) leaves, for every segment j but the last,
+    // the state at its end when it starts from zero (from h0 for j = 0) in
+    // carry[j][b][d][:] and the sum of dt over it in carry_dt[j][b][d]; the
+    // full pass starts segment j >= 1 from the state these give.
+    int seg_chunks;      // 0: no split (one segment of every chunk)
+    float* carry;        // (segments - 1, batch, dim, N) fp32
+    float* carry_dt;     // (segments - 1, batch, dim) fp32
 };
 
 template <typename T, int NS>
@@ -108,17 +131,17 @@ struct ScanStage {
     alignas(128) T u[G::kCh][kTL];
     alignas(128) T dl[G::kCh][kTL];
     alignas(128) T z[G::kCh][kTL];
-    alignas(128) float bc[kTL][G::kBCW];
+    alignas(128) T bc[2][NS][kTL];   // B rows then C rows of the chunk, as the TMA boxes land them
 };
 
 template <typename T, int NS>
 struct ScanSmem {
     using G = FwdGeo<NS>;
     ScanStage<T, NS> st[G::kStages];
+    alignas(16) float bcT[kTL][G::kBCW];       // the chunk's B and C, fp32: row s = B[:, s] then C[:, s]
     alignas(16) float2 W[G::kCh][G::kWP];      // {dt, dt*u} per (channel, step); {dt, u} with ZOH
     alignas(16) float P[G::kG * G::kPH];       // [state group][4-step group][channel][4 steps]
     alignas(8) uint64_t full[G::kStages];      // TMA transaction barrier per slot
-    alignas(16) float U[G::kCh][kTL + 1];      // u after the convolution (CONV only)
     float XH[2][G::kCh][kConvW - 1];           // the last inputs x of the previous chunk (CONV only)
 };
 
@@ -241,11 +264,12 @@ __device__ __forceinline__ float2 zoh_gain2(float2 x2, float2 e, float2 dt, floa
 
 // ------------------------------------------------------------- kernel ------
 
-template <typename T, int NS, bool SOFTPLUS, bool HAS_Z, bool CONV, bool ZOH>
+// STATE: the state-only pass of a split sequence (no readout, no output).
+template <typename T, int NS, bool SOFTPLUS, bool HAS_Z, bool CONV, bool ZOH, bool STATE>
 __global__ void __launch_bounds__(kScanThreads)
 scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_dl, const __grid_constant__ CUtensorMap tm_z,
-                const __grid_constant__ CUtensorMap tm_bc) {
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c) {
     using G = FwdGeo<NS>;
     constexpr int kS = G::kS, kG = G::kG, kCh = G::kCh, kSP = G::kSP, kBCW = G::kBCW;
     constexpr int kPJ = G::kPJ, kPH = G::kPH, kStages = G::kStages;
@@ -254,28 +278,65 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     const int lane = threadIdx.x;
     const int b = blockIdx.y;
     const int d0 = blockIdx.x * kCh;
+    static_assert(!(STATE && HAS_Z), "the state-only pass reads no z");
     const int L = a.seqlen;
-    const int n = (L + kTL - 1) / kTL;
+    const int nall = (L + kTL - 1) / kTL;                 // chunks of the whole sequence
+    const int seg = blockIdx.z;                           // segment of a split sequence
+    const int c0 = a.seg_chunks ? seg * a.seg_chunks : 0; // first chunk of this segment
+    const int n = a.seg_chunks ? min(a.seg_chunks, nall - c0) : nall;  // its chunks
+    const bool last_seg = c0 + n == nall;
 
-    // Chunk k's tiles into slot k % kStages (lane 0 only).
-    auto issue = [&](int k) {
+    const bool plain = a.plain != 0;  // warp-uniform
+
+    // Chunk c0 + i's tiles into slot i % kStages by TMA (lane 0 only). Boxes
+    // that reach past the last channel or step are zero-filled. The state-only
+    // pass loads no C.
+    auto issue = [&](int i) {
         constexpr uint32_t kTile = kCh * kTL * sizeof(T);
-        constexpr uint32_t kStageBytes = (HAS_Z ? 3u : 2u) * kTile + kTL * kBCW * 4u;
-        ScanStage<T, NS>& S = sm.st[k % kStages];
-        uint64_t* bar = &sm.full[k % kStages];
+        constexpr uint32_t kStageBytes = (HAS_Z ? 3u : 2u) * kTile + (STATE ? 1u : 2u) * NS * kTL * sizeof(T);
+        ScanStage<T, NS>& S = sm.st[i % kStages];
+        uint64_t* bar = &sm.full[i % kStages];
         mbar_arrive_expect_tx(bar, kStageBytes);
-        const int l0 = k * kTL;
+        const int l0 = (c0 + i) * kTL;
         tma_load_3d(&S.u[0][0], &tm_u, bar, l0, d0, b);
         tma_load_3d(&S.dl[0][0], &tm_dl, bar, l0, d0, b);
         if (HAS_Z) tma_load_3d(&S.z[0][0], &tm_z, bar, l0, d0, b);
-        tma_load_3d(&S.bc[0][0], &tm_bc, bar, 0, l0, b);
+        tma_load_3d(&S.bc[0][0][0], &tm_b, bar, l0, 0, b);
+        if (!STATE) tma_load_3d(&S.bc[1][0][0], &tm_c, bar, l0, 0, b);
     };
 
-    if (lane == 0) {
+    // The same tiles with plain loads by every lane (rows that TMA cannot
+    // stride over); values past the last channel or step are zero.
+    auto load_plain = [&](ScanStage<T, NS>& S, int k) {
+        const int l0 = k * kTL;
+        const T zero = Io<T>::from_f(0.f);
+        const T* ug = static_cast<const T*>(a.u);
+        const T* dg = static_cast<const T*>(a.delta);
+        const T* zg = static_cast<const T*>(a.z);
+        for (int i = lane; i < kCh * kTL; i += 32) {
+            const int c = i / kTL, s = i % kTL;
+            const bool ok = d0 + c < a.dim && l0 + s < L;
+            const size_t g = ok ? (static_cast<size_t>(b) * a.dim + d0 + c) * L + l0 + s : 0;
+            S.u[c][s] = ok ? ug[g] : zero;
+            S.dl[c][s] = ok ? dg[g] : zero;
+            if (HAS_Z) S.z[c][s] = ok ? zg[g] : zero;
+        }
+        const T* bg = static_cast<const T*>(a.B);
+        const T* cg = static_cast<const T*>(a.C);
+        for (int i = lane; i < NS * kTL; i += 32) {
+            const int r = i / kTL, s = i % kTL;
+            const bool ok = l0 + s < L;
+            const size_t g = ok ? (static_cast<size_t>(b) * NS + r) * L + l0 + s : 0;
+            S.bc[0][r][s] = ok ? bg[g] : zero;
+            S.bc[1][r][s] = ok ? cg[g] : zero;
+        }
+    };
+
+    if (lane == 0 && !plain) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s) mbar_init(&sm.full[s], 1);
         fence_barrier_init();
-        for (int k = 0; k < n && k < kStages; ++k) issue(k);
+        for (int i = 0; i < n && i < kStages; ++i) issue(i);
     }
     __syncwarp();
 
@@ -293,7 +354,30 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);  // inf at a = 0: that branch is never taken there
     }
     float2 h[H];
-    if (a.h0) {
+    if (seg > 0 && !STATE) {
+        // the state before this segment: the state-only pass's end states,
+        // combined in order: h = S_0, then h = exp(A sum(dt_j)) h + S_j
+        const size_t bd = static_cast<size_t>(a.batch) * a.dim;
+        const size_t row = static_cast<size_t>(b) * a.dim + rd;
+        for (int j = 0; j < seg; ++j) {
+            const float4* sp = reinterpret_cast<const float4*>(a.carry + (j * bd + row) * NS + kS * rh);
+            const float sdt = a.carry_dt[j * bd + row];
+#pragma unroll
+            for (int q = 0; q < kS / 4; ++q) {
+                const float4 p = sp[q];
+                const float2 s0 = make_float2(p.x, p.y), s1 = make_float2(p.z, p.w);
+                if (j == 0) {
+                    h[2 * q] = s0;
+                    h[2 * q + 1] = s1;
+                } else {
+                    const float2 x0 = __fmul2_rn(make_float2(sdt, sdt), A2[2 * q]);
+                    const float2 x1 = __fmul2_rn(make_float2(sdt, sdt), A2[2 * q + 1]);
+                    h[2 * q] = __ffma2_rn(make_float2(ex2_approx(x0.x), ex2_approx(x0.y)), h[2 * q], s0);
+                    h[2 * q + 1] = __ffma2_rn(make_float2(ex2_approx(x1.x), ex2_approx(x1.y)), h[2 * q + 1], s1);
+                }
+            }
+        }
+    } else if (seg == 0 && a.h0) {
         const float4* hp = reinterpret_cast<const float4*>(a.h0 + (static_cast<size_t>(b) * a.dim + rd) * NS +
                                                            kS * rh);
 #pragma unroll
@@ -317,44 +401,100 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + static_cast<size_t>(edc) * kConvW);
         cw[0] = w4.x; cw[1] = w4.y; cw[2] = w4.z; cw[3] = w4.w;
         cb = a.conv_b ? a.conv_b[edc] : 0.f;
-        // the inputs before step 0 (read in the first pre-pass)
+        // the inputs before the segment's first step (read in the first
+        // pre-pass): the convolution state before step 0, else the sequence's
+        // own inputs before the segment
         if (ej == 0) {
 #pragma unroll
-            for (int m = 0; m < kConvW - 1; ++m)
-                sm.XH[1][ec][m] = (a.conv_state && eactive)
-                    ? Io<T>::to_f(static_cast<const T*>(a.conv_state)[(static_cast<size_t>(b) * a.dim + ed) *
-                                                                          (kConvW - 1) + m])
-                    : 0.f;
+            for (int m = 0; m < kConvW - 1; ++m) {
+                float x = 0.f;
+                if (c0 > 0 && eactive)
+                    x = Io<T>::to_f(static_cast<const T*>(a.u)[(static_cast<size_t>(b) * a.dim + ed) * L + c0 * kTL -
+                                                              (kConvW - 1) + m]);
+                else if (a.conv_state && eactive)
+                    x = Io<T>::to_f(static_cast<const T*>(a.conv_state)[(static_cast<size_t>(b) * a.dim + ed) *
+                                                                          (kConvW - 1) + m]);
+                sm.XH[(c0 + 1) & 1][ec][m] = x;
+            }
         }
     }
+    float ukeep[kSP];  // u of this lane's pre-pass steps (after the convolution), kept for the epilogue
+    float dt_sum = 0.f;  // state-only pass: the sum of dt over the segment (this lane's channel)
     // this lane's output: steps kSP*ej .. kSP*ej + kSP - 1 of every chunk of channel ed
     T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + kSP * ej;
     const bool vec_ok = eactive && (L % G::template vec_steps<T>()) == 0;
 
-    // Bounded wait for the tiles of chunk k in slot s; warp-uniform verdict. On
-    // a timeout the warp records the error and waits (bounded again) for the
-    // copies that may still be in flight, so that none lands after it exits.
-    auto wait_full = [&](int s, int k) -> bool {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.full[s], (k / kStages) & 1));
+    // Bounded wait for the tiles of the segment's chunk i (slot i % kStages);
+    // warp-uniform verdict. On a timeout the warp records the error and waits
+    // (bounded again) for the copies that may still be in flight, so that
+    // none lands after it exits.
+    auto wait_full = [&](int i) -> bool {
+        if (plain) {
+            load_plain(sm.st[i % kStages], c0 + i);
+            __syncwarp();
+            return true;
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&sm.full[i % kStages], (i / kStages) & 1));
         if (!ok) {
             report_device_error(a.err, -6);
-            for (int j = k + 1; j < n && j < k + kStages; ++j)
+            for (int j = i + 1; j < n && j < i + kStages; ++j)
                 mbar_wait_bounded(&sm.full[j % kStages], (j / kStages) & 1);
         }
         return ok;
     };
 
-    // Slot s is free once every lane is done with chunk k: lane 0 refills it
-    // with chunk k + kStages (the proxy fence orders the lanes' generic reads
-    // of the slot before the TMA's writes).
-    auto release = [&](int k) {
-        if (lane == 0 && k + kStages < n) {
+    // The slot of the segment's chunk i is free once every lane is done with
+    // it: lane 0 refills it with chunk i + kStages (the proxy fence orders the
+    // lanes' generic reads of the slot before the TMA's writes).
+    auto release = [&](int i) {
+        if (lane == 0 && !plain && i + kStages < n) {
             fence_proxy_async_smem();
-            issue(k + kStages);
+            issue(i + kStages);
         }
     };
 
-    // --- the three phases --------------------------------------------------
+    // --- the four phases ---------------------------------------------------
+    // B and C of the chunk into bcT (fp32, one row per step). bf16: 16 x 16
+    // blocks with ldmatrix.trans; lane t receives, for each of the 4 8x8
+    // matrices j of a block, rows n and n + 1 (n = 8(j%2) + 2(t%4)) of column
+    // l = 8(j/2) + t/4, i.e. the pair (B[n][l], B[n+1][l]), stored as one
+    // 8-byte word of row l. fp32: a lane per tile row, each lane writing one
+    // column of bcT (the 32 lanes of a store write 32 consecutive words).
+    auto transpose = [&](const ScanStage<T, NS>& S) {
+        const T* raw = &S.bc[0][0][0];
+        if constexpr (sizeof(T) == 2) {
+            const int mj = lane / 8, mr = lane % 8;
+            constexpr int kBlocks = STATE ? (NS + 15) / 16 : NS / 8;  // 16-row blocks (the state pass needs B only)
+#pragma unroll
+            for (int blk = 0; blk < kBlocks; ++blk) {
+                const T* rowp = raw + (16 * blk + 8 * (mj % 2) + mr) * kTL + 8 * (mj / 2);
+                uint32_t q[4];
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3])
+                             : "r"(smem_u32(rowp)));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int nn = 16 * blk + 8 * (j % 2) + 2 * (lane % 4);
+                    const int l = 8 * (j / 2) + lane / 4;
+                    float lo, hi;
+                    bf16x2_to_f(q[j], lo, hi);
+                    *reinterpret_cast<float2*>(&sm.bcT[l][nn]) = make_float2(lo, hi);
+                }
+            }
+        } else {
+            constexpr int kRows = STATE ? NS : 2 * NS;
+#pragma unroll
+            for (int r0 = 0; r0 < kRows; r0 += 32) {
+                if (r0 + lane < kRows) {
+                    float v[kTL];
+                    lds_n<kTL>(reinterpret_cast<const float*>(raw) + (r0 + lane) * kTL, v);
+#pragma unroll
+                    for (int t = 0; t < kTL; ++t) sm.bcT[t][r0 + lane] = v[t];
+                }
+            }
+        }
+    };
+
     auto prepass = [&](const ScanStage<T, NS>& S, int k) {
         float uv[kSP], dv[kSP];
         lds_n<kSP>(&S.u[ec][kSP * ej], uv);
@@ -383,9 +523,10 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
                 for (int m = 0; m < kConvW; ++m) acc = fmaf(cw[m], xs[i + m], acc);
                 uv[i] = silu_f(acc);
-                sm.U[ec][kSP * ej + i] = uv[i];
             }
         }
+#pragma unroll
+        for (int i = 0; i < kSP; ++i) ukeep[i] = uv[i];
         const float2 bb = make_float2(bias, bias);
         float4* W = reinterpret_cast<float4*>(&sm.W[ec][kSP * ej]);
         const int lr = k * kTL + kSP * ej;  // first step of this lane's kSP
@@ -406,17 +547,19 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     // The recurrence is software-pipelined by one step: the loads, the ex2 of
     // dt*A and the input term of step t+1 are issued before the state update
     // of step t uses them.
-    auto recurrence = [&](const ScanStage<T, NS>& S) {
+    auto recurrence = [&]() {
         const float2* W = &sm.W[rc][0];
-        const float* bc = &S.bc[0][0] + kS * rh;  // B of this lane's states; their C is NS floats further
+        const float* bc = &sm.bcT[0][0] + kS * rh;  // B of this lane's states; their C is NS floats further
         float* P = &sm.P[rh * kPH + 4 * rc];
         auto load_bc = [&](int t, float2 (&bn)[H], float2 (&cn)[H]) {
 #pragma unroll
             for (int q = 0; q < kS / 4; ++q) {
                 const float4 bq = *reinterpret_cast<const float4*>(bc + t * kBCW + 4 * q);
-                const float4 cq = *reinterpret_cast<const float4*>(bc + t * kBCW + NS + 4 * q);
                 bn[2 * q] = make_float2(bq.x, bq.y); bn[2 * q + 1] = make_float2(bq.z, bq.w);
-                cn[2 * q] = make_float2(cq.x, cq.y); cn[2 * q + 1] = make_float2(cq.z, cq.w);
+                if (!STATE) {
+                    const float4 cq = *reinterpret_cast<const float4*>(bc + t * kBCW + NS + 4 * q);
+                    cn[2 * q] = make_float2(cq.x, cq.y); cn[2 * q + 1] = make_float2(cq.z, cq.w);
+                }
             }
         };
         float2 e[H], pb[H], cv[H];
@@ -425,6 +568,7 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             const float2 w = W[0];
             float2 bn[H];
             load_bc(0, bn, cv);
+            if (STATE) dt_sum += w.x;
             const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
 #pragma unroll
             for (int i = 0; i < H; ++i) {
@@ -447,8 +591,9 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             float2 bn[H], cn[H];
             load_bc(tn, bn, cn);
             const float2 dd = make_float2(w.x, w.x), du = make_float2(w.y, w.y);
+            if (STATE && t + 1 < kTL) dt_sum += w.x;  // step t + 1's dt
             float2 acc = make_float2(0.f, 0.f);
-            if (t > 0) {  // step t - 1
+            if (!STATE && t > 0) {  // step t - 1
                 acc = __fmul2_rn(cp[0], h[0]);
 #pragma unroll
                 for (int j = 1; j < H; ++j) acc = __ffma2_rn(cp[j], h[j], acc);
@@ -467,16 +612,19 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
                     if (ZOH) pb[j] = __fmul2_rn(zoh_gain2(x[j], e[j], dd, IA[j]), pb[j]);
                 }
             }
-            if (t > 0) p[t - 1] = acc.x + acc.y;
+            if (!STATE) {
+                if (t > 0) p[t - 1] = acc.x + acc.y;
 #pragma unroll
-            for (int j = 0; j < H; ++j) {
-                cp[j] = cv[j];
-                cv[j] = cn[j];
+                for (int j = 0; j < H; ++j) {
+                    cp[j] = cv[j];
+                    cv[j] = cn[j];
+                }
+                if (t > 0 && t % 4 == 0)  // steps t-4 .. t-1: one 16-byte store
+                    *reinterpret_cast<float4*>(P + (t / 4 - 1) * kPJ) =
+                        make_float4(p[t - 4], p[t - 3], p[t - 2], p[t - 1]);
             }
-            if (t > 0 && t % 4 == 0)  // steps t-4 .. t-1: one 16-byte store
-                *reinterpret_cast<float4*>(P + (t / 4 - 1) * kPJ) = make_float4(p[t - 4], p[t - 3], p[t - 2], p[t - 1]);
         }
-        {  // the last step's contraction
+        if (!STATE) {  // the last step's contraction
             float2 acc = __fmul2_rn(cp[0], h[0]);
 #pragma unroll
             for (int j = 1; j < H; ++j) acc = __ffma2_rn(cp[j], h[j], acc);
@@ -512,12 +660,8 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             y[0] = s.x; y[1] = s.y;
         }
         float uv[kSP];
-        if (CONV) {
 #pragma unroll
-            for (int i = 0; i < kSP; ++i) uv[i] = sm.U[ec][kSP * ej + i];
-        } else {
-            lds_n<kSP>(&S.u[ec][kSP * ej], uv);
-        }
+        for (int i = 0; i < kSP; ++i) uv[i] = ukeep[i];
         float zv[kSP];
         if (HAS_Z) lds_n<kSP>(&S.z[ec][kSP * ej], zv);
         const float2 DD = make_float2(Dd, Dd);
@@ -549,34 +693,45 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     // slots each phase leaves idle. The loop body is not unrolled over the
     // ring: one copy of the (fully unrolled) chunk code stays in the
     // instruction cache.
+    // Local chunk i of the segment is the sequence's chunk c0 + i.
     if (n > 0) {
-        if (!wait_full(0, 0)) return;
-        prepass(sm.st[0], 0);
+        if (!wait_full(0)) return;
+        transpose(sm.st[0]);
+        prepass(sm.st[0], c0);
         __syncwarp();
-        float* const ck = a.chunk_states
-            ? a.chunk_states + (static_cast<size_t>(b) * a.dim + rd) * n * NS + kS * rh
+        float* const ck = (!STATE && a.chunk_states)
+            ? a.chunk_states + (static_cast<size_t>(b) * a.dim + rd) * nall * NS + kS * rh
             : nullptr;
         const bool ck_store = ck && d0 + rc < a.dim;
 #pragma unroll 1
-        for (int k = 0; k < n; ++k) {
-            const ScanStage<T, NS>& S = sm.st[k % kStages];
-            if (ck_store) store_state(ck + static_cast<size_t>(k) * NS);  // the state before chunk k, for the backward
-            recurrence(S);
+        for (int i = 0; i < n; ++i) {
+            const ScanStage<T, NS>& S = sm.st[i % kStages];
+            // the state before chunk c0 + i, for the backward
+            if (ck_store) store_state(ck + static_cast<size_t>(c0 + i) * NS);
+            recurrence();
             __syncwarp();
-            epilogue(S, k);
+            if (!STATE) epilogue(S, c0 + i);
             __syncwarp();
-            release(k);
-            if (k + 1 < n) {
-                const int s1 = (k + 1) % kStages;
-                if (!wait_full(s1, k + 1)) return;
-                prepass(sm.st[s1], k + 1);
+            release(i);
+            if (i + 1 < n) {
+                const int s1 = (i + 1) % kStages;
+                if (!wait_full(i + 1)) return;
+                transpose(sm.st[s1]);  // bcT is free: the recurrence of chunk i is done
+                prepass(sm.st[s1], c0 + i + 1);
             }
             __syncwarp();
         }
     }
 
-    if (a.final_state && d0 + rc < a.dim)
+    if (STATE) {  // the segment's end state and its sum of dt, for the segments after it
+        if (d0 + rc < a.dim) {
+            const size_t row = static_cast<size_t>(seg) * a.batch * a.dim + static_cast<size_t>(b) * a.dim + d0 + rc;
+            store_state(a.carry + row * NS + kS * rh);
+            if (rh == 0) a.carry_dt[row] = dt_sum;
+        }
+    } else if (a.final_state && last_seg && d0 + rc < a.dim) {
         store_state(a.final_state + (static_cast<size_t>(b) * a.dim + d0 + rc) * NS + kS * rh);
+    }
 }
 
 // Packs B and C ((batch, NS, L) each, io dtype) into one fp32 buffer

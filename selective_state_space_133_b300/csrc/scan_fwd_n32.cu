@@ -1,7 +1,7 @@
-// Forward-scan kernels for state size N = 32 (all 16 flag combinations, fp32 and bf16 I/O).
+// Forward-scan kernels for state size N = 32 (all 16 flag combinations and their state-only passes, fp32 and bf16 I/O).
 #include "fwd_launch.cuh"
 
 namespace mhost {
-template int launch_scan_n<float, 32>(const mscan::ScanArgs&, const FwdInputs&, int, cudaStream_t);
-template int launch_scan_n<__nv_bfloat16, 32>(const mscan::ScanArgs&, const FwdInputs&, int, cudaStream_t);
+template int launch_scan_n<float, 32>(const mscan::ScanArgs&, int, int, bool, cudaStream_t);
+template int launch_scan_n<__nv_bfloat16, 32>(const mscan::ScanArgs&, int, int, bool, cudaStream_t);
 }  // namespace mhost

@@ -47,7 +47,8 @@ def _flags(softplus, zoh=False) -> int:
 
 
 def workspace_bytes(batch: int, dim: int, seqlen: int, dtype: torch.dtype, dstate: int = 16) -> int:
-    """Device workspace the scan needs for these sizes (mamba_scan_workspace_size)."""
+    """Device workspace the scan can use for these sizes (mamba_scan_workspace_size): the carries of a
+    sequence split, non-zero only for long sequences over few channels."""
     return int(_lib.lib().mamba_scan_workspace_size(batch, dim, seqlen, dstate, _IO[dtype]))
 
 
@@ -62,7 +63,8 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     ``final_state`` may be a preallocated (batch, dim, N) fp32 tensor, or True
     to allocate one.
     ``workspace`` may be a uint8 CUDA tensor of at least ``workspace_bytes(...)``
-    bytes; otherwise one is taken from torch's caching allocator.
+    bytes; otherwise, where that size is not zero (a sequence split), one is taken
+    from torch's caching allocator.
     ``initial_state``: (batch, dim, N) fp32 state before the first step, or None
     for zero (continuing an earlier scan from its final state).
     ``chunk_states``: a (batch, dim, ceil(L/16), N) fp32 tensor that receives the
@@ -98,14 +100,14 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     lib = _lib.lib()
     need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[u.dtype]))
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
     elif workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
     st = lib.mamba_scan_fwd_ws(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         _flags(softplus, zoh), _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), batch, dim, L, N,
         _IO[u.dtype],
-        _ptr(workspace), workspace.numel(), _stream_handle(stream, dev))
+        _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream_handle(stream, dev))
     _lib.check(st, "mamba_scan_fwd")
     return (y, final_state) if want_state else y
 
@@ -150,11 +152,12 @@ def mamba_conv_scan_fwd(x, conv_weight, delta, A, B, C, D=None, z=None, delta_bi
     lib = _lib.lib()
     need = int(lib.mamba_scan_workspace_size(batch, dim, L, N, _IO[x.dtype]))
     if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
     st = lib.mamba_conv_scan_fwd_ws(
         _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_state), width, _ptr(delta), _ptr(A), _ptr(B),
         _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _flags(softplus, zoh), _ptr(initial_state), _ptr(y),
-        _ptr(final_state), batch, dim, L, N, _IO[x.dtype], _ptr(workspace), workspace.numel(),
+        _ptr(final_state), batch, dim, L, N, _IO[x.dtype], _ptr(workspace),
+        0 if workspace is None else workspace.numel(),
         _stream_handle(stream, dev))
     _lib.check(st, "mamba_conv_scan_fwd")
     return (y, final_state) if want_state else y

@@ -33,7 +33,7 @@ def run(x, w, b, s, h0=None):
 
 @pytest.mark.parametrize("batch,dim,L,dtype,bias,state", [
     (2, 24, 96, torch.bfloat16, True, False),
-    (1, 33, 203, torch.bfloat16, True, True),     # ragged channels and length, row-pitch copies
+    (1, 33, 203, torch.bfloat16, True, True),     # ragged channels and length, plain loads
     (2, 16, 45, torch.float32, False, True),
     (2, 32, 256, torch.float32, True, False),
     (2, 64, 4096, torch.bfloat16, True, True),

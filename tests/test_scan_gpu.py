@@ -78,17 +78,17 @@ EDGE = [
     # batch, dim, L, dtype, flags
     (1, 16, 32, torch.float32, {}),              # exactly one tile, two chunks
     (2, 20, 40, torch.bfloat16, {}),             # ragged channels and ragged last chunk
-    (1, 33, 100, torch.float32, {}),             # ragged everything, fp32 row pitch 400 B
-    (3, 17, 7, torch.bfloat16, {}),              # L % 8 != 0: rows copied to a 16-byte pitch first
+    (1, 33, 100, torch.float32, {}),             # ragged everything, fp32 rows of 400 B (TMA)
+    (3, 17, 7, torch.bfloat16, {}),              # L % 8 != 0: tiles loaded with plain loads
     (2, 5, 1, torch.float32, {}),                # L = 1
     (1, 1, 1, torch.bfloat16, {}),               # a single element row
-    (2, 48, 257, torch.bfloat16, {}),            # ragged, row-pitch copy, several chunks
-    (1, 16, 6, torch.float32, {}),               # fp32 row of 24 bytes: row-pitch copy
+    (2, 48, 257, torch.bfloat16, {}),            # ragged, plain loads, several chunks
+    (1, 16, 6, torch.float32, {}),               # fp32 row of 24 bytes: plain loads
     (1, 64, 1000, torch.float32, dict(with_z=False)),
     (1, 64, 512, torch.bfloat16, dict(with_D=False)),
     (2, 32, 96, torch.float32, dict(softplus_in_kernel=False)),
     (1, 40, 64, torch.bfloat16, dict(with_D=False, with_z=False, softplus_in_kernel=False)),
-    (4, 64, 4096, torch.bfloat16, dict(a_noise=0.1)),
+    (4, 64, 4096, torch.bfloat16, dict(a_noise=0.1)),   # few channel rows: sequence split
     (1, 48, 48, torch.bfloat16, {}),             # three chunks
     (1, 32, 80, torch.bfloat16, {}),             # five chunks: the ring (4 slots) wraps
     (1, 16, 16 * 9, torch.bfloat16, {}),         # nine chunks: every slot reused twice
@@ -152,11 +152,12 @@ def test_inputs_not_modified():
         assert torch.equal(v, d[k]), k
 
 
-def test_allocating_entry_point_through_the_c_abi():
-    """mamba_scan_fwd (workspace allocated stream-ordered by the library) equals the _ws path."""
+def test_entry_point_without_workspace_through_the_c_abi():
+    """mamba_scan_fwd (no workspace; the library allocates nothing) equals the _ws path on a shape
+    that takes no sequence split."""
     import ctypes
     from selective_state_space_133_b300 import _lib
-    x = syn.scan_inputs(2, 40, 203, torch.bfloat16, seed=21)   # 203: odd length, row-pitch copies too
+    x = syn.scan_inputs(2, 40, 203, torch.bfloat16, seed=21)   # 203: odd length, plain loads
     d = to_dev(x)
     y_ref, h_ref = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
                                       d["delta_bias"], True, final_state=True)

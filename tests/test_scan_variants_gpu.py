@@ -55,7 +55,7 @@ SHAPES = [
     (3, 17, 7, torch.bfloat16),    # L % 8 != 0: rows copied to a 16-byte pitch
     (2, 5, 1, torch.float32),      # L = 1
     (1, 9, 16 * 9, torch.bfloat16),  # nine chunks: the ring wraps at every depth
-    (2, 37, 301, torch.float32),   # fp32 rows of 1204 B: row-pitch copies, ragged tail of 13 steps
+    (2, 37, 301, torch.float32),   # fp32 rows of 1204 B: plain loads, ragged tail of 13 steps
 ]
 
 
