@@ -3,6 +3,7 @@
 Plausible mistakes planted in copies of the backward code of
 ``oracle/scan_oracle.c`` (the real file is never touched) must each fail a pin.
 """
+import numpy as np
 import pytest
 
 import oracle
@@ -49,3 +50,21 @@ def test_mutant_is_caught(name, tmp_path):
         except AssertionError:
             failed.append(check.__name__)
     assert failed, f"mutant '{name}' passes every pin"
+
+
+def test_sharded_backward_equals_the_whole():
+    """The block-sharded oracle backward (used for the full-size GPU check) sums its blocks into the
+    same gradients as one call over every row: ragged blocks, h0, bf16 inputs."""
+    import torch
+    from oracle_shards import scan_bwd_sharded
+    from selective_state_space_133_b300 import synthetic as syn
+    x = syn.scan_inputs(2, 40, 64, torch.bfloat16, seed=17, a_noise=0.1)
+    g = torch.Generator().manual_seed(18)
+    dy = torch.randn(2, 40, 64, generator=g).to(torch.bfloat16)
+    h0 = torch.randn(2, 40, 16, generator=g) * 0.3
+    whole = oracle.scan_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                            x["softplus"], dy=dy, h0=h0)
+    parts = scan_bwd_sharded(x, dy, h0=h0, block=16, workers=2)
+    assert set(parts) == set(whole)
+    for k, v in whole.items():
+        assert np.allclose(parts[k], v, rtol=1e-12, atol=1e-12), k

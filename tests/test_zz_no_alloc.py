@@ -23,13 +23,15 @@ from selective_state_space_133_b300 import synthetic as syn
 P = 0x10000  # 16-byte aligned fake address; never dereferenced by a rejected call
 
 
-def _noalloc(d, y, h, stream, dstate=16):
+def _noalloc(d, y, h, stream, zoh=False):
     batch, dim, L = d["u"].shape
+    dstate = d["A"].shape[1]
     ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     io = _lib.MAMBA_BF16 if d["u"].dtype == torch.bfloat16 else _lib.MAMBA_F32
+    flags = (_lib.MAMBA_FLAG_SOFTPLUS if d["softplus"] else 0) | (_lib.MAMBA_FLAG_ZOH if zoh else 0)
     return _lib.lib().mamba_scan_fwd_noalloc(
         ptr(d["u"]), ptr(d["delta"]), ptr(d["A"]), ptr(d["B"]), ptr(d["C"]), ptr(d["D"]), ptr(d["z"]),
-        ptr(d["delta_bias"]), int(bool(d["softplus"])), ptr(y), ptr(h), batch, dim, L, dstate, io,
+        ptr(d["delta_bias"]), flags, ptr(y), ptr(h), batch, dim, L, dstate, io,
         ctypes.c_void_p(stream.cuda_stream))
 
 
@@ -53,6 +55,30 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert _noalloc(d, y, h, stream) == 0
         ops.check_device_error()
         assert torch.equal(y, y_ref) and torch.equal(h, h_ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dstate,L,zoh,dtype", [
+    (64, 4096, True, torch.bfloat16),    # the largest state: 65 carries a row
+    (32, 2100, True, torch.float32),     # ragged last segment
+    (8, 5003, False, torch.bfloat16),    # odd length: plain loads
+])
+def test_noalloc_state_sizes_zoh_and_no_final_state(dstate, L, zoh, dtype):
+    # y only (final_state NULL), the exact ZOH gain, every state size; the
+    # workspace entry point's carries fit the array here, so both split alike
+    lib = _lib.lib()
+    x = syn.scan_inputs(1, 64, L, dtype, seed=40 + dstate, dstate=dstate, a_noise=0.1)
+    need = lib.mamba_scan_workspace_size(1, 64, L, dstate, _lib.MAMBA_BF16 if dtype == torch.bfloat16
+                                         else _lib.MAMBA_F32)
+    assert 0 < need <= 1 << 20
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y_ref = ops.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                               d["softplus"], zoh=zoh)
+    for _ in range(2):
+        y = torch.full_like(y_ref, float("nan"))
+        assert _noalloc(d, y, None, torch.cuda.current_stream(), zoh=zoh) == 0
+        ops.check_device_error()
+        assert torch.equal(y, y_ref)
 
 
 @pytest.mark.gpu
