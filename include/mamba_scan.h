@@ -74,7 +74,9 @@ typedef enum {
     MAMBA_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed (launch or tensor map) */
     MAMBA_ERR_DEVICE_TIMEOUT = -6,  /* a kernel gave up waiting on its own copies (see below) */
     MAMBA_ERR_WORKSPACE = -7,       /* workspace_bytes < mamba_scan_workspace_size(...) */
-    MAMBA_ERR_FLAGS = -8            /* flags holds an unknown bit, or one this entry point lacks */
+    MAMBA_ERR_FLAGS = -8,           /* flags holds an unknown bit, or one this entry point lacks */
+    MAMBA_ERR_DEVICE_BOUNDS = -9    /* checked-bounds build only: a kernel computed an index outside
+                                       a tensor and skipped that access (see mamba_checked_bounds) */
 } mamba_status;
 
 typedef enum {
@@ -358,10 +360,26 @@ int mamba_ssd_update(float* state, const void* x, const void* delta, const float
  * Synchronises `stream`, then reads and clears the library's device error word.
  * Kernels that wait on their own asynchronous copies give up after a bounded
  * number of polls (far beyond any normal copy time), set this word and return
- * early instead of hanging. Returns MAMBA_OK, MAMBA_ERR_DEVICE_TIMEOUT, or
- * MAMBA_ERR_CUDA if the synchronisation itself failed.
+ * early instead of hanging. In the checked-bounds build a kernel that computes
+ * an index outside a tensor skips that access and sets the word too. The first
+ * error recorded since the last check wins. Returns MAMBA_OK,
+ * MAMBA_ERR_DEVICE_TIMEOUT, MAMBA_ERR_DEVICE_BOUNDS, or MAMBA_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 int mamba_check_device_error(void* stream);
+
+/*
+ * 1 if this build of the library is the checked-bounds one, else 0. That
+ * build (compiled with -DMAMBA_DEBUG_BOUNDS; the Python package builds it as
+ * libmambascan_checked.so) exports the same calls with the same results, but
+ * every global load and store its kernels make with ordinary instructions is
+ * first checked against the extent of the tensor it belongs to, computed from
+ * the call's sizes. An access outside is skipped (a load yields zero) and
+ * recorded as MAMBA_ERR_DEVICE_BOUNDS in the device error word; nothing traps.
+ * TMA copies are bounded by their tensor maps, which are encoded from the same
+ * sizes. It is a testing aid (slower), not for production.
+ */
+int mamba_checked_bounds(void);
 
 /* Human-readable name of a mamba_status value (static string, never NULL). */
 const char* mamba_status_string(int status);

@@ -1,13 +1,16 @@
 """ctypes handle on libmambascan.so (the C ABI in include/mamba_scan.h).
 
 There is no fallback: if the library is missing the import of an op raises.
+``using(path)`` points every op at another build of the same ABI for a while
+(the checked-bounds build, libmambascan_checked.so, in its tests).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
-from .build import LIBRARY
+from .build import CHECKED_LIBRARY, LIBRARY  # noqa: F401
 
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
@@ -15,7 +18,7 @@ MAMBA_FLAG_SOFTPLUS = 1
 MAMBA_FLAG_ZOH = 2
 STATUS = {0: "MAMBA_OK", -1: "MAMBA_ERR_NULL", -2: "MAMBA_ERR_SHAPE", -3: "MAMBA_ERR_DTYPE",
           -4: "MAMBA_ERR_ALIGN", -5: "MAMBA_ERR_CUDA", -6: "MAMBA_ERR_DEVICE_TIMEOUT",
-          -7: "MAMBA_ERR_WORKSPACE", -8: "MAMBA_ERR_FLAGS"}
+          -7: "MAMBA_ERR_WORKSPACE", -8: "MAMBA_ERR_FLAGS", -9: "MAMBA_ERR_DEVICE_BOUNDS"}
 
 # (name, restype, argtypes) of every symbol the header declares.
 _P = ctypes.c_void_p
@@ -38,9 +41,11 @@ SIGNATURES = {
     "mamba_check_device_error": (_I, [_P]),
     "mamba_status_string": (ctypes.c_char_p, [_I]),
     "mamba_version": (_I, []),
+    "mamba_checked_bounds": (_I, []),
 }
 
 _lib = None
+_handles = {}
 
 
 class MambaError(RuntimeError):
@@ -49,20 +54,39 @@ class MambaError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
-def lib() -> ctypes.CDLL:
-    """Load the library once; raise if it has not been built."""
-    global _lib
-    if _lib is None:
-        if not os.path.exists(LIBRARY):
-            raise RuntimeError(f"{LIBRARY} is missing: build it with "
+def load(path: str) -> ctypes.CDLL:
+    """The library at ``path`` (loaded once, with every ABI signature set); raise if it has not been built."""
+    if path not in _handles:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
                                "selective_state_space_133_b300.build.build_library()")
-        handle = ctypes.CDLL(LIBRARY)
+        handle = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(handle, name)
             fn.restype = res
             fn.argtypes = args
-        _lib = handle
+        _handles[path] = handle
+    return _handles[path]
+
+
+def lib() -> ctypes.CDLL:
+    """The library every op calls: libmambascan.so unless ``using`` says otherwise."""
+    global _lib
+    if _lib is None:
+        _lib = load(LIBRARY)
     return _lib
+
+
+@contextlib.contextmanager
+def using(path: str):
+    """Route every op through the build at ``path`` inside the ``with`` block."""
+    global _lib
+    before = lib()
+    _lib = load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = before
 
 
 def check(status: int, where: str) -> None:

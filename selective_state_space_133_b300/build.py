@@ -2,7 +2,10 @@
 
 Each .cu file is compiled to an object on its own (in parallel: the forward
 kernels of each state size have a file of their own), then the objects are
-linked into the shared library.
+linked into the shared library. ``build_library(checked=True)`` builds the
+same sources with -DMAMBA_DEBUG_BOUNDS into libmambascan_checked.so, the
+testing build whose kernels check every plain global access against its
+tensor's extent (include/mamba_scan.h, mamba_checked_bounds).
 """
 from __future__ import annotations
 
@@ -15,6 +18,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBRARY = os.path.join(HERE, "libmambascan.so")
+CHECKED_LIBRARY = os.path.join(HERE, "libmambascan_checked.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 # every source and header the library is built from: any change triggers a rebuild
@@ -32,32 +36,36 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIBRARY):
+def up_to_date(library: str = LIBRARY) -> bool:
+    if not os.path.exists(library):
         return False
-    t = os.path.getmtime(LIBRARY)
+    t = os.path.getmtime(library)
     return all(os.path.getmtime(f) <= t for f in DEPENDS)
 
 
-def _compile(src: str, extra_flags) -> str:
-    obj = os.path.join(OBJDIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+def _compile(src: str, objdir: str, extra_flags) -> str:
+    obj = os.path.join(objdir, os.path.splitext(os.path.basename(src))[0] + ".o")
     subprocess.run([nvcc(), *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj], check=True)
     return obj
 
 
-def build_library(force: bool = False, extra_flags=()) -> str:
-    """Compile the CUDA sources into libmambascan.so next to this file."""
-    if force or not up_to_date():
-        os.makedirs(OBJDIR, exist_ok=True)
+def build_library(force: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Compile the CUDA sources into libmambascan.so (or, checked, libmambascan_checked.so) next to this file."""
+    library = CHECKED_LIBRARY if checked else LIBRARY
+    objdir = os.path.join(OBJDIR, "checked") if checked else OBJDIR
+    flags = (*extra_flags, "-DMAMBA_DEBUG_BOUNDS") if checked else tuple(extra_flags)
+    if force or not up_to_date(library):
+        os.makedirs(objdir, exist_ok=True)
         workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
         with concurrent.futures.ThreadPoolExecutor(workers) as pool:
-            objs = list(pool.map(lambda src: _compile(src, extra_flags), SOURCES))
-        tmp = LIBRARY + ".tmp"
+            objs = list(pool.map(lambda src: _compile(src, objdir, flags), SOURCES))
+        tmp = library + ".tmp"
         subprocess.run([nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", *objs, "-o", tmp],
                        check=True)
-        os.replace(tmp, LIBRARY)
-    return LIBRARY
+        os.replace(tmp, library)
+    return library
 
 
 if __name__ == "__main__":
     print(build_library(force=True))
+    print(build_library(force=True, checked=True))

@@ -170,6 +170,44 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // reads (and clears) it in mamba_check_device_error.
 __device__ __forceinline__ void report_device_error(int* err, int code) { atomicCAS(err, 0, code); }
 
+// ------------------------------------------------- checked-bounds build ----
+// Built with -DMAMBA_DEBUG_BOUNDS, every global load and store that a kernel
+// makes with ordinary instructions is first checked to lie inside the tensor
+// it belongs to (its base pointer and its extent, from the call's sizes). An
+// access outside is skipped (a load yields zero) and the kernel records
+// MAMBA_ERR_DEVICE_BOUNDS in the device error word: nothing traps. TMA copies
+// need no check, the tensor map encoded from the same sizes bounds them (and
+// fills zeros outside). In the normal build the checks compile to nothing.
+#ifdef MAMBA_DEBUG_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+constexpr int kErrDeviceBounds = -9;  // MAMBA_ERR_DEVICE_BOUNDS
+
+// Whether the `count` values of type U at p lie inside the tensor that starts
+// at `base` and holds `extent` values of type T (a null tensor holds none).
+template <typename T, typename U>
+__host__ __device__ __forceinline__ bool span_inside(const T* base, size_t extent, const U* p, long long count) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(base), q = reinterpret_cast<uintptr_t>(p);
+    return base != nullptr && count >= 0 && q >= lo &&
+           q + sizeof(U) * static_cast<size_t>(count) <= lo + sizeof(T) * extent;
+}
+
+// True when the access lies inside its tensor (span_inside); in the checked
+// build an access outside it is recorded in *err and the caller skips it. In
+// the normal build: true, and nothing is computed.
+template <typename T, typename U>
+__device__ __forceinline__ bool in_bounds(int* err, const T* base, size_t extent, const U* p, long long count = 1) {
+    if constexpr (kCheckBounds) {
+        if (!span_inside(base, extent, p, count)) {
+            report_device_error(err, kErrDeviceBounds);
+            return false;
+        }
+    }
+    return true;
+}
+
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {

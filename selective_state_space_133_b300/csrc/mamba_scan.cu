@@ -26,6 +26,7 @@ using mhost::aligned;
 using mhost::round_up;
 
 constexpr int kKnownFlags = MAMBA_FLAG_SOFTPLUS | MAMBA_FLAG_ZOH;
+static_assert(mscan::kErrDeviceBounds == MAMBA_ERR_DEVICE_BOUNDS, "the kernels' bounds status is the ABI's");
 
 bool forward_dstate(int dstate) { return dstate == 8 || dstate == 16 || dstate == 32 || dstate == 64; }
 
@@ -90,10 +91,10 @@ bool mhost::make_map_3d(CUtensorMap* m, CUtensorMapDataType t, size_t es, const 
 namespace {
 
 template <typename T, int NS>
-void launch_pack(const void* B, const void* C, float* bc, int batch, int L, int Lp, cudaStream_t stream) {
+void launch_pack(const void* B, const void* C, float* bc, int batch, int L, int Lp, int* err, cudaStream_t stream) {
     const long long threads = static_cast<long long>(batch) * Lp;
     mscan::bc_pack_kernel<T, NS><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const T*>(B), static_cast<const T*>(C), bc, batch, L, Lp);
+        static_cast<const T*>(B), static_cast<const T*>(C), bc, batch, L, Lp, err);
 }
 
 // Streaming multiprocessors of the current device (looked up once per device).
@@ -232,6 +233,7 @@ int launch_bwd(mscan::ScanBwdArgs a, int flags, int dstate, const void* B, const
                char* ws, cudaStream_t stream) {
     const BwdWorkspace w = bwd_workspace(a.batch, a.dim, a.seqlen, dstate);
     a.Lp = w.Lp;
+    if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
     if (cudaMemsetAsync(a.dA, 0, static_cast<size_t>(a.dim) * dstate * sizeof(float), stream) != cudaSuccess)
         return MAMBA_ERR_CUDA;
     if (a.dD && cudaMemsetAsync(a.dD, 0, a.dim * sizeof(float), stream) != cudaSuccess) return MAMBA_ERR_CUDA;
@@ -245,10 +247,10 @@ int launch_bwd(mscan::ScanBwdArgs a, int flags, int dstate, const void* B, const
             return MAMBA_ERR_CUDA;
         float* bc = const_cast<float*>(a.bc);
         switch (dstate) {
-            case 8: launch_pack<T, 8>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
-            case 16: launch_pack<T, 16>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
-            case 32: launch_pack<T, 32>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
-            default: launch_pack<T, 64>(B, C, bc, a.batch, a.seqlen, w.Lp, stream); break;
+            case 8: launch_pack<T, 8>(B, C, bc, a.batch, a.seqlen, w.Lp, a.err, stream); break;
+            case 16: launch_pack<T, 16>(B, C, bc, a.batch, a.seqlen, w.Lp, a.err, stream); break;
+            case 32: launch_pack<T, 32>(B, C, bc, a.batch, a.seqlen, w.Lp, a.err, stream); break;
+            default: launch_pack<T, 64>(B, C, bc, a.batch, a.seqlen, w.Lp, a.err, stream); break;
         }
     }
     int st;
@@ -263,7 +265,7 @@ int launch_bwd(mscan::ScanBwdArgs a, int flags, int dstate, const void* B, const
         const long long total = static_cast<long long>(a.batch) * 2 * dstate * a.seqlen;
         const unsigned blocks = static_cast<unsigned>(std::min<long long>((total + 255) / 256, 148ll * 32));
         mscan::dbc_unpack_kernel<T><<<blocks, 256, 0, stream>>>(a.dbc, static_cast<T*>(dB), static_cast<T*>(dC),
-                                                               a.batch, dstate, a.seqlen, w.Lp);
+                                                               a.batch, dstate, a.seqlen, w.Lp, a.err);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
@@ -509,6 +511,7 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
     mscan::UpdateArgs a;
     a.state = state; a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C; a.A = A; a.D = D; a.bias = delta_bias;
     a.y = y; a.batch = batch; a.dim = dim; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool zoh = (flags & MAMBA_FLAG_ZOH) != 0;
     return io_dtype == MAMBA_BF16 ? launch_update<__nv_bfloat16>(a, dstate, zoh, s)
@@ -592,7 +595,7 @@ int mamba_ssd_fwd(const void* x, const void* delta, const float* A, const void* 
             const unsigned blocks = static_cast<unsigned>(std::min<long long>((rows[i] * seqlen + 255) / 256, 148ll * 16));
             mscan::row_pitch_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
                 static_cast<const __nv_bfloat16*>(src[i]), reinterpret_cast<__nv_bfloat16*>(ws + dst[i]), rows[i],
-                seqlen, w.pitch);
+                seqlen, w.pitch, a.err);
         }
         if (cudaGetLastError() != cudaSuccess) return MAMBA_ERR_CUDA;
         x = ws + w.x; B = ws + w.b; C = ws + w.c;
@@ -622,6 +625,7 @@ int mamba_ssd_update(float* state, const void* x, const void* delta, const float
     mscan::SsdUpdateArgs a;
     a.state = state; a.x = x; a.delta = delta; a.B = B; a.C = C; a.A = A; a.D = D; a.bias = delta_bias; a.y = y;
     a.batch = batch; a.nheads = nheads; a.headdim = headdim; a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (io_dtype == MAMBA_BF16) {
         if (dstate == 64) launch_ssd_update_n<__nv_bfloat16, 64>(a, s); else launch_ssd_update_n<__nv_bfloat16, 128>(a, s);
@@ -654,10 +658,13 @@ const char* mamba_status_string(int status) {
         case MAMBA_ERR_DEVICE_TIMEOUT: return "MAMBA_ERR_DEVICE_TIMEOUT: a kernel gave up waiting on its copies";
         case MAMBA_ERR_WORKSPACE: return "MAMBA_ERR_WORKSPACE: the workspace is smaller than mamba_scan_workspace_size";
         case MAMBA_ERR_FLAGS: return "MAMBA_ERR_FLAGS: an unknown flag bit, or one this entry point does not support";
+        case MAMBA_ERR_DEVICE_BOUNDS: return "MAMBA_ERR_DEVICE_BOUNDS: a kernel computed an index outside a tensor";
         default: return "unknown mamba_status";
     }
 }
 
 int mamba_version(void) { return 300; }
+
+int mamba_checked_bounds(void) { return mscan::kCheckBounds ? 1 : 0; }
 
 }  // extern "C"

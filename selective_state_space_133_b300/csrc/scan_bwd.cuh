@@ -62,6 +62,7 @@ struct ScanBwdArgs {
     float* dD;              // (dim) or null, zeroed by the host
     float* dbias;           // (dim) or null, zeroed by the host
     float* dh0;             // (batch, dim, N) or null
+    int* err;               // device error word
     int batch, dim, seqlen, Lp;
 };
 
@@ -146,27 +147,45 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
     const size_t rrow = static_cast<size_t>(b) * a.dim + rd;
     const size_t erow = static_cast<size_t>(b) * a.dim + ed;
     const bool vec_ok = eactive && (L % G::template vec_steps<T>()) == 0;
+    // extents (elements) of the tensors, for the checked-bounds build
+    const size_t nrows = static_cast<size_t>(a.batch) * a.dim;   // (batch, channel) rows
+    const size_t nx = nrows * L;                                  // u, delta, z, dy, du, ddelta, dz
+    const size_t npk = static_cast<size_t>(a.batch) * a.Lp;       // packed B/C rows, dB/dC sum columns
 
     float2 A2[H], IA[H];
 #pragma unroll
     for (int i = 0; i < H; ++i) {
-        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i);
+        const float* ap = a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i;
+        const float2 av = in_bounds(a.err, a.A, static_cast<size_t>(a.dim) * NS, ap, 2)
+            ? *reinterpret_cast<const float2*>(ap) : make_float2(-1.f, -1.f);
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
         if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);
     }
-    const float bias = a.bias ? a.bias[ed] : 0.f;
-    const float Dd = a.D ? a.D[ed] : 0.f;
+    const float bias = a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + ed) ? a.bias[ed] : 0.f;
+    const float Dd = a.D && in_bounds(a.err, a.D, a.dim, a.D + ed) ? a.D[ed] : 0.f;
     float* const hck = a.hck + rrow * n * NS + kS * rh;
     const float* const bcb = a.bc + static_cast<size_t>(b) * a.Lp * kCols;
 
     // the kSP values of the pre-pass lane's row at steps k*16 + kSP*ej .. (zero past L)
     auto loadN = [&](const void* base, int k, float (&v)[kSP]) {
         const int l = k * kBwdTL + kSP * ej;
-        ldg_n<kSP>(static_cast<const T*>(base) + erow * L + l, v, vec_ok && l + kSP <= L, eactive ? L - l : 0);
+        const T* tb = static_cast<const T*>(base);
+        const bool vec = vec_ok && l + kSP <= L;
+        const int valid = eactive ? L - l : 0;
+        if constexpr (kCheckBounds) {
+            if ((vec || valid > 0) && !in_bounds(a.err, tb, nx, tb + erow * L + l, vec ? kSP : min(valid, kSP))) {
+#pragma unroll
+                for (int i = 0; i < kSP; ++i) v[i] = 0.f;
+                return;
+            }
+        }
+        ldg_n<kSP>(tb + erow * L + l, v, vec, valid);
     };
     // the chunk's packed B/C rows (16 x 2N floats, contiguous) into shared memory
     auto stage_bc = [&](int k) {
-        const float4* src = reinterpret_cast<const float4*>(bcb + static_cast<size_t>(k) * kBwdTL * kCols);
+        const float* srcf = bcb + static_cast<size_t>(k) * kBwdTL * kCols;
+        if (!in_bounds(a.err, a.bc, npk * kCols, srcf, kBwdTL * kCols)) return;
+        const float4* src = reinterpret_cast<const float4*>(srcf);
         float4* dst = reinterpret_cast<float4*>(&sm.BC[0][0]);
 #pragma unroll
         for (int j = 0; j < kBwdTL * kCols / 128; ++j) dst[32 * j + lane] = src[32 * j + lane];
@@ -207,15 +226,17 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             }
         }
     };
-    auto store_h = [&](float* p, const float2 (&v)[H]) {
+    auto store_h = [&](float* base, size_t extent, float* p, const float2 (&v)[H]) {
+        if (!in_bounds(a.err, base, extent, p, kS)) return;
 #pragma unroll
         for (int q = 0; q < kS / 4; ++q)
             reinterpret_cast<float4*>(p)[q] = make_float4(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
     };
-    auto load_h = [&](const float* p, float2 (&v)[H]) {
+    auto load_h = [&](const float* base, size_t extent, const float* p, float2 (&v)[H]) {
+        const bool ok = in_bounds(a.err, base, extent, p, kS);
 #pragma unroll
         for (int q = 0; q < kS / 4; ++q) {
-            const float4 t = reinterpret_cast<const float4*>(p)[q];
+            const float4 t = ok ? reinterpret_cast<const float4*>(p)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
             v[2 * q] = make_float2(t.x, t.y);
             v[2 * q + 1] = make_float2(t.z, t.w);
         }
@@ -224,7 +245,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
     // ---------------------------------------------------- sweep 1: forward ----
     float2 h[H];
     if (a.h0) {
-        load_h(a.h0 + rrow * NS + kS * rh, h);
+        load_h(a.h0, nrows * NS, a.h0 + rrow * NS + kS * rh, h);
     } else {
 #pragma unroll
         for (int i = 0; i < H; ++i) h[i] = make_float2(0.f, 0.f);
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         prepass(k, false);
         stage_bc(k);
         __syncwarp();
-        if (ractive) store_h(hck + static_cast<size_t>(k) * NS, h);
+        if (ractive) store_h(a.hck, nrows * n * NS, hck + static_cast<size_t>(k) * NS, h);
 #pragma unroll
         for (int t = 0; t < kBwdTL; ++t) {
             const float2 w = sm.W[rc][t];
@@ -262,7 +283,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         const int le = l0 + kSP * ej;  // first step of the pre-pass lane's kSP
         // the chunk's checkpoint (issued first: its latency overlaps the pre-pass)
         float2 hs[H];
-        load_h(hck + static_cast<size_t>(k) * NS, hs);
+        load_h(a.hck, nrows * n * NS, hck + static_cast<size_t>(k) * NS, hs);
         // (i) dt, its second operand, d(dt)/dx and u per (channel, step), into shared memory
         prepass(k, true);
         stage_bc(k);
@@ -347,7 +368,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             }
             if (HAS_Z) {
                 T* dzp = static_cast<T*>(a.dz) + erow * L + le;
-                if (eactive && le < L) stg_n<kSP>(dzp, dzv, vec_ok && le + kSP <= L, L - le);
+                const bool vec = vec_ok && le + kSP <= L;
+                if (eactive && le < L && in_bounds(a.err, static_cast<T*>(a.dz), nx, dzp, vec ? kSP : min(L - le, kSP)))
+                    stg_n<kSP>(dzp, dzv, vec, L - le);
             }
         }
         __syncwarp();
@@ -445,7 +468,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
               const int col = lane + 32 * c;
               if (col < kCols) {
                   float* dcol = a.dbc + ((static_cast<size_t>(b) * 2 + col / NS) * NS + col % NS) * a.Lp + l0;
-                  red_add4(dcol + t0, make_float4(accBC[c][0], accBC[c][1], accBC[c][2], accBC[c][3]));
+                  if (in_bounds(a.err, a.dbc, npk * kCols, dcol + t0, 4))
+                      red_add4(dcol + t0, make_float4(accBC[c][0], accBC[c][1], accBC[c][2], accBC[c][3]));
               }
           }
         }
@@ -464,16 +488,22 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                 dbacc += dxv[i];
             }
             if (eactive && le < L) {
-                stg_n<kSP>(static_cast<T*>(a.du) + erow * L + le, duv, vec_ok && le + kSP <= L, L - le);
-                stg_n<kSP>(static_cast<T*>(a.ddelta) + erow * L + le, dxv, vec_ok && le + kSP <= L, L - le);
+                const bool vec = vec_ok && le + kSP <= L;
+                T* dup = static_cast<T*>(a.du) + erow * L + le;
+                T* ddp = static_cast<T*>(a.ddelta) + erow * L + le;
+                if (in_bounds(a.err, static_cast<T*>(a.du), nx, dup, vec ? kSP : min(L - le, kSP)))
+                    stg_n<kSP>(dup, duv, vec, L - le);
+                if (in_bounds(a.err, static_cast<T*>(a.ddelta), nx, ddp, vec ? kSP : min(L - le, kSP)))
+                    stg_n<kSP>(ddp, dxv, vec, L - le);
             }
         }
         __syncwarp();
     }
 
     // the gradient of the initial state, dA, dD and the bias's gradient
-    if (a.dh0 && ractive) store_h(a.dh0 + rrow * NS + kS * rh, g);
-    if (ractive) {
+    if (a.dh0 && ractive) store_h(a.dh0, nrows * NS, a.dh0 + rrow * NS + kS * rh, g);
+    if (ractive && in_bounds(a.err, a.dA, static_cast<size_t>(a.dim) * NS, a.dA + static_cast<size_t>(rd) * NS + kS * rh,
+                             kS)) {
         float* p = a.dA + static_cast<size_t>(rd) * NS + kS * rh;
 #pragma unroll
         for (int j = 0; j < H; ++j) {
@@ -487,8 +517,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         dbacc += __shfl_xor_sync(0xffffffffu, dbacc, o);
     }
     if (eactive && ej == 0) {
-        if (a.dD) atomicAdd(a.dD + ed, dDacc);
-        if (a.dbias) atomicAdd(a.dbias + ed, dbacc);
+        if (a.dD && in_bounds(a.err, a.dD, a.dim, a.dD + ed)) atomicAdd(a.dD + ed, dDacc);
+        if (a.dbias && in_bounds(a.err, a.dbias, a.dim, a.dbias + ed)) atomicAdd(a.dbias + ed, dbacc);
     }
 }
 
@@ -496,7 +526,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(256)
 dbc_unpack_kernel(const float* __restrict__ dbc, T* __restrict__ dB, T* __restrict__ dC, int batch, int ns, int L,
-                  int Lp) {
+                  int Lp, int* err) {
     const long long total = static_cast<long long>(batch) * 2 * ns * L;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -505,9 +535,12 @@ dbc_unpack_kernel(const float* __restrict__ dbc, T* __restrict__ dB, T* __restri
         const int nn = static_cast<int>(r % ns);
         const int which = static_cast<int>((r / ns) % 2);
         const int bb = static_cast<int>(r / (2 * ns));
+        const size_t nout = static_cast<size_t>(batch) * ns * L;
+        if (!in_bounds(err, dbc, static_cast<size_t>(batch) * 2 * ns * Lp, dbc + r * Lp + l)) continue;
         const float v = dbc[r * Lp + l];
         T* out = which ? dC : dB;
-        out[(static_cast<size_t>(bb) * ns + nn) * L + l] = Io<T>::from_f(v);
+        T* o = out + (static_cast<size_t>(bb) * ns + nn) * L + l;
+        if (in_bounds(err, out, nout, o)) *o = Io<T>::from_f(v);
     }
 }
 

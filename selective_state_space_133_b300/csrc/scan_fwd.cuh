@@ -285,6 +285,11 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     const int c0 = a.seg_chunks ? seg * a.seg_chunks : 0; // first chunk of this segment
     const int n = a.seg_chunks ? min(a.seg_chunks, nall - c0) : nall;  // its chunks
     const bool last_seg = c0 + n == nall;
+    // extents (elements) of the tensors, for the checked-bounds build
+    const size_t nrows = static_cast<size_t>(a.batch) * a.dim;        // (batch, channel) rows
+    const size_t nx = nrows * L;                                       // u, delta, z, y
+    const size_t nbc = static_cast<size_t>(a.batch) * NS * L;          // B, C
+    const size_t ncarry = (STATE ? gridDim.z : gridDim.z - 1) * nrows;  // carries of a split sequence
 
     const bool plain = a.plain != 0;  // warp-uniform
 
@@ -317,9 +322,9 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             const int c = i / kTL, s = i % kTL;
             const bool ok = d0 + c < a.dim && l0 + s < L;
             const size_t g = ok ? (static_cast<size_t>(b) * a.dim + d0 + c) * L + l0 + s : 0;
-            S.u[c][s] = ok ? ug[g] : zero;
-            S.dl[c][s] = ok ? dg[g] : zero;
-            if (HAS_Z) S.z[c][s] = ok ? zg[g] : zero;
+            S.u[c][s] = ok && in_bounds(a.err, ug, nx, ug + g) ? ug[g] : zero;
+            S.dl[c][s] = ok && in_bounds(a.err, dg, nx, dg + g) ? dg[g] : zero;
+            if (HAS_Z) S.z[c][s] = ok && in_bounds(a.err, zg, nx, zg + g) ? zg[g] : zero;
         }
         const T* bg = static_cast<const T*>(a.B);
         const T* cg = static_cast<const T*>(a.C);
@@ -327,8 +332,8 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             const int r = i / kTL, s = i % kTL;
             const bool ok = l0 + s < L;
             const size_t g = ok ? (static_cast<size_t>(b) * NS + r) * L + l0 + s : 0;
-            S.bc[0][r][s] = ok ? bg[g] : zero;
-            S.bc[1][r][s] = ok ? cg[g] : zero;
+            S.bc[0][r][s] = ok && in_bounds(a.err, bg, nbc, bg + g) ? bg[g] : zero;
+            S.bc[1][r][s] = ok && in_bounds(a.err, cg, nbc, cg + g) ? cg[g] : zero;
         }
     };
 
@@ -349,7 +354,9 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     float2 A2[H], IA[H];
 #pragma unroll
     for (int i = 0; i < H; ++i) {
-        const float2 av = *reinterpret_cast<const float2*>(a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i);
+        const float* ap = a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i;
+        const float2 av = in_bounds(a.err, a.A, static_cast<size_t>(a.dim) * NS, ap, 2)
+            ? *reinterpret_cast<const float2*>(ap) : make_float2(-1.f, -1.f);
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
         if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);  // inf at a = 0: that branch is never taken there
     }
@@ -360,11 +367,14 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         const size_t bd = static_cast<size_t>(a.batch) * a.dim;
         const size_t row = static_cast<size_t>(b) * a.dim + rd;
         for (int j = 0; j < seg; ++j) {
-            const float4* sp = reinterpret_cast<const float4*>(a.carry + (j * bd + row) * NS + kS * rh);
-            const float sdt = a.carry_dt[j * bd + row];
+            const float* cp = a.carry + (j * bd + row) * NS + kS * rh;
+            const float4* sp = reinterpret_cast<const float4*>(cp);
+            const bool cok = in_bounds(a.err, a.carry, ncarry * NS, cp, kS);
+            const float sdt = in_bounds(a.err, a.carry_dt, ncarry, a.carry_dt + j * bd + row)
+                ? a.carry_dt[j * bd + row] : 0.f;
 #pragma unroll
             for (int q = 0; q < kS / 4; ++q) {
-                const float4 p = sp[q];
+                const float4 p = cok ? sp[q] : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float2 s0 = make_float2(p.x, p.y), s1 = make_float2(p.z, p.w);
                 if (j == 0) {
                     h[2 * q] = s0;
@@ -378,11 +388,12 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
             }
         }
     } else if (seg == 0 && a.h0) {
-        const float4* hp = reinterpret_cast<const float4*>(a.h0 + (static_cast<size_t>(b) * a.dim + rd) * NS +
-                                                           kS * rh);
+        const float* h0p = a.h0 + (static_cast<size_t>(b) * a.dim + rd) * NS + kS * rh;
+        const float4* hp = reinterpret_cast<const float4*>(h0p);
+        const bool hok = in_bounds(a.err, a.h0, nrows * NS, h0p, kS);
 #pragma unroll
         for (int q = 0; q < kS / 4; ++q) {
-            const float4 p = hp[q];
+            const float4 p = hok ? hp[q] : make_float4(0.f, 0.f, 0.f, 0.f);
             h[2 * q] = make_float2(p.x, p.y);
             h[2 * q + 1] = make_float2(p.z, p.w);
         }
@@ -394,13 +405,16 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     const int ed = d0 + ec;
     const bool eactive = ed < a.dim;
     const int edc = eactive ? ed : a.dim - 1;
-    const float bias = a.bias ? a.bias[edc] : 0.f;
-    const float Dd = a.D ? a.D[edc] : 0.f;
+    const float bias = a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + edc) ? a.bias[edc] : 0.f;
+    const float Dd = a.D && in_bounds(a.err, a.D, a.dim, a.D + edc) ? a.D[edc] : 0.f;
     float cw[kConvW] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f;
     if (CONV) {
-        const float4 w4 = *reinterpret_cast<const float4*>(a.conv_w + static_cast<size_t>(edc) * kConvW);
-        cw[0] = w4.x; cw[1] = w4.y; cw[2] = w4.z; cw[3] = w4.w;
-        cb = a.conv_b ? a.conv_b[edc] : 0.f;
+        const float* wp = a.conv_w + static_cast<size_t>(edc) * kConvW;
+        if (in_bounds(a.err, a.conv_w, static_cast<size_t>(a.dim) * kConvW, wp, kConvW)) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wp);
+            cw[0] = w4.x; cw[1] = w4.y; cw[2] = w4.z; cw[3] = w4.w;
+        }
+        cb = a.conv_b && in_bounds(a.err, a.conv_b, a.dim, a.conv_b + edc) ? a.conv_b[edc] : 0.f;
         // the inputs before the segment's first step (read in the first
         // pre-pass): the convolution state before step 0, else the sequence's
         // own inputs before the segment
@@ -408,12 +422,15 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
             for (int m = 0; m < kConvW - 1; ++m) {
                 float x = 0.f;
-                if (c0 > 0 && eactive)
-                    x = Io<T>::to_f(static_cast<const T*>(a.u)[(static_cast<size_t>(b) * a.dim + ed) * L + c0 * kTL -
-                                                              (kConvW - 1) + m]);
-                else if (a.conv_state && eactive)
-                    x = Io<T>::to_f(static_cast<const T*>(a.conv_state)[(static_cast<size_t>(b) * a.dim + ed) *
-                                                                          (kConvW - 1) + m]);
+                const T* xg = static_cast<const T*>(a.u);
+                const T* sg = static_cast<const T*>(a.conv_state);
+                const size_t gx = (static_cast<size_t>(b) * a.dim + ed) * L + c0 * kTL - (kConvW - 1) + m;
+                const size_t gs = (static_cast<size_t>(b) * a.dim + ed) * (kConvW - 1) + m;
+                if (c0 > 0 && eactive) {
+                    if (in_bounds(a.err, xg, nx, xg + gx)) x = Io<T>::to_f(xg[gx]);
+                } else if (sg && eactive) {
+                    if (in_bounds(a.err, sg, nrows * (kConvW - 1), sg + gs)) x = Io<T>::to_f(sg[gs]);
+                }
                 sm.XH[(c0 + 1) & 1][ec][m] = x;
             }
         }
@@ -421,7 +438,8 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     float ukeep[kSP];  // u of this lane's pre-pass steps (after the convolution), kept for the epilogue
     float dt_sum = 0.f;  // state-only pass: the sum of dt over the segment (this lane's channel)
     // this lane's output: steps kSP*ej .. kSP*ej + kSP - 1 of every chunk of channel ed
-    T* const yrow = static_cast<T*>(a.y) + (static_cast<size_t>(b) * a.dim + edc) * L + kSP * ej;
+    T* const ybase = static_cast<T*>(a.y);
+    T* const yrow = ybase + (static_cast<size_t>(b) * a.dim + edc) * L + kSP * ej;
     const bool vec_ok = eactive && (L % G::template vec_steps<T>()) == 0;
 
     // Bounded wait for the tiles of the segment's chunk i (slot i % kStages);
@@ -674,14 +692,17 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         }
         const int l = k * kTL + kSP * ej;
         if (vec_ok && l + kSP <= L) {
-            stg_n<kSP>(yrow + k * kTL, y, true, kSP);
+            if (in_bounds(a.err, ybase, nx, yrow + k * kTL, kSP)) stg_n<kSP>(yrow + k * kTL, y, true, kSP);
         } else if (eactive && l < L) {
-            stg_n<kSP>(yrow + k * kTL, y, false, L - l);
+            if (in_bounds(a.err, ybase, nx, yrow + k * kTL, min(L - l, kSP)))
+                stg_n<kSP>(yrow + k * kTL, y, false, L - l);
         }
     };
 
-    // this lane's states as 16-byte groups, to global memory
-    auto store_state = [&](float* p) {
+    // this lane's states as 16-byte groups, to global memory (p inside the
+    // tensor of `extent` floats at `base`)
+    auto store_state = [&](float* base, size_t extent, float* p) {
+        if (!in_bounds(a.err, base, extent, p, kS)) return;
 #pragma unroll
         for (int q = 0; q < kS / 4; ++q)
             reinterpret_cast<float4*>(p)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
@@ -707,7 +728,7 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
         for (int i = 0; i < n; ++i) {
             const ScanStage<T, NS>& S = sm.st[i % kStages];
             // the state before chunk c0 + i, for the backward
-            if (ck_store) store_state(ck + static_cast<size_t>(c0 + i) * NS);
+            if (ck_store) store_state(a.chunk_states, nrows * nall * NS, ck + static_cast<size_t>(c0 + i) * NS);
             recurrence();
             __syncwarp();
             if (!STATE) epilogue(S, c0 + i);
@@ -726,11 +747,11 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
     if (STATE) {  // the segment's end state and its sum of dt, for the segments after it
         if (d0 + rc < a.dim) {
             const size_t row = static_cast<size_t>(seg) * a.batch * a.dim + static_cast<size_t>(b) * a.dim + d0 + rc;
-            store_state(a.carry + row * NS + kS * rh);
-            if (rh == 0) a.carry_dt[row] = dt_sum;
+            store_state(a.carry, ncarry * NS, a.carry + row * NS + kS * rh);
+            if (rh == 0 && in_bounds(a.err, a.carry_dt, ncarry, a.carry_dt + row)) a.carry_dt[row] = dt_sum;
         }
     } else if (a.final_state && last_seg && d0 + rc < a.dim) {
-        store_state(a.final_state + (static_cast<size_t>(b) * a.dim + d0 + rc) * NS + kS * rh);
+        store_state(a.final_state, nrows * NS, a.final_state + (static_cast<size_t>(b) * a.dim + d0 + rc) * NS + kS * rh);
     }
 }
 
@@ -741,14 +762,16 @@ scan_fwd_kernel(const ScanArgs a, const __grid_constant__ CUtensorMap tm_u,
 template <typename T, int NS>
 __global__ void __launch_bounds__(256)
 bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restrict__ out, int batch, int L,
-               int Lp) {
+               int Lp, int* err) {
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<long long>(batch) * Lp) return;
     const int b = static_cast<int>(i / Lp);
     const int l = static_cast<int>(i % Lp);
     const bool ok = l < L;
     const size_t base = static_cast<size_t>(b) * NS * L + l;
+    const size_t nbc = static_cast<size_t>(batch) * NS * L;
     float4* o = reinterpret_cast<float4*>(out + i * (2 * NS));
+    if (!in_bounds(err, out, static_cast<size_t>(batch) * Lp * 2 * NS, out + i * (2 * NS), 2 * NS)) return;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
         const T* src = which ? C : B;
@@ -756,7 +779,10 @@ bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restri
         for (int s = 0; s < NS; s += 4) {
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = ok ? Io<T>::to_f(src[base + static_cast<size_t>(s + j) * L]) : 0.f;
+            for (int j = 0; j < 4; ++j) {
+                const T* q = src + base + static_cast<size_t>(s + j) * L;
+                v[j] = ok && in_bounds(err, src, nbc, q) ? Io<T>::to_f(*q) : 0.f;
+            }
             o[(which * NS + s) / 4] = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
@@ -768,13 +794,15 @@ bc_pack_kernel(const T* __restrict__ B, const T* __restrict__ C, float* __restri
 // map cannot stride over.
 template <typename T>
 __global__ void __launch_bounds__(256)
-row_pitch_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, int L, int Lpitch) {
+row_pitch_kernel(const T* __restrict__ src, T* __restrict__ dst, long long rows, int L, int Lpitch, int* err) {
     const long long total = rows * L;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long r = i / L;
         const int l = static_cast<int>(i - r * L);
-        dst[r * Lpitch + l] = src[i];
+        if (in_bounds(err, src, static_cast<size_t>(total), src + i) &&
+            in_bounds(err, dst, static_cast<size_t>(rows) * Lpitch, dst + r * Lpitch + l))
+            dst[r * Lpitch + l] = src[i];
     }
 }
 

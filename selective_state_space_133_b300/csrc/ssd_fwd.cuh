@@ -193,10 +193,14 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const int n = (L + kSsdQ - 1) / kSsdQ;
     const int dim = a.nheads * kSsdP;
     const int ch0 = h * kSsdP;  // first channel of the head
-    const float Ah2 = a.A[h] * kLog2e;
-    const float bias = a.bias ? a.bias[h] : 0.f;
-    const float Dh = a.D ? a.D[h] : 0.f;
+    const float Ah2 = (in_bounds(a.err, a.A, a.nheads, a.A + h) ? a.A[h] : -1.f) * kLog2e;
+    const float bias = a.bias && in_bounds(a.err, a.bias, a.nheads, a.bias + h) ? a.bias[h] : 0.f;
+    const float Dh = a.D && in_bounds(a.err, a.D, a.nheads, a.D + h) ? a.D[h] : 0.f;
     const size_t head_row = static_cast<size_t>(b) * a.nheads + h;
+    // extents (elements) of the tensors, for the checked-bounds build
+    const size_t nheads_all = static_cast<size_t>(a.batch) * a.nheads;   // (batch, head) rows
+    const size_t nstate = nheads_all * kSsdP * NS;                         // h0, final state
+    const size_t ny = nheads_all * kSsdP * L;                              // y
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
@@ -239,8 +243,10 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     const bool have_state = a.h0 != nullptr;
     float S[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        S[j] = (have_state && sact) ? a.h0[(head_row * kSsdP + 32 * half + j) * NS + sn] : 0.f;
+    for (int j = 0; j < 32; ++j) {
+        const float* hp = a.h0 + (head_row * kSsdP + 32 * half + j) * NS + sn;
+        S[j] = (have_state && sact && in_bounds(a.err, a.h0, nstate, hp)) ? *hp : 0.f;
+    }
     // the state's high and low parts as the Y1 product's operand: row n, this
     // thread's 32 channels as four 16-byte units of each part
     auto store_state_parts = [&]() {
@@ -268,7 +274,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int gl = k * kSsdQ + 2 * lane + i;
-            r[i] = gl < L ? __bfloat162float(dl[gl]) : 0.f;
+            r[i] = gl < L && in_bounds(a.err, static_cast<const __nv_bfloat16*>(a.delta), nheads_all * L, dl + gl)
+                ? __bfloat162float(dl[gl]) : 0.f;
         }
     };
     auto decay_prefix = [&](int k, const float (&r)[2]) {
@@ -335,6 +342,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             if (gl >= L) continue;
             __nv_bfloat16* dst = yb + static_cast<size_t>(p) * L + gl;
             const __nv_bfloat16* src = yt + p * kSsdYPitch + lc;
+            if (!in_bounds(a.err, static_cast<__nv_bfloat16*>(a.y), ny, dst, min(8, L - gl))) continue;
             if (vec_ok && gl + 8 <= L) {
                 *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
             } else {
@@ -562,7 +570,10 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 
     if (a.final_state && sact) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) a.final_state[(head_row * kSsdP + 32 * half + j) * NS + sn] = S[j];
+        for (int j = 0; j < 32; ++j) {
+            float* fp = a.final_state + (head_row * kSsdP + 32 * half + j) * NS + sn;
+            if (in_bounds(a.err, a.final_state, nstate, fp)) *fp = S[j];
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -34,6 +34,7 @@ struct UpdateArgs {
     const float* D;     // may be null
     const float* bias;  // may be null
     void* y;
+    int* err;           // device error word
     int batch, dim;
     int softplus;
 };
@@ -68,22 +69,29 @@ __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const Upda
     const T* u = static_cast<const T*>(a.u);
     const T* dl = static_cast<const T*>(a.delta);
 
+    const size_t nrows = static_cast<size_t>(a.batch) * a.dim;  // extents, for the checked-bounds build
+
     // B, C of this batch row: the same for every row of the block
-    float2 B01, B23, C01, C23;
-    ldg4(static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q, B01, B23);
-    ldg4(static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q, C01, C23);
+    float2 B01 = {}, B23 = {}, C01 = {}, C23 = {};
+    const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q;
+    const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q;
+    if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4)) ldg4(Bp, B01, B23);
+    if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4)) ldg4(Cp, C01, C23);
 
     // all loads first
     const int d = blockIdx.x * UpdateGeo<NS>::kRows + threadIdx.x / kQ;
     const int dc = d < a.dim ? d : a.dim - 1;  // padding lanes recompute the last channel, store nothing
     const size_t row = static_cast<size_t>(b) * a.dim + dc;
-    const float4 s4 = *reinterpret_cast<const float4*>(a.state + row * NS + 4 * q);
-    float2 A01, A23;
-    ldg4(a.A + static_cast<size_t>(dc) * NS + 4 * q, A01, A23);
-    const float uu = Io<T>::to_f(u[row]);
-    const float dv = Io<T>::to_f(dl[row]);
+    float* const sp = a.state + row * NS + 4 * q;
+    const bool sok = in_bounds(a.err, a.state, nrows * NS, sp, 4);
+    const float4 s4 = sok ? *reinterpret_cast<const float4*>(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 A01 = make_float2(-1.f, -1.f), A23 = make_float2(-1.f, -1.f);
+    const float* Ap = a.A + static_cast<size_t>(dc) * NS + 4 * q;
+    if (in_bounds(a.err, a.A, static_cast<size_t>(a.dim) * NS, Ap, 4)) ldg4(Ap, A01, A23);
+    const float uu = in_bounds(a.err, u, nrows, u + row) ? Io<T>::to_f(u[row]) : 0.f;
+    const float dv = in_bounds(a.err, dl, nrows, dl + row) ? Io<T>::to_f(dl[row]) : 0.f;
 
-    float dt = dv + (a.bias ? a.bias[dc] : 0.f);
+    float dt = dv + (a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + dc) ? a.bias[dc] : 0.f);
     if (a.softplus) dt = softplus_f(dt);
     const float2 dlt = make_float2(dt * kLog2e, dt * kLog2e);
     const float2 w = make_float2(dt * uu, dt * uu);
@@ -112,11 +120,13 @@ __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const Upda
 #pragma unroll
     for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
     if (d < a.dim) {
-        *reinterpret_cast<float4*>(a.state + row * NS + 4 * q) = make_float4(h01.x, h01.y, h23.x, h23.y);
+        if (sok) *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
         if (q == 0) {
-            float yy = a.D ? fmaf(a.D[d], uu, yp) : yp;
-            if (a.z) yy *= silu_f(Io<T>::to_f(static_cast<const T*>(a.z)[row]));
-            static_cast<T*>(a.y)[row] = Io<T>::from_f(yy);
+            float yy = a.D && in_bounds(a.err, a.D, a.dim, a.D + d) ? fmaf(a.D[d], uu, yp) : yp;
+            const T* zg = static_cast<const T*>(a.z);
+            if (zg && in_bounds(a.err, zg, nrows, zg + row)) yy *= silu_f(Io<T>::to_f(zg[row]));
+            T* yg = static_cast<T*>(a.y);
+            if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
         }
     }
 }
@@ -142,6 +152,7 @@ struct SsdUpdateArgs {
     const float* D;      // (nheads) or null
     const float* bias;   // (nheads) or null
     void* y;             // (batch, nheads * headdim)
+    int* err;            // device error word
     int batch, nheads, headdim;
     int softplus;
 };
@@ -157,16 +168,25 @@ __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpd
     const int dc = d < dim ? d : dim - 1;            // padding lanes recompute the last row, store nothing
     const int h = dc / a.headdim;
     const size_t row = static_cast<size_t>(b) * dim + dc;
+    const size_t nrows = static_cast<size_t>(a.batch) * dim;  // extents, for the checked-bounds build
     // all loads first
-    const float4 s4 = *reinterpret_cast<const float4*>(a.state + row * NS + 4 * q);
-    float2 B01, B23, C01, C23;
-    ldg4(static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q, B01, B23);
-    ldg4(static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q, C01, C23);
-    const float xv = Io<T>::to_f(static_cast<const T*>(a.x)[row]);
-    float dt = Io<T>::to_f(static_cast<const T*>(a.delta)[static_cast<size_t>(b) * a.nheads + h]) +
-               (a.bias ? a.bias[h] : 0.f);
+    float* const sp = a.state + row * NS + 4 * q;
+    const bool sok = in_bounds(a.err, a.state, nrows * NS, sp, 4);
+    const float4 s4 = sok ? *reinterpret_cast<const float4*>(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 B01 = {}, B23 = {}, C01 = {}, C23 = {};
+    const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q;
+    const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q;
+    if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4)) ldg4(Bp, B01, B23);
+    if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4)) ldg4(Cp, C01, C23);
+    const T* xg = static_cast<const T*>(a.x);
+    const T* dg = static_cast<const T*>(a.delta);
+    const size_t hrow = static_cast<size_t>(b) * a.nheads + h;
+    const float xv = in_bounds(a.err, xg, nrows, xg + row) ? Io<T>::to_f(xg[row]) : 0.f;
+    float dt = (in_bounds(a.err, dg, static_cast<size_t>(a.batch) * a.nheads, dg + hrow) ? Io<T>::to_f(dg[hrow]) : 0.f) +
+               (a.bias && in_bounds(a.err, a.bias, a.nheads, a.bias + h) ? a.bias[h] : 0.f);
     if (a.softplus) dt = softplus_f(dt);
-    const float decay = ex2_approx(dt * a.A[h] * kLog2e);
+    const float Ah = in_bounds(a.err, a.A, a.nheads, a.A + h) ? a.A[h] : -1.f;
+    const float decay = ex2_approx(dt * Ah * kLog2e);
     const float2 ea = make_float2(decay, decay);
     const float2 w = make_float2(dt * xv, dt * xv);
     const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, B01));
@@ -176,10 +196,11 @@ __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpd
 #pragma unroll
     for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
     if (d < dim) {
-        *reinterpret_cast<float4*>(a.state + row * NS + 4 * q) = make_float4(h01.x, h01.y, h23.x, h23.y);
+        if (sok) *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
         if (q == 0) {
-            const float yy = a.D ? fmaf(a.D[h], xv, yp) : yp;
-            static_cast<T*>(a.y)[row] = Io<T>::from_f(yy);
+            const float yy = a.D && in_bounds(a.err, a.D, a.nheads, a.D + h) ? fmaf(a.D[h], xv, yp) : yp;
+            T* yg = static_cast<T*>(a.y);
+            if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
         }
     }
 }

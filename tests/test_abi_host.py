@@ -31,8 +31,56 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_checked_bounds_build_exports_the_same_abi(L):
+    """The checked-bounds testing build loads, exports every declared symbol and says which it is."""
+    C = _lib.load(build.build_library(checked=True))
+    for name in declared_functions():
+        assert hasattr(C, name), name
+    assert C.mamba_checked_bounds() == 1 and L.mamba_checked_bounds() == 0
+    assert C.mamba_status_string(-9).decode().startswith("MAMBA_ERR_DEVICE_BOUNDS")
+
+
+SPAN_HARNESS = r"""
+#include <cstdio>
+#include "common.cuh"
+using mscan::span_inside;
+int main() {
+    static float t[10];
+    const float* b = t;
+    int bad = 0;
+    auto expect = [&](bool got, bool want, int line) { if (got != want) { std::printf("case %d\n", line); ++bad; } };
+    expect(span_inside(b, 10, b, 10), true, __LINE__);                      // the whole tensor
+    expect(span_inside(b, 10, b + 9, 1), true, __LINE__);                   // the last element
+    expect(span_inside(b, 10, b + 9, 2), false, __LINE__);                  // one past the end
+    expect(span_inside(b, 10, b + 10, 1), false, __LINE__);                 // starts at the end
+    expect(span_inside(b, 10, b - 1, 1), false, __LINE__);                  // before the start
+    expect(span_inside(b, 10, b + 10, 0), true, __LINE__);                  // empty access at the end
+    expect(span_inside(b, 10, b, -1), false, __LINE__);                     // negative count
+    expect(span_inside(static_cast<const float*>(nullptr), 10, b, 1), false, __LINE__);  // null tensor
+    expect(span_inside(b, 10, reinterpret_cast<const float4*>(b + 6), 1), true, __LINE__);   // 16 bytes, last 4
+    expect(span_inside(b, 10, reinterpret_cast<const float4*>(b + 7), 1), false, __LINE__);  // 16 bytes, 1 over
+    expect(span_inside(reinterpret_cast<const unsigned short*>(b), 20, b + 4, 6), true, __LINE__);  // mixed types
+    expect(span_inside(reinterpret_cast<const unsigned short*>(b), 19, b + 4, 6), false, __LINE__);
+    std::printf("%d bad\n", bad);
+    return bad != 0;
+}
+"""
+
+
+def test_span_check_of_the_checked_build(tmp_path):
+    """The extent test the checked build applies to every access, run on the host over its edge cases."""
+    import subprocess
+    src = tmp_path / "span.cu"
+    src.write_text(SPAN_HARNESS)
+    exe = tmp_path / "span"
+    subprocess.run([build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-DMAMBA_DEBUG_BOUNDS",
+                    "-I", build.CSRC, str(src), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "0 bad", r.stdout
+
+
 def test_status_strings(L):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         s = L.mamba_status_string(code).decode()
         assert s.startswith(_lib.STATUS[code])
     assert L.mamba_status_string(42).decode() == "unknown mamba_status"
