@@ -183,15 +183,15 @@ int launch_scan(mscan::ScanArgs a, int flags, int dstate, const SplitPlan& plan,
 
 template <typename T, int NS>
 void launch_update_n(const mscan::UpdateArgs& a, bool zoh, cudaStream_t stream) {
-    constexpr int rows = mscan::UpdateGeo<NS>::kRows;
-    const dim3 grid((a.dim + rows - 1) / rows, a.batch);
+    using G = mscan::UpdateGeo<NS>;
+    const dim3 grid((a.dim + G::kCh - 1) / G::kCh, (a.batch + G::kR - 1) / G::kR);
     if (zoh) mscan::state_update_kernel<T, NS, true><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
     else mscan::state_update_kernel<T, NS, false><<<grid, mscan::kUpdateThreads, 0, stream>>>(a);
 }
 
 template <typename T, int NS>
 void launch_ssd_update_n(const mscan::SsdUpdateArgs& a, cudaStream_t s) {
-    constexpr int rows = mscan::kUpdateThreads / (NS / 4);
+    constexpr int rows = mscan::SsdUpdateGeo<NS>::kRows;
     const dim3 grid((a.nheads * a.headdim + rows - 1) / rows, a.batch);
     mscan::ssd_update_kernel<T, NS><<<grid, mscan::kUpdateThreads, 0, s>>>(a);
 }

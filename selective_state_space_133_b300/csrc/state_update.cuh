@@ -15,8 +15,13 @@
 // (B, C) or channel (A). N/4 lanes share a row, each owning 4 consecutive
 // states, so a warp moves 512 contiguous bytes of state per load and store;
 // the partial C.h sums are added with xor-shuffles inside the lane group.
-// All of a row's loads are issued before any arithmetic. The grid is
-// (channels / rows per block, batch), so no thread divides to find its row.
+// A thread takes the same channel in kR consecutive batch rows: A, D and the
+// bias of the channel are loaded once for all of them, and their states
+// (16 bytes each) are copied into shared memory with asynchronous copies
+// before any arithmetic, so that the copies in flight hold no registers and a
+// full SM of threads keeps enough bytes in flight to cover the memory latency
+// at full bandwidth. The block's B and C rows are staged in shared memory as
+// fp32. The grid is (channels / channels per block, batch rows / kR).
 #pragma once
 
 #include "common.cuh"
@@ -39,14 +44,15 @@ struct UpdateArgs {
     int softplus;
 };
 
-constexpr int kUpdateThreads = 256;
+constexpr int kUpdateThreads = 128;
 
 // Lanes per row and rows per block of the state update for state size NS.
 template <int NS>
 struct UpdateGeo {
     static_assert(NS == 8 || NS == 16 || NS == 32 || NS == 64, "state sizes 8, 16, 32 and 64 are compiled");
     static constexpr int kQ = NS / 4;                       // lanes per row, 4 states each
-    static constexpr int kRows = kUpdateThreads / kQ;       // rows (channels) per block
+    static constexpr int kCh = kUpdateThreads / kQ;         // channels per block
+    static constexpr int kR = 4;                            // batch rows per thread (and per block)
 };
 
 // Four consecutive values (16-byte aligned for fp32, 8-byte for bf16) as fp32 pairs.
@@ -63,70 +69,96 @@ __device__ __forceinline__ void ldg4(const __nv_bfloat16* p, float2& lo, float2&
 
 template <typename T, int NS, bool ZOH>
 __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const UpdateArgs a) {
-    constexpr int kQ = UpdateGeo<NS>::kQ;
-    const int b = blockIdx.y;
-    const int q = threadIdx.x % kQ;
+    using G = UpdateGeo<NS>;
+    constexpr int kQ = G::kQ, kR = G::kR;
+    __shared__ float4 stage[kR][kUpdateThreads];  // the state of each of this thread's rows
+    __shared__ alignas(16) float bc[kR][2][NS];     // B and C of the block's batch rows
+    const int tid = threadIdx.x;
+    const int q = tid % kQ;
+    const int b0 = blockIdx.y * kR;
+    const int d = blockIdx.x * G::kCh + tid / kQ;
+    const int dc = d < a.dim ? d : a.dim - 1;  // padding lanes recompute the last channel, store nothing
     const T* u = static_cast<const T*>(a.u);
     const T* dl = static_cast<const T*>(a.delta);
-
+    const T* zg = static_cast<const T*>(a.z);
     const size_t nrows = static_cast<size_t>(a.batch) * a.dim;  // extents, for the checked-bounds build
 
-    // B, C of this batch row: the same for every row of the block
-    float2 B01 = {}, B23 = {}, C01 = {}, C23 = {};
-    const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q;
-    const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q;
-    if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4)) ldg4(Bp, B01, B23);
-    if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4)) ldg4(Cp, C01, C23);
-
-    // all loads first
-    const int d = blockIdx.x * UpdateGeo<NS>::kRows + threadIdx.x / kQ;
-    const int dc = d < a.dim ? d : a.dim - 1;  // padding lanes recompute the last channel, store nothing
-    const size_t row = static_cast<size_t>(b) * a.dim + dc;
-    float* const sp = a.state + row * NS + 4 * q;
-    const bool sok = in_bounds(a.err, a.state, nrows * NS, sp, 4);
-    const float4 s4 = sok ? *reinterpret_cast<const float4*>(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // every load first: the states (asynchronous), then the rest
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        const float* sp = a.state + (static_cast<size_t>(b0 + r) * a.dim + dc) * NS + 4 * q;
+        if (b0 + r < a.batch && in_bounds(a.err, a.state, nrows * NS, sp, 4)) cp_async16(&stage[r][tid], sp);
+    }
+    for (int i = tid; i < kR * 2 * NS; i += kUpdateThreads) {
+        const int r = i / (2 * NS), which = (i / NS) % 2, n = i % NS;
+        const T* src = static_cast<const T*>(which ? a.C : a.B) + static_cast<size_t>(b0 + r) * NS + n;
+        bc[r][which][n] = b0 + r < a.batch && in_bounds(a.err, static_cast<const T*>(which ? a.C : a.B),
+                                                        static_cast<size_t>(a.batch) * NS, src)
+            ? Io<T>::to_f(*src) : 0.f;
+    }
     float2 A01 = make_float2(-1.f, -1.f), A23 = make_float2(-1.f, -1.f);
     const float* Ap = a.A + static_cast<size_t>(dc) * NS + 4 * q;
     if (in_bounds(a.err, a.A, static_cast<size_t>(a.dim) * NS, Ap, 4)) ldg4(Ap, A01, A23);
-    const float uu = in_bounds(a.err, u, nrows, u + row) ? Io<T>::to_f(u[row]) : 0.f;
-    const float dv = in_bounds(a.err, dl, nrows, dl + row) ? Io<T>::to_f(dl[row]) : 0.f;
-
-    float dt = dv + (a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + dc) ? a.bias[dc] : 0.f);
-    if (a.softplus) dt = softplus_f(dt);
-    const float2 dlt = make_float2(dt * kLog2e, dt * kLog2e);
-    const float2 w = make_float2(dt * uu, dt * uu);
-    float2 h01 = make_float2(s4.x, s4.y), h23 = make_float2(s4.z, s4.w);
-    const float2 x01 = __fmul2_rn(dlt, A01), x23 = __fmul2_rn(dlt, A23);
-    float2 g01, g23;  // input terms
-    if (ZOH) {
-        // (exp(dt a) - 1) / a per state, dt where dt*a = 0 (its limit)
-        const float av[4] = {A01.x, A01.y, A23.x, A23.y};
-        float gv[4];
+    const float bias = a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + dc) ? a.bias[dc] : 0.f;
+    const float Dd = a.D && q == 0 && in_bounds(a.err, a.D, a.dim, a.D + dc) ? a.D[dc] : 0.f;
+    float uu[kR], dv[kR], zz[kR];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x = dt * av[i];
-            gv[i] = (x == 0.f ? dt : expm1f(x) / av[i]) * uu;
-        }
-        g01 = __fmul2_rn(make_float2(gv[0], gv[1]), B01);
-        g23 = __fmul2_rn(make_float2(gv[2], gv[3]), B23);
-    } else {
-        g01 = __fmul2_rn(w, B01);
-        g23 = __fmul2_rn(w, B23);
+    for (int r = 0; r < kR; ++r) {
+        const size_t row = static_cast<size_t>(b0 + r < a.batch ? b0 + r : a.batch - 1) * a.dim + dc;
+        uu[r] = in_bounds(a.err, u, nrows, u + row) ? Io<T>::to_f(u[row]) : 0.f;
+        dv[r] = in_bounds(a.err, dl, nrows, dl + row) ? Io<T>::to_f(dl[row]) : 0.f;
+        zz[r] = zg && q == 0 && in_bounds(a.err, zg, nrows, zg + row) ? Io<T>::to_f(zg[row]) : 0.f;
     }
-    h01 = __ffma2_rn(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, g01);
-    h23 = __ffma2_rn(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, g23);
-    const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
-    float yp = acc.x + acc.y;
+    cp_async_wait_all();
+    __syncthreads();  // bc, written by other threads
+
 #pragma unroll
-    for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
-    if (d < a.dim) {
-        if (sok) *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
-        if (q == 0) {
-            float yy = a.D && in_bounds(a.err, a.D, a.dim, a.D + d) ? fmaf(a.D[d], uu, yp) : yp;
-            const T* zg = static_cast<const T*>(a.z);
-            if (zg && in_bounds(a.err, zg, nrows, zg + row)) yy *= silu_f(Io<T>::to_f(zg[row]));
-            T* yg = static_cast<T*>(a.y);
-            if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
+    for (int r = 0; r < kR; ++r) {
+        if (b0 + r >= a.batch) break;
+        const float4 s4 = stage[r][tid];
+        const float4 b4 = *reinterpret_cast<const float4*>(&bc[r][0][4 * q]);
+        const float4 c4 = *reinterpret_cast<const float4*>(&bc[r][1][4 * q]);
+        const float2 B01 = make_float2(b4.x, b4.y), B23 = make_float2(b4.z, b4.w);
+        const float2 C01 = make_float2(c4.x, c4.y), C23 = make_float2(c4.z, c4.w);
+        float dt = dv[r] + bias;
+        if (a.softplus) dt = softplus_f(dt);
+        const float2 dlt = make_float2(dt * kLog2e, dt * kLog2e);
+        const float2 w = make_float2(dt * uu[r], dt * uu[r]);
+        float2 h01 = make_float2(s4.x, s4.y), h23 = make_float2(s4.z, s4.w);
+        const float2 x01 = __fmul2_rn(dlt, A01), x23 = __fmul2_rn(dlt, A23);
+        float2 g01, g23;  // input terms
+        if (ZOH) {
+            // (exp(dt a) - 1) / a per state, dt where dt*a = 0 (its limit)
+            const float av[4] = {A01.x, A01.y, A23.x, A23.y};
+            float gv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x = dt * av[i];
+                gv[i] = (x == 0.f ? dt : expm1f(x) / av[i]) * uu[r];
+            }
+            g01 = __fmul2_rn(make_float2(gv[0], gv[1]), B01);
+            g23 = __fmul2_rn(make_float2(gv[2], gv[3]), B23);
+        } else {
+            g01 = __fmul2_rn(w, B01);
+            g23 = __fmul2_rn(w, B23);
+        }
+        h01 = __ffma2_rn(make_float2(ex2_approx(x01.x), ex2_approx(x01.y)), h01, g01);
+        h23 = __ffma2_rn(make_float2(ex2_approx(x23.x), ex2_approx(x23.y)), h23, g23);
+        const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
+        float yp = acc.x + acc.y;
+#pragma unroll
+        for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+        if (d < a.dim) {
+            const size_t row = static_cast<size_t>(b0 + r) * a.dim + d;
+            float* sp = a.state + row * NS + 4 * q;
+            if (in_bounds(a.err, a.state, nrows * NS, sp, 4))
+                *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
+            if (q == 0) {
+                float yy = a.D ? fmaf(Dd, uu[r], yp) : yp;
+                if (zg) yy *= silu_f(zz[r]);
+                T* yg = static_cast<T*>(a.y);
+                if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
+            }
         }
     }
 }
@@ -140,7 +172,9 @@ __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const Upda
 //     y[b,h*P+p] = S[p,:] . C[b,:] + D[h] x[b,h*P+p]
 // Bound by HBM like the scan's state update: each state row (4N bytes) is
 // read and written once. N/4 lanes share a row, 4 states each, and add their
-// partial C.S with xor-shuffles.
+// partial C.S with xor-shuffles. A thread takes kR rows of the same batch row,
+// which share B and C (loaded once), and copies their states into shared
+// memory with asynchronous copies before any arithmetic.
 
 struct SsdUpdateArgs {
     float* state;        // (batch, nheads, headdim, N) fp32, in place
@@ -157,50 +191,81 @@ struct SsdUpdateArgs {
     int softplus;
 };
 
+template <int NS>
+struct SsdUpdateGeo {
+    static constexpr int kQ = NS / 4;                    // lanes per row (a power of two up to 32)
+    static constexpr int kPass = kUpdateThreads / kQ;    // rows the block's threads cover at once
+    static constexpr int kR = 4;                         // rows per thread
+    static constexpr int kRows = kPass * kR;             // rows per block
+};
+
 template <typename T, int NS>
 __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpdateArgs a) {
-    constexpr int kQ = NS / 4;                       // lanes per row (a power of two up to 32)
-    constexpr int kRows = kUpdateThreads / kQ;       // rows per block
+    using G = SsdUpdateGeo<NS>;
+    constexpr int kQ = G::kQ, kR = G::kR;
+    __shared__ float4 stage[kR][kUpdateThreads];  // the state of each of this thread's rows
+    const int tid = threadIdx.x;
     const int b = blockIdx.y;
-    const int q = threadIdx.x % kQ;
+    const int q = tid % kQ;
     const int dim = a.nheads * a.headdim;
-    const int d = blockIdx.x * kRows + threadIdx.x / kQ;
-    const int dc = d < dim ? d : dim - 1;            // padding lanes recompute the last row, store nothing
-    const int h = dc / a.headdim;
-    const size_t row = static_cast<size_t>(b) * dim + dc;
     const size_t nrows = static_cast<size_t>(a.batch) * dim;  // extents, for the checked-bounds build
-    // all loads first
-    float* const sp = a.state + row * NS + 4 * q;
-    const bool sok = in_bounds(a.err, a.state, nrows * NS, sp, 4);
-    const float4 s4 = sok ? *reinterpret_cast<const float4*>(sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const T* xg = static_cast<const T*>(a.x);
+    const T* dg = static_cast<const T*>(a.delta);
+    // every load first: the states (asynchronous), then the rest
+    int dcs[kR];
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        const int d = blockIdx.x * G::kRows + r * G::kPass + tid / kQ;
+        dcs[r] = d < dim ? d : dim - 1;  // padding lanes recompute the last row, store nothing
+        const float* sp = a.state + (static_cast<size_t>(b) * dim + dcs[r]) * NS + 4 * q;
+        if (in_bounds(a.err, a.state, nrows * NS, sp, 4)) cp_async16(&stage[r][tid], sp);
+        else stage[r][tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float2 B01 = {}, B23 = {}, C01 = {}, C23 = {};
     const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q;
     const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q;
     if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4)) ldg4(Bp, B01, B23);
     if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4)) ldg4(Cp, C01, C23);
-    const T* xg = static_cast<const T*>(a.x);
-    const T* dg = static_cast<const T*>(a.delta);
-    const size_t hrow = static_cast<size_t>(b) * a.nheads + h;
-    const float xv = in_bounds(a.err, xg, nrows, xg + row) ? Io<T>::to_f(xg[row]) : 0.f;
-    float dt = (in_bounds(a.err, dg, static_cast<size_t>(a.batch) * a.nheads, dg + hrow) ? Io<T>::to_f(dg[hrow]) : 0.f) +
-               (a.bias && in_bounds(a.err, a.bias, a.nheads, a.bias + h) ? a.bias[h] : 0.f);
-    if (a.softplus) dt = softplus_f(dt);
-    const float Ah = in_bounds(a.err, a.A, a.nheads, a.A + h) ? a.A[h] : -1.f;
-    const float decay = ex2_approx(dt * Ah * kLog2e);
-    const float2 ea = make_float2(decay, decay);
-    const float2 w = make_float2(dt * xv, dt * xv);
-    const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, B01));
-    const float2 h23 = __ffma2_rn(ea, make_float2(s4.z, s4.w), __fmul2_rn(w, B23));
-    const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
-    float yp = acc.x + acc.y;
+    float xv[kR], dt[kR], Ah[kR], Dh[kR];
 #pragma unroll
-    for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
-    if (d < dim) {
-        if (sok) *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
-        if (q == 0) {
-            const float yy = a.D && in_bounds(a.err, a.D, a.nheads, a.D + h) ? fmaf(a.D[h], xv, yp) : yp;
-            T* yg = static_cast<T*>(a.y);
-            if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
+    for (int r = 0; r < kR; ++r) {
+        const int h = dcs[r] / a.headdim;
+        const size_t row = static_cast<size_t>(b) * dim + dcs[r];
+        const size_t hrow = static_cast<size_t>(b) * a.nheads + h;
+        xv[r] = in_bounds(a.err, xg, nrows, xg + row) ? Io<T>::to_f(xg[row]) : 0.f;
+        dt[r] = (in_bounds(a.err, dg, static_cast<size_t>(a.batch) * a.nheads, dg + hrow) ? Io<T>::to_f(dg[hrow])
+                                                                                           : 0.f) +
+                (a.bias && in_bounds(a.err, a.bias, a.nheads, a.bias + h) ? a.bias[h] : 0.f);
+        Ah[r] = in_bounds(a.err, a.A, a.nheads, a.A + h) ? a.A[h] : -1.f;
+        Dh[r] = a.D && q == 0 && in_bounds(a.err, a.D, a.nheads, a.D + h) ? a.D[h] : 0.f;
+    }
+    cp_async_wait_all();  // this thread's own copies: no other thread reads them
+
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        const float4 s4 = stage[r][tid];
+        float dtr = dt[r];
+        if (a.softplus) dtr = softplus_f(dtr);
+        const float decay = ex2_approx(dtr * Ah[r] * kLog2e);
+        const float2 ea = make_float2(decay, decay);
+        const float2 w = make_float2(dtr * xv[r], dtr * xv[r]);
+        const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, B01));
+        const float2 h23 = __ffma2_rn(ea, make_float2(s4.z, s4.w), __fmul2_rn(w, B23));
+        const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
+        float yp = acc.x + acc.y;
+#pragma unroll
+        for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+        const int d = blockIdx.x * G::kRows + r * G::kPass + tid / kQ;
+        if (d < dim) {
+            const size_t row = static_cast<size_t>(b) * dim + d;
+            float* sp = a.state + row * NS + 4 * q;
+            if (in_bounds(a.err, a.state, nrows * NS, sp, 4))
+                *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
+            if (q == 0) {
+                const float yy = a.D ? fmaf(Dh[r], xv[r], yp) : yp;
+                T* yg = static_cast<T*>(a.y);
+                if (in_bounds(a.err, yg, nrows, yg + row)) yg[row] = Io<T>::from_f(yy);
+            }
         }
     }
 }
