@@ -11,7 +11,7 @@ namespace mhost {
 
 template <typename T, int NS>
 int launch_bwd_n(const mscan::ScanBwdArgs& a, int flags, cudaStream_t stream) {
-    const dim3 grid((a.dim + mscan::FwdGeo<NS>::kCh - 1) / mscan::FwdGeo<NS>::kCh, a.batch);
+    const dim3 grid((a.dim + mscan::ScanBwdGeo<NS>::kCh - 1) / mscan::ScanBwdGeo<NS>::kCh, a.batch);
     auto go = [&](auto sp, auto hz, auto zo) {
         mscan::scan_bwd_kernel<T, NS, decltype(sp)::value, decltype(hz)::value, decltype(zo)::value>
             <<<grid, 32, 0, stream>>>(a);

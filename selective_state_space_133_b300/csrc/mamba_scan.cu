@@ -138,7 +138,10 @@ SplitPlan plan_split(long long batch, long long dim, long long L, int dstate, si
     SplitPlan p;
     const int sms = device_sms();
     if (batch <= 0 || dim <= 0 || L <= 0 || sms <= 0) return p;
-    const long long kch = dstate == 8 ? 16 : 32 / (dstate / 8);  // channels per warp
+    const long long kch = dstate == 8    ? mscan::FwdGeo<8>::kCh    // channels per warp
+                          : dstate == 16 ? mscan::FwdGeo<16>::kCh
+                          : dstate == 32 ? mscan::FwdGeo<32>::kCh
+                                         : mscan::FwdGeo<64>::kCh;
     const long long warps = batch * ((dim + kch - 1) / kch);
     const long long schedulers = 4ll * sms;
     if (warps >= schedulers) return p;

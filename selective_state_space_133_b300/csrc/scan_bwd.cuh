@@ -19,7 +19,8 @@
 // dt^2 (1/2 + x/3 + x^2/8), x = dt A, where |x| < 1/64 (next term <= 1e-7
 // relative).
 //
-// Layout as in the forward (FwdGeo<N>): one warp per CTA; recurrence lane
+// Layout as in the forward with 8 states a lane (4 at N = 8; ScanBwdGeo):
+// one warp per CTA; recurrence lane
 // (rh, rc) = (lane / kCh, lane % kCh) owns states kS*rh .. kS*rh + kS - 1 of
 // channel rc; pre-pass/epilogue lanes (ec, ej) = (lane / kG, lane % kG) own
 // steps kSP*ej .. kSP*ej + kSP - 1 of channel ec.
@@ -41,6 +42,11 @@
 namespace mscan {
 
 constexpr int kBwdTL = 16;   // steps per chunk (the checkpoint interval)
+
+// The backward's lane geometry: the forward's with 8 states per lane (4 at
+// N = 8); wider lanes would take it past the register file.
+template <int NS>
+using ScanBwdGeo = FwdGeo<NS, NS == 8 ? 4 : 8>;
 
 struct ScanBwdArgs {
     const void* u;
@@ -66,13 +72,13 @@ struct ScanBwdArgs {
     int batch, dim, seqlen, Lp;
 };
 
-template <int NS>
+template <int NS, bool ZOH>
 struct ScanBwdSmem {
-    using G = FwdGeo<NS>;
+    using G = ScanBwdGeo<NS>;
     alignas(16) float2 W[G::kCh][kBwdTL + 1];        // {dt, dt*u} ({dt, u} with ZOH); odd row pitch
     alignas(16) float SG[G::kCh][kBwdTL + 1];        // d(dt)/d(delta + bias)
     alignas(16) float DP[G::kCh][kBwdTL + 1];        // dp = dy * silu(z)
-    alignas(16) float U[G::kCh][kBwdTL + 1];         // u
+    alignas(16) float U[ZOH ? 1 : G::kCh][kBwdTL + 1];  // u (with ZOH, W's second value holds it)
     alignas(16) float4 traj[kBwdTL][G::kS / 4][32];  // recomputed states: [step][4-state group][lane]
     alignas(16) float P[G::kG][kBwdTL / 4][G::kCh * 4 + 8];  // partial C.h: [state group][4-step group][channel][4]
     alignas(16) float2 Q[G::kCh][kBwdTL + 1];        // per (channel, step), all state groups summed:
@@ -105,6 +111,19 @@ __device__ __forceinline__ void ldg_n(const __nv_bfloat16* p, float (&v)[n], boo
     }
 }
 
+// A float2 in shared memory read and written with volatile instructions,
+// which the compiler may not hoist out of a loop (so that it does not keep
+// the value in registers across the loop instead) and keeps in order among
+// themselves.
+__device__ __forceinline__ float2 lds2_pinned(const float2* p) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(smem_u32(p)));
+    return v;
+}
+__device__ __forceinline__ void sts2_pinned(float2* p, float2 v) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(smem_u32(p)), "f"(v.x), "f"(v.y));
+}
+
 // Adds four consecutive floats (16-byte aligned) to global memory atomically.
 __device__ __forceinline__ void red_add4(float* p, float4 v) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
@@ -127,14 +146,14 @@ __device__ __forceinline__ float2 zoh_dgain_da2(float2 x2, float2 e, float2 gain
 
 template <typename T, int NS, bool SOFTPLUS, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
-    using G = FwdGeo<NS>;
+    using G = ScanBwdGeo<NS>;
     constexpr int kS = G::kS, kG = G::kG, kCh = G::kCh, kSP = G::kSP;
     constexpr int H = kS / 2;                              // state pairs per recurrence lane
     constexpr int kPJ = kCh * 4 + 8;
     constexpr int kCols = 2 * NS;                          // dB and dC columns of a step
     constexpr int kCPL = kCols >= 32 ? kCols / 32 : 1;     // columns summed per lane
     constexpr float kLn2 = 0.6931471805599453f;
-    __shared__ ScanBwdSmem<NS> sm;
+    __shared__ ScanBwdSmem<NS, ZOH> sm;
     const int lane = threadIdx.x;
     const int b = blockIdx.y, d0 = blockIdx.x * kCh;
     const int L = a.seqlen, n = (L + kBwdTL - 1) / kBwdTL;
@@ -152,15 +171,26 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
     const size_t nx = nrows * L;                                  // u, delta, z, dy, du, ddelta, dz
     const size_t npk = static_cast<size_t>(a.batch) * a.Lp;       // packed B/C rows, dB/dC sum columns
 
-    float2 A2[H], IA[H];
+    // With ZOH, 1/a of this lane's states and their dA sums live in shared
+    // memory (each lane reads back only what it wrote): in registers they
+    // would take the kernel past the register file.
+    __shared__ float2 inv_a[ZOH ? H : 1][32];
+    __shared__ float2 dA_zoh[ZOH ? H : 1][32];
+    float2 A2[H];
 #pragma unroll
     for (int i = 0; i < H; ++i) {
         const float* ap = a.A + static_cast<size_t>(rd) * NS + kS * rh + 2 * i;
         const float2 av = in_bounds(a.err, a.A, static_cast<size_t>(a.dim) * NS, ap, 2)
             ? *reinterpret_cast<const float2*>(ap) : make_float2(-1.f, -1.f);
         A2[i] = make_float2(av.x * kLog2e, av.y * kLog2e);
-        if (ZOH) IA[i] = make_float2(1.f / av.x, 1.f / av.y);
+        if (ZOH) {
+            sts2_pinned(&inv_a[i][lane], make_float2(1.f / av.x, 1.f / av.y));
+            sts2_pinned(&dA_zoh[i][lane], make_float2(0.f, 0.f));
+        }
     }
+    auto IA = [&](int j) -> float2 { return lds2_pinned(&inv_a[ZOH ? j : 0][lane]); };
+    // u of (channel c, step t) of the chunk in shared memory
+    auto u_at = [&](int c, int t) -> float { return ZOH ? sm.W[c][t].y : sm.U[ZOH ? 0 : c][t]; };
     const float bias = a.bias && in_bounds(a.err, a.bias, a.dim, a.bias + ed) ? a.bias[ed] : 0.f;
     const float Dd = a.D && in_bounds(a.err, a.D, a.dim, a.D + ed) ? a.D[ed] : 0.f;
     float* const hck = a.hck + rrow * n * NS + kS * rh;
@@ -202,7 +232,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
     // the input term of one step on pair j: dt*u*B, or the ZOH gain times u*B (du holds u then)
     auto input_term = [&](float2 x2, float2 e, float2 dd, float2 du, float2 Bj, int j) {
         const float2 t = __fmul2_rn(du, Bj);
-        return ZOH ? __fmul2_rn(zoh_gain2(x2, e, dd, IA[j]), t) : t;
+        return ZOH ? __fmul2_rn(zoh_gain2(x2, e, dd, IA(j)), t) : t;
     };
     // pre-pass of chunk k: dt and its second operand (dt*u, or u with ZOH) per (channel, step)
     auto prepass = [&](int k, bool full) {
@@ -222,7 +252,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             sm.W[ec][kSP * ej + i] = make_float2(dt, ZOH ? uv[i] : dt * uv[i]);
             if (full) {
                 sm.SG[ec][kSP * ej + i] = sg;
-                sm.U[ec][kSP * ej + i] = uv[i];
+                if (!ZOH) sm.U[ec][kSP * ej + i] = uv[i];
             }
         }
     };
@@ -355,7 +385,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
             float dzv[kSP];
 #pragma unroll
             for (int i = 0; i < kSP; ++i) {
-                const float uu = sm.U[ec][kSP * ej + i];
+                const float uu = u_at(ec, kSP * ej + i);
                 const float p = fmaf(Dd, uu, pre[i]);
                 float dp = gy[i];
                 if (HAS_Z) {
@@ -415,19 +445,23 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                 const float2 gh = __ffma2_rn(dpp, Cv[j], g[j]);
                 dCv[j] = __fmul2_rn(dpp, hT[j]);
                 if (ZOH) {  // du holds u
-                    const float2 gain = zoh_gain2(x2, e, dd, IA[j]);
+                    const float2 gain = zoh_gain2(x2, e, dd, IA(j));
                     const float2 ghB = __fmul2_rn(gh, Bv[j]);
                     dBv[j] = __fmul2_rn(__fmul2_rn(gh, gain), du);
                     sa = __ffma2_rn(ghB, gain, sa);
                     sc = __ffma2_rn(ghB, e, sc);
-                    dAacc[j] = __ffma2_rn(__fmul2_rn(ghB, du), zoh_dgain_da2(x2, e, gain, dd, IA[j]), dAacc[j]);
+                    const float2 dee = __fmul2_rn(__fmul2_rn(gh, hP[j]), e);
+                    sb = __ffma2_rn(dee, A2[j], sb);
+                    float2* da = &dA_zoh[ZOH ? j : 0][lane];
+                    sts2_pinned(da, __ffma2_rn(__fmul2_rn(ghB, du), zoh_dgain_da2(x2, e, gain, dd, IA(j)),
+                                               __ffma2_rn(dee, dd, lds2_pinned(da))));
                 } else {    // du holds dt*u
                     dBv[j] = __fmul2_rn(gh, du);
                     sa = __ffma2_rn(gh, Bv[j], sa);
+                    const float2 dee = __fmul2_rn(__fmul2_rn(gh, hP[j]), e);
+                    sb = __ffma2_rn(dee, A2[j], sb);
+                    dAacc[j] = __ffma2_rn(dee, dd, dAacc[j]);
                 }
-                const float2 dee = __fmul2_rn(__fmul2_rn(gh, hP[j]), e);
-                sb = __ffma2_rn(dee, A2[j], sb);
-                dAacc[j] = __ffma2_rn(dee, dd, dAacc[j]);
                 g[j] = __fmul2_rn(gh, e);
             }
             {   // all state groups of the channel: lanes rc + kCh * m
@@ -439,7 +473,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                     if (ZOH) qc += __shfl_xor_sync(0xffffffffu, qc, o);
                 }
                 // with ZOH the term sum_n gh B u e (d gain / d dt = e) completes d(dt) here
-                if (rh == 0) sm.Q[rc][t] = make_float2(qa, ZOH ? fmaf(qc, sm.U[rc][t], qb * kLn2) : qb * kLn2);
+                if (rh == 0) sm.Q[rc][t] = make_float2(qa, ZOH ? fmaf(qc, u_at(rc, t), qb * kLn2) : qb * kLn2);
             }
             // channel sums of this step's dB and dC
 #pragma unroll
@@ -482,7 +516,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
                 const int t = kSP * ej + i;
                 const float2 q = sm.Q[ec][t];
                 const float dsum = ZOH ? q.x : q.x * sm.W[ec][t].x;      // sum_n gh B gain
-                const float sdt = ZOH ? q.y : fmaf(q.x, sm.U[ec][t], q.y);  // d(dt)
+                const float sdt = ZOH ? q.y : fmaf(q.x, u_at(ec, t), q.y);  // d(dt)
                 duv[i] = fmaf(sm.DP[ec][t], Dd, dsum);
                 dxv[i] = le + i < L ? sdt * sm.SG[ec][t] : 0.f;
                 dbacc += dxv[i];
@@ -507,8 +541,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const ScanBwdArgs a) {
         float* p = a.dA + static_cast<size_t>(rd) * NS + kS * rh;
 #pragma unroll
         for (int j = 0; j < H; ++j) {
-            atomicAdd(p + 2 * j, dAacc[j].x);
-            atomicAdd(p + 2 * j + 1, dAacc[j].y);
+            const float2 v = ZOH ? lds2_pinned(&dA_zoh[ZOH ? j : 0][lane]) : dAacc[j];
+            atomicAdd(p + 2 * j, v.x);
+            atomicAdd(p + 2 * j + 1, v.y);
         }
     }
 #pragma unroll

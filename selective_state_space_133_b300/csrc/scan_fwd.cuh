@@ -22,12 +22,17 @@
 //    sequence for its states sequentially: no cross-thread scan and no carry
 //    fix-up pass, which would add work per element.
 //  * A CTA is one warp with its own copy ring, so no warp ever waits for
-//    another. In the recurrence a lane owns kS = 8 consecutive states of one
-//    channel (4 at N = 8, so that a warp still holds 16 channels): lane
-//    (h, c) = (lane / kCh, lane % kCh) owns states kS*h .. kS*h + kS - 1 of
-//    channel c. The kG = N / kS lanes of a channel read B/C at kG addresses
-//    per step (16-byte broadcast loads), and share the per-(channel, step)
-//    values dt and dt*u. At N = 16 that is 16 channels per CTA.
+//    another. In the recurrence a lane owns kS consecutive states of one
+//    channel: lane (h, c) = (lane / kCh, lane % kCh) owns states
+//    kS*h .. kS*h + kS - 1 of channel c. The kG = N / kS lanes of a channel
+//    read B/C at kG addresses per step (16-byte broadcast loads), and share
+//    the per-(channel, step) values dt and dt*u. kS = 8 at N = 16 (16
+//    channels per CTA), 4 at N = 8 (16 channels), 16 at N = 32 and 64 (16 and
+//    8 channels): the chunk's B/C transposition is shared by the CTA's
+//    channels, and at N >= 32 the wider lanes halve its cost per element
+//    (measured on B300: N = 64 1.64 -> 1.16 ms, N = 32 0.76 -> 0.61 ms on
+//    8 x 2048 x 4096), while at N <= 16 they would leave fewer warps than
+//    schedulers.
 //  * The sequence is cut into 16-step chunks. Lane 0 issues 3-D TMA loads of
 //    a chunk's u/delta/z tiles (kCh channels x 16 steps) and of its B and C
 //    tiles in their own (batch, N, L) layout (N rows x 16 steps each) into a
@@ -67,11 +72,12 @@ constexpr int kTL = 16;          // steps per chunk
 constexpr int kScanThreads = 32;
 constexpr int kConvW = 4;        // width of the causal convolution fused in front of the scan
 
-// Geometry of the forward kernel for state size NS.
-template <int NS>
+// Geometry of the forward kernel for state size NS with KS states per
+// recurrence lane (the backward keeps 8, see ScanBwdGeo).
+template <int NS, int KS = (NS == 8 ? 4 : NS >= 32 ? 16 : 8)>
 struct FwdGeo {
     static_assert(NS == 8 || NS == 16 || NS == 32 || NS == 64, "state sizes 8, 16, 32 and 64 are compiled");
-    static constexpr int kS = NS == 8 ? 4 : 8;    // states per recurrence lane
+    static constexpr int kS = KS;                 // states per recurrence lane
     static constexpr int kG = NS / kS;            // lanes per channel
     static constexpr int kCh = 32 / kG;           // channels per CTA (one warp)
     static constexpr int kSP = kTL / kG;          // steps per lane in the pre-pass and epilogue

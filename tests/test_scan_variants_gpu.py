@@ -49,7 +49,7 @@ def compare(x, zoh, what, h0=None):
 
 SHAPES = [
     # batch, dim, L, dtype
-    (1, 16, 32, torch.float32),    # whole tiles at every N (4, 8, 16 or 32 channels a CTA)
+    (1, 16, 32, torch.float32),    # whole tiles at every N (16 channels a CTA, 8 at N = 64)
     (2, 20, 40, torch.bfloat16),   # ragged channels, ragged last chunk
     (1, 33, 100, torch.float32),   # ragged everything
     (3, 17, 7, torch.bfloat16),    # L % 8 != 0: rows copied to a 16-byte pitch
