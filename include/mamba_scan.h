@@ -322,7 +322,7 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
  *                   (0 bytes unless seqlen is not a multiple of 8: then row
  *                   copies of x, B and C at a 16-byte pitch)
  * Supported: io_dtype MAMBA_BF16 (MAMBA_ERR_DTYPE otherwise), headdim 64 and
- * dstate 64 or 128 (MAMBA_ERR_SHAPE otherwise), flags MAMBA_FLAG_SOFTPLUS only
+ * dstate 64, 128 or 256 (MAMBA_ERR_SHAPE otherwise), flags MAMBA_FLAG_SOFTPLUS only
  * (MAMBA_ERR_FLAGS otherwise). Alignment: x, y, B, C and the states 16 bytes,
  * delta 2, A, D, delta_bias 4. State and accumulation are fp32; y is rounded to
  * bf16 once. Returns MAMBA_OK or a negative mamba_status.
@@ -348,7 +348,7 @@ int mamba_ssd_fwd(const void* x, const void* delta, const float* A,
  *   x, y    : (batch, nheads * headdim) io_dtype;  delta : (batch, nheads) io_dtype
  *   B, C    : (batch, dstate) io_dtype, 16-byte aligned
  *   A       : (nheads) fp32;  D, delta_bias : (nheads) fp32 or NULL
- * Supported: io_dtype MAMBA_F32 or MAMBA_BF16, headdim 64, dstate 64 or 128,
+ * Supported: io_dtype MAMBA_F32 or MAMBA_BF16, headdim 64, dstate 64, 128 or 256,
  * flags MAMBA_FLAG_SOFTPLUS only. Returns MAMBA_OK or a negative mamba_status.
  */
 int mamba_ssd_update(float* state, const void* x, const void* delta, const float* A,

@@ -523,7 +523,7 @@ int mamba_state_update(float* state, const void* u, const void* delta, const flo
 
 // --- SSD (Mamba-2 chunked form) ---------------------------------------------
 
-static bool ssd_dstate(int dstate) { return dstate == 64 || dstate == 128; }
+static bool ssd_dstate(int dstate) { return dstate == 64 || dstate == 128 || dstate == 256; }
 
 // Workspace of one SSD call: row-pitched copies of x, B and C when a row of
 // seqlen bf16 values is not a whole number of 16-byte units (a TMA stride rule).
@@ -603,8 +603,9 @@ int mamba_ssd_fwd(const void* x, const void* delta, const float* A, const void* 
         if (cudaGetLastError() != cudaSuccess) return MAMBA_ERR_CUDA;
         x = ws + w.x; B = ws + w.b; C = ws + w.c;
     }
-    return dstate == 64 ? mhost::launch_ssd_n<64>(a, x, B, C, w.pitch, s)
-                        : mhost::launch_ssd_n<128>(a, x, B, C, w.pitch, s);
+    return dstate == 64    ? mhost::launch_ssd_n<64>(a, x, B, C, w.pitch, s)
+           : dstate == 128 ? mhost::launch_ssd_n<128>(a, x, B, C, w.pitch, s)
+                           : mhost::launch_ssd_n<256>(a, x, B, C, w.pitch, s);
 }
 
 int mamba_ssd_update(float* state, const void* x, const void* delta, const float* A, const void* B, const void* C,
@@ -631,9 +632,13 @@ int mamba_ssd_update(float* state, const void* x, const void* delta, const float
     if (!(a.err = device_error_word())) return MAMBA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (io_dtype == MAMBA_BF16) {
-        if (dstate == 64) launch_ssd_update_n<__nv_bfloat16, 64>(a, s); else launch_ssd_update_n<__nv_bfloat16, 128>(a, s);
+        if (dstate == 64) launch_ssd_update_n<__nv_bfloat16, 64>(a, s);
+        else if (dstate == 128) launch_ssd_update_n<__nv_bfloat16, 128>(a, s);
+        else launch_ssd_update_n<__nv_bfloat16, 256>(a, s);
     } else {
-        if (dstate == 64) launch_ssd_update_n<float, 64>(a, s); else launch_ssd_update_n<float, 128>(a, s);
+        if (dstate == 64) launch_ssd_update_n<float, 64>(a, s);
+        else if (dstate == 128) launch_ssd_update_n<float, 128>(a, s);
+        else launch_ssd_update_n<float, 256>(a, s);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }

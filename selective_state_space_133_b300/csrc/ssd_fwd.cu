@@ -1,4 +1,4 @@
-// SSD (Mamba-2 chunked form) kernels, state sizes 64 and 128: tensor maps and launch.
+// SSD (Mamba-2 chunked form) kernels, state sizes 64, 128 and 256: tensor maps and launch.
 #include <string.h>
 
 #include "../../include/mamba_scan.h"
@@ -22,7 +22,8 @@ int launch_ssd_n(const mscan::SsdArgs& a, const void* x, const void* B, const vo
     }
     // the tiles need 1024-byte alignment inside the dynamic shared memory
     const size_t smem = sizeof(mscan::SsdSmem<NS>) + 1024;
-    // two CTAs (110 KB each at N = 128) share an SM: ask for the whole carveout
+    // two CTAs (110 KB each at N = 128) share an SM, one (177 KB) at N = 256:
+    // ask for the whole carveout
     if (cudaFuncSetAttribute(mscan::ssd_fwd_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
         cudaFuncSetAttribute(mscan::ssd_fwd_kernel<NS>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -35,5 +36,6 @@ int launch_ssd_n(const mscan::SsdArgs& a, const void* x, const void* B, const vo
 
 template int launch_ssd_n<64>(const mscan::SsdArgs&, const void*, const void*, const void*, int, cudaStream_t);
 template int launch_ssd_n<128>(const mscan::SsdArgs&, const void*, const void*, const void*, int, cudaStream_t);
+template int launch_ssd_n<256>(const mscan::SsdArgs&, const void*, const void*, const void*, int, cudaStream_t);
 
 }  // namespace mhost

@@ -32,7 +32,9 @@
 // channels), updated from U as S = e^{c_Q} S + U and written back, split, as
 // the next chunk's operand. Two CTAs share an SM (104 KB of shared memory and
 // 256 TMEM columns each), so one's elementwise work overlaps the other's
-// contractions and loads. Per chunk: one thread issues G and Y1 as soon as C and
+// contractions and loads. At N = 256 (the Mamba-2 section's largest state) U
+// is two M = 128 products and a CTA takes the SM (177 KB, 512 TMEM columns),
+// each thread holding one state column for all 64 channels. Per chunk: one thread issues G and Y1 as soon as C and
 // B are in; every thread forms W; barrier; it issues U while every
 // thread forms Gm from G (tcgen05.ld, mask, decay weights, split), with D_h
 // added on its diagonal so that Y2 = Gm X^T carries the skip term D x;
@@ -172,10 +174,17 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // ------------------------------------------------------------- kernel ------
 
 template <int NS>
-__global__ void __launch_bounds__(kSsdThreads, 2)
+__global__ void __launch_bounds__(kSsdThreads, NS == 256 ? 1 : 2)
 ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_c) {
-    static_assert(NS == 64 || NS == 128, "state sizes 64 and 128 are compiled");
+    static_assert(NS == 64 || NS == 128 || NS == 256, "state sizes 64, 128 and 256 are compiled");
+    // At N = 256 U is two M = 128 products (rows n < 128 and n >= 128) into
+    // 64 more TMEM columns, so a CTA takes all 512 (and, at 177 KB of shared
+    // memory, the SM); a thread then holds one state column for all 64
+    // channels.
+    constexpr int kTmemCols = NS == 256 ? 512 : kSsdTmemCols;
+    constexpr int kSC = NS == 256 ? 64 : 32;      // state channels a thread holds
+    constexpr int kUM = NS == 256 ? 128 : NS;     // M of each U product
     extern __shared__ unsigned char ssd_smem_raw[];
     // 1024-byte aligned view of the dynamic shared memory, derived from the
     // shared array itself so that every access stays a shared-memory access
@@ -204,7 +213,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
-                     "n"(kSsdTmemCols)
+                     "n"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -235,32 +244,34 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     }
     __syncwarp();
 
-    // The state: this thread holds column sn of it for channels p = 32 half + j.
-    // U's row n lies in TMEM lane n at N = 128 (M = 128) and in lane
-    // 32 (n / 16) + n % 16 at N = 64 (M = 64), where lanes 16..31 of a warp hold none.
-    const bool sact = NS == 128 || lane < 16;
-    const int sn = NS == 128 ? 32 * q + lane : 16 * q + (lane & 15);
+    // The state: this thread holds column sn of it for channels p = pc0 + j,
+    // j < kSC. U's row n lies in TMEM lane n at N = 128 (M = 128), in lane
+    // 32 (n / 16) + n % 16 at N = 64 (M = 64), where lanes 16..31 of a warp
+    // hold none, and at N = 256 in lane n % 128 of the product of its half.
+    const bool sact = NS != 64 || lane < 16;
+    const int sn = NS == 256 ? 32 * q + lane + 128 * half : NS == 128 ? 32 * q + lane : 16 * q + (lane & 15);
+    const int pc0 = NS == 256 ? 0 : 32 * half;
     const bool have_state = a.h0 != nullptr;
-    float S[32];
+    float S[kSC];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float* hp = a.h0 + (head_row * kSsdP + 32 * half + j) * NS + sn;
+    for (int j = 0; j < kSC; ++j) {
+        const float* hp = a.h0 + (head_row * kSsdP + pc0 + j) * NS + sn;
         S[j] = (have_state && sact && in_bounds(a.err, a.h0, nstate, hp)) ? *hp : 0.f;
     }
     // the state's high and low parts as the Y1 product's operand: row n, this
-    // thread's 32 channels as four 16-byte units of each part
+    // thread's kSC channels as 16-byte units of each part
     auto store_state_parts = [&]() {
         if (!sact) return;
         unsigned char* hb = reinterpret_cast<unsigned char*>(&sm.Sh[sn][0]);
         unsigned char* lb = reinterpret_cast<unsigned char*>(&sm.Sl[sn][0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kSC / 8; ++c) {
             uint4 hi, lo;
             split2(S[8 * c], S[8 * c + 1], hi.x, lo.x);
             split2(S[8 * c + 2], S[8 * c + 3], hi.y, lo.y);
             split2(S[8 * c + 4], S[8 * c + 5], hi.z, lo.z);
             split2(S[8 * c + 6], S[8 * c + 7], hi.w, lo.w);
-            const int off = ((4 * half + c) ^ (sn & 7)) << 4;
+            const int off = ((pc0 / 8 + c) ^ (sn & 7)) << 4;
             *reinterpret_cast<uint4*>(hb + off) = hi;
             *reinterpret_cast<uint4*>(lb + off) = lo;
         }
@@ -317,7 +328,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     tc_fence_after();
 
     const uint32_t tmem = sm.tmem;
-    const uint32_t tG = tmem, tY1 = tmem + 64, tY2 = tmem + 128, tU = tmem + 192;
+    const uint32_t tG = tmem, tY1 = tmem + 64, tY2 = tmem + 128, tU = tmem + 192, tU2 = tmem + 256;
     const uint32_t xs = smem_u32(&sm.X[0][0]), bs = smem_u32(&sm.Bt[0][0]), cs = smem_u32(&sm.Ct[0][0]);
     const uint32_t ghs = smem_u32(&sm.Gh[0][0]), gls = smem_u32(&sm.Gl[0][0]);
     const uint32_t whs = smem_u32(&sm.Wh[0][0]), wls = smem_u32(&sm.Wl[0][0]);
@@ -325,7 +336,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     constexpr uint32_t kIdG = umma_idesc(64, 64, true, true);     // C^T (MN-major) x B (MN-major)
     constexpr uint32_t kIdY1 = umma_idesc(64, 64, true, true);    // C^T (MN-major) x S^T (MN-major)
     constexpr uint32_t kIdY2 = umma_idesc(64, 64, false, false);  // Gm x X^T
-    constexpr uint32_t kIdU = umma_idesc(NS, 64, false, false);   // B x W^T
+    constexpr uint32_t kIdU = umma_idesc(kUM, 64, false, false);  // B x W^T (each half of B at N = 256)
 
     __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(a.y) + (static_cast<size_t>(b) * dim + ch0) * L;
     // Output staging [p][kSsdYPitch] over the Gm buffers: written once the
@@ -420,6 +431,10 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             for (int kk = 0; kk < kSsdQ / 16; ++kk) {
                 umma(tU, desc_k(bs + kk * 32), desc_k(whs + kk * 32), kIdU, kk > 0);
                 umma(tU, desc_k(bs + kk * 32), desc_k(wls + kk * 32), kIdU, true);
+                if (NS == 256) {  // rows n = 128..255 of B: 128 rows of 128 bytes further
+                    umma(tU2, desc_k(bs + 16384 + kk * 32), desc_k(whs + kk * 32), kIdU, kk > 0);
+                    umma(tU2, desc_k(bs + 16384 + kk * 32), desc_k(wls + kk * 32), kIdU, true);
+                }
             }
             umma_commit(&sm.done[2]);
             if (k + 1 < n && !timed_out && mbar_try_wait(&sm.done[1], par)) issue(2, k + 1);  // C is free already
@@ -499,13 +514,18 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         if (!mbar_wait_bounded(&sm.done[2], par)) timed_out = true;  // U
         tc_fence_after();
         {
-            uint32_t u[2][16];
-            tmem_ld_32x32b_x16(tU + lane_base + 32 * half, u[0]);
-            tmem_ld_32x32b_x16(tU + lane_base + 32 * half + 16, u[1]);
-            tmem_wait_ld();
             const float ed = ex2_approx(c2[kSsdQ - 1]);
+            // this thread's row of U (its TMEM lane), kSC columns, 32 at a time
+            const uint32_t urow = (NS == 256 ? (half ? tU2 : tU) : tU + 32 * half) + lane_base;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = fmaf(ed, S[j], __uint_as_float(u[j >> 4][j & 15]));
+            for (int j0 = 0; j0 < kSC; j0 += 32) {
+                uint32_t u[2][16];
+                tmem_ld_32x32b_x16(urow + j0, u[0]);
+                tmem_ld_32x32b_x16(urow + j0 + 16, u[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[j0 + j] = fmaf(ed, S[j0 + j], __uint_as_float(u[j >> 4][j & 15]));
+            }
         }
         if (!mbar_wait_bounded(&sm.done[1], par)) timed_out = true;  // Y1, the parts' last reader, is done
         store_state_parts();
@@ -560,7 +580,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
             __syncthreads();
             tc_fence_after();
             if (warp == 0)
-                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kSsdTmemCols)
+                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
                              : "memory");
             return;
         }
@@ -570,8 +590,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
 
     if (a.final_state && sact) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            float* fp = a.final_state + (head_row * kSsdP + 32 * half + j) * NS + sn;
+        for (int j = 0; j < kSC; ++j) {
+            float* fp = a.final_state + (head_row * kSsdP + pc0 + j) * NS + sn;
             if (in_bounds(a.err, a.final_state, nstate, fp)) *fp = S[j];
         }
     }
@@ -579,7 +599,7 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
     __syncthreads();
     tc_fence_after();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kSsdTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
 }  // namespace mscan

@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(kUpdateThreads) state_update_kernel(const Upda
 //     y[b,h*P+p] = S[p,:] . C[b,:] + D[h] x[b,h*P+p]
 // Bound by HBM like the scan's state update: each state row (4N bytes) is
 // read and written once. N/4 lanes share a row, 4 states each, and add their
-// partial C.S with xor-shuffles. A thread takes kR rows of the same batch row,
+// partial C.S with xor-shuffles (8 states a lane at N = 256, so that a row
+// fits one warp). A thread takes kR rows of the same batch row,
 // which share B and C (loaded once), and copies their states into shared
 // memory with asynchronous copies before any arithmetic.
 
@@ -193,7 +194,9 @@ struct SsdUpdateArgs {
 
 template <int NS>
 struct SsdUpdateGeo {
-    static constexpr int kQ = NS / 4;                    // lanes per row (a power of two up to 32)
+    static_assert(NS == 64 || NS == 128 || NS == 256, "state sizes 64, 128 and 256 are compiled");
+    static constexpr int kV = NS == 256 ? 8 : 4;         // states per lane (a row fits one warp)
+    static constexpr int kQ = NS / kV;                   // lanes per row (a power of two up to 32)
     static constexpr int kPass = kUpdateThreads / kQ;    // rows the block's threads cover at once
     static constexpr int kR = 4;                         // rows per thread
     static constexpr int kRows = kPass * kR;             // rows per block
@@ -202,8 +205,8 @@ struct SsdUpdateGeo {
 template <typename T, int NS>
 __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpdateArgs a) {
     using G = SsdUpdateGeo<NS>;
-    constexpr int kQ = G::kQ, kR = G::kR;
-    __shared__ float4 stage[kR][kUpdateThreads];  // the state of each of this thread's rows
+    constexpr int kQ = G::kQ, kR = G::kR, kV4 = G::kV / 4;
+    __shared__ float4 stage[kR][kV4][kUpdateThreads];  // the state of each of this thread's rows
     const int tid = threadIdx.x;
     const int b = blockIdx.y;
     const int q = tid % kQ;
@@ -217,15 +220,24 @@ __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpd
     for (int r = 0; r < kR; ++r) {
         const int d = blockIdx.x * G::kRows + r * G::kPass + tid / kQ;
         dcs[r] = d < dim ? d : dim - 1;  // padding lanes recompute the last row, store nothing
-        const float* sp = a.state + (static_cast<size_t>(b) * dim + dcs[r]) * NS + 4 * q;
-        if (in_bounds(a.err, a.state, nrows * NS, sp, 4)) cp_async16(&stage[r][tid], sp);
-        else stage[r][tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* sp = a.state + (static_cast<size_t>(b) * dim + dcs[r]) * NS + G::kV * q;
+#pragma unroll
+        for (int v = 0; v < kV4; ++v) {
+            if (in_bounds(a.err, a.state, nrows * NS, sp + 4 * v, 4)) cp_async16(&stage[r][v][tid], sp + 4 * v);
+            else stage[r][v][tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
-    float2 B01 = {}, B23 = {}, C01 = {}, C23 = {};
-    const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + 4 * q;
-    const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + 4 * q;
-    if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4)) ldg4(Bp, B01, B23);
-    if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4)) ldg4(Cp, C01, C23);
+    float2 Bv[2 * kV4], Cv[2 * kV4];  // this lane's kV values of B and C as pairs
+#pragma unroll
+    for (int v = 0; v < kV4; ++v) {
+        Bv[2 * v] = Bv[2 * v + 1] = Cv[2 * v] = Cv[2 * v + 1] = make_float2(0.f, 0.f);
+        const T* Bp = static_cast<const T*>(a.B) + static_cast<size_t>(b) * NS + G::kV * q + 4 * v;
+        const T* Cp = static_cast<const T*>(a.C) + static_cast<size_t>(b) * NS + G::kV * q + 4 * v;
+        if (in_bounds(a.err, static_cast<const T*>(a.B), static_cast<size_t>(a.batch) * NS, Bp, 4))
+            ldg4(Bp, Bv[2 * v], Bv[2 * v + 1]);
+        if (in_bounds(a.err, static_cast<const T*>(a.C), static_cast<size_t>(a.batch) * NS, Cp, 4))
+            ldg4(Cp, Cv[2 * v], Cv[2 * v + 1]);
+    }
     float xv[kR], dt[kR], Ah[kR], Dh[kR];
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
@@ -243,24 +255,32 @@ __global__ void __launch_bounds__(kUpdateThreads) ssd_update_kernel(const SsdUpd
 
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
-        const float4 s4 = stage[r][tid];
         float dtr = dt[r];
         if (a.softplus) dtr = softplus_f(dtr);
         const float decay = ex2_approx(dtr * Ah[r] * kLog2e);
         const float2 ea = make_float2(decay, decay);
         const float2 w = make_float2(dtr * xv[r], dtr * xv[r]);
-        const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, B01));
-        const float2 h23 = __ffma2_rn(ea, make_float2(s4.z, s4.w), __fmul2_rn(w, B23));
-        const float2 acc = __ffma2_rn(C23, h23, __fmul2_rn(C01, h01));
+        float4 hn[kV4];
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int v = 0; v < kV4; ++v) {
+            const float4 s4 = stage[r][v][tid];
+            const float2 h01 = __ffma2_rn(ea, make_float2(s4.x, s4.y), __fmul2_rn(w, Bv[2 * v]));
+            const float2 h23 = __ffma2_rn(ea, make_float2(s4.z, s4.w), __fmul2_rn(w, Bv[2 * v + 1]));
+            acc = __ffma2_rn(Cv[2 * v + 1], h23, __ffma2_rn(Cv[2 * v], h01, acc));
+            hn[v] = make_float4(h01.x, h01.y, h23.x, h23.y);
+        }
         float yp = acc.x + acc.y;
 #pragma unroll
         for (int o = 1; o < kQ; o <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
         const int d = blockIdx.x * G::kRows + r * G::kPass + tid / kQ;
         if (d < dim) {
             const size_t row = static_cast<size_t>(b) * dim + d;
-            float* sp = a.state + row * NS + 4 * q;
-            if (in_bounds(a.err, a.state, nrows * NS, sp, 4))
-                *reinterpret_cast<float4*>(sp) = make_float4(h01.x, h01.y, h23.x, h23.y);
+            float* sp = a.state + row * NS + G::kV * q;
+#pragma unroll
+            for (int v = 0; v < kV4; ++v)
+                if (in_bounds(a.err, a.state, nrows * NS, sp + 4 * v, 4))
+                    *reinterpret_cast<float4*>(sp + 4 * v) = hn[v];
             if (q == 0) {
                 const float yy = a.D ? fmaf(Dh[r], xv[r], yp) : yp;
                 T* yg = static_cast<T*>(a.y);

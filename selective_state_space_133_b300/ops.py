@@ -259,7 +259,7 @@ def mamba_ssd_fwd(x, delta, A, B, C, D=None, delta_bias=None, softplus=False, in
     """SSD (Mamba-2) layer (see include/mamba_scan.h, mamba_ssd_fwd).
 
     x: (batch, nheads * 64, L) bf16; delta: (batch, nheads, L) bf16; A, D,
-    delta_bias: (nheads,) fp32; B, C: (batch, N, L) bf16, N in {64, 128};
+    delta_bias: (nheads,) fp32; B, C: (batch, N, L) bf16, N in {64, 128, 256};
     initial_state: (batch, nheads, 64, N) fp32 or None; final_state: a tensor of
     that shape, or True to allocate one. Returns y, or (y, final_state).
     """
@@ -303,7 +303,7 @@ def mamba_ssd_fwd(x, delta, A, B, C, D=None, delta_bias=None, softplus=False, in
 def mamba_ssd_update(state, x, delta, A, B, C, D=None, delta_bias=None, softplus=False, y=None, stream=None):
     """One decode step of the SSD form in place on ``state`` (see include/mamba_scan.h, mamba_ssd_update).
 
-    state: (batch, nheads, 64, N) fp32, N in {64, 128}; x: (batch, nheads * 64);
+    state: (batch, nheads, 64, N) fp32, N in {64, 128, 256}; x: (batch, nheads * 64);
     delta: (batch, nheads); B, C: (batch, N), all fp32 or all bf16; A, D,
     delta_bias: (nheads,) fp32. Returns y (batch, nheads * 64).
     """

@@ -145,11 +145,12 @@ class SsdWorkload:
 
 
 # The paper walkthrough's Mamba-2 usage example (§5.2: d_model 2048, expand 2,
-# headdim 64, d_state 128, one sequence of 1024 tokens), and the same layer on
-# 8 x 4096 tokens.
+# headdim 64, d_state 128, one sequence of 1024 tokens), the same layer on
+# 8 x 4096 tokens, and that with d_state 256 (§4: states of 64 to 256).
 SSD_WORKLOADS: Dict[str, SsdWorkload] = {w.name: w for w in [
     SsdWorkload("ssd_b1_h64_l1024_n128_bf16", 1, 64, 1024, 128, 9),
     SsdWorkload("ssd_b8_h64_l4096_n128_bf16", 8, 64, 4096, 128, 10),
+    SsdWorkload("ssd_b8_h64_l4096_n256_bf16", 8, 64, 4096, 256, 11),   # the largest state the section names
 ]}
 
 

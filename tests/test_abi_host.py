@@ -245,7 +245,7 @@ def ssd(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dtype=0), -3), (dict(dtype=4), -3), (dict(flags=2), -8), (dict(flags=4), -8),
-    (dict(headdim=32), -2), (dict(headdim=128), -2), (dict(dstate=16), -2), (dict(dstate=256), -2),
+    (dict(headdim=32), -2), (dict(headdim=128), -2), (dict(dstate=16), -2), (dict(dstate=512), -2),
     (dict(batch=-1), -2), (dict(nheads=-1), -2), (dict(seqlen=-3), -2), (dict(batch=70000), -2),
     (dict(A=None), -1), (dict(x=None), -1), (dict(delta=None), -1), (dict(B=None), -1), (dict(y=None), -1),
     (dict(x=P + 8), -4), (dict(y=P + 4), -4), (dict(C=P + 2), -4), (dict(delta=P + 1), -4), (dict(fs=P + 8), -4),

@@ -178,7 +178,8 @@ def test_state_update(batch, dim, dtype, N, zoh):
     finish(st, state, y, written=(y,))
 
 
-@pytest.mark.parametrize("batch,nheads,L,N", [(2, 3, 100, 128), (2, 2, 7, 128), (1, 4, 257, 128), (3, 2, 130, 64)],
+@pytest.mark.parametrize("batch,nheads,L,N", [(2, 3, 100, 128), (2, 2, 7, 128), (1, 4, 257, 128), (3, 2, 130, 64),
+                                              (1, 2, 201, 256)],
                          ids=lambda v: str(v))
 def test_ssd(batch, nheads, L, N):
     d = dev(syn.ssd_inputs(batch, nheads, L, N, seed=L))
@@ -193,7 +194,7 @@ def test_ssd(batch, nheads, L, N):
     finish(st, y, h, ws, written=(y, h))
 
 
-@pytest.mark.parametrize("N,dtype", [(64, torch.bfloat16), (128, torch.float32)])
+@pytest.mark.parametrize("N,dtype", [(64, torch.bfloat16), (128, torch.float32), (256, torch.bfloat16)])
 def test_ssd_update(N, dtype):
     batch, nheads = 3, 5
     g = torch.Generator().manual_seed(N)

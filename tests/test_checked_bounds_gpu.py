@@ -128,7 +128,7 @@ def test_ssd(batch, nheads, L, N):
     ssd_t.test_shapes(batch, nheads, L, N)
 
 
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 def test_ssd_state_and_update(N):
     ssd_t.test_initial_state_and_pieces(N)
     ssd_t.test_ssd_update_parity(N, torch.bfloat16)

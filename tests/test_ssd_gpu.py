@@ -51,6 +51,9 @@ SHAPES = [
     (2, 2, 7, 128),      # L < 8
     (1, 4, 257, 128),    # five chunks, one step in the last
     (3, 2, 512, 64),     # eight chunks, both ring slots reused
+    (1, 2, 200, 256),    # N = 256: U as two M = 128 products, one CTA per SM
+    (2, 1, 7, 256),      # N = 256, L < 8
+    (1, 3, 321, 256),    # N = 256, six chunks, one step in the last
 ]
 
 
@@ -73,7 +76,7 @@ def test_no_bias():
     compare(x, "no bias")
 
 
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 def test_initial_state_and_pieces(N):
     x = syn.ssd_inputs(2, 2, 300, N, seed=11)
     g = torch.Generator().manual_seed(3)
@@ -91,7 +94,7 @@ def test_initial_state_and_pieces(N):
     assert max_rel_err(h2.reshape(-1, N), hr.reshape(-1, N)) <= TOL_BF16
 
 
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 def test_strong_decay(N):
     # dt near 1 and A down to -32: the decay sum of a chunk runs to thousands
     # (log2 units), so e^{c_l}, the state-update weights and every off-diagonal
@@ -176,7 +179,7 @@ def ssd_step_inputs(batch, nheads, N, dtype, seed):
                 delta_bias=syn.inv_softplus(torch.full((nheads,), 0.01, dtype=torch.float64)).float())
 
 
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_ssd_update_parity(N, dtype):
     batch, nheads = 3, 5   # 15 (row, head) pairs of 64 channels
@@ -192,7 +195,7 @@ def test_ssd_update_parity(N, dtype):
     assert max_rel_err(st.double().cpu().numpy().reshape(-1, N), hr.reshape(-1, N)) <= TOL["float32"]
 
 
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 def test_ssd_update_continues_forward(N):
     # a chunked forward over L0 steps, then one decode step per further token
     x = syn.ssd_inputs(2, 3, 80, N, seed=21)
