@@ -90,7 +90,9 @@ struct SsdSmem {
     alignas(1024) __nv_bfloat16 Sl[NS][kSsdP];     //                       low part
     alignas(16) float c2[2][kSsdQ];  // c_l * log2(e), chunk k in [k & 1]
     alignas(16) float dt[2][kSsdQ];
-    alignas(16) float wq[2][kSsdQ];  // e^{c_Q - c_s} dt_s
+    alignas(16) float wq[2][kSsdQ + 8];  // e^{c_Q - c_s} dt_s at wq_at(s): 4 floats of padding after
+                                         // each 32 steps keep the W phase's 16-byte reads of steps
+                                         // 8u.. (u = 0, 2, 4, 6 in one quarter-warp) in distinct banks
     alignas(8) uint64_t full[3];     // TMA: x, B, C
     alignas(8) uint64_t done[4];     // MMA completion: G, Y1, U, Y2 (each also covers the earlier ones)
     uint32_t tmem;                   // base address of this CTA's tensor memory
@@ -98,6 +100,9 @@ struct SsdSmem {
 static_assert(kSsdP * kSsdYPitch * 2 <= 2 * kSsdQ * kSsdQ * 2, "the y staging tile fits in the Gm buffers");
 
 // ------------------------------------------------------------ helpers ------
+
+// Index of step s in the padded decay-weight row (SsdSmem::wq).
+__device__ __forceinline__ int wq_at(int s) { return s + ((s >> 5) << 2); }
 
 // Byte offset of element (row, col) in a swizzled tile of 128-byte rows.
 __device__ __forceinline__ int swz(int row, int col) {
@@ -299,9 +304,9 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 d[i] = r[i] + bias;
                 if (a.softplus) d[i] = softplus_f(d[i]);
             }
-            sm.dt[k & 1][l] = d[i];
             v[i] = d[i] * Ah2;
         }
+        *reinterpret_cast<float2*>(&sm.dt[k & 1][2 * lane]) = make_float2(d[0], d[1]);
         const float pair = v[0] + v[1];
         float incl = pair;
 #pragma unroll
@@ -312,10 +317,9 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
         const float excl = incl - pair;
         const float cq = __shfl_sync(0xffffffffu, incl, 31);
         const float c0 = excl + v[0], c1 = excl + pair;
-        sm.c2[k & 1][2 * lane] = c0;
-        sm.c2[k & 1][2 * lane + 1] = c1;
-        sm.wq[k & 1][2 * lane] = ex2_approx(cq - c0) * d[0];
-        sm.wq[k & 1][2 * lane + 1] = ex2_approx(cq - c1) * d[1];
+        *reinterpret_cast<float2*>(&sm.c2[k & 1][2 * lane]) = make_float2(c0, c1);
+        *reinterpret_cast<float2*>(&sm.wq[k & 1][wq_at(2 * lane)]) =
+            make_float2(ex2_approx(cq - c0) * d[0], ex2_approx(cq - c1) * d[1]);
     };
     if (warp == kDecayWarp && n > 0) {
         float r[2];
@@ -408,8 +412,8 @@ ssd_fwd_kernel(const SsdArgs a, const __grid_constant__ CUtensorMap tm_x, const 
                 const int u = 2 * (tid & 3) + i;  // 16-byte unit: steps 8u .. 8u + 7
                 const int off = p * 128 + ((u ^ (p & 7)) << 4);
                 const uint4 xv = *reinterpret_cast<const uint4*>(xb + off);
-                const float4 w0 = *reinterpret_cast<const float4*>(&wq[8 * u]);
-                const float4 w1 = *reinterpret_cast<const float4*>(&wq[8 * u + 4]);
+                const float4 w0 = *reinterpret_cast<const float4*>(&wq[wq_at(8 * u)]);
+                const float4 w1 = *reinterpret_cast<const float4*>(&wq[wq_at(8 * u) + 4]);
                 const float2 x0 = bf2_to_f2(xv.x), x1 = bf2_to_f2(xv.y), x2 = bf2_to_f2(xv.z), x3 = bf2_to_f2(xv.w);
                 uint4 hi, lo;
                 split2(x0.x * w0.x, x0.y * w0.y, hi.x, lo.x);
