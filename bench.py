@@ -310,13 +310,15 @@ def run_ours(args, w):
     # e2e: pinned host inputs -> device, scan, y -> pinned host, every step.
     # The batch rows go in groups: a group's inputs are copied in on one
     # stream, scanned on the launch stream and its y copied out on a third,
-    # so the two copy directions (PCIe is full duplex) and the kernels overlap.
+    # so within a step the two copy directions (PCIe is full duplex) and the
+    # kernels overlap; a step's first copy waits until the previous step's y
+    # is on the host.
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
     d2h = y_host.numel() * y_host.element_size()
     K2 = max(3, min(K, 20))
-    n_groups = min(w.batch, 4)
+    n_groups = min(w.batch, 8)
     bounds = [(w.batch * i // n_groups, w.batch * (i + 1) // n_groups) for i in range(n_groups)]
     row_keys = [k for k, v in host.items() if isinstance(v, torch.Tensor) and v.dim() == 3]  # (batch, ., L)
     other_keys = [k for k, v in host.items() if isinstance(v, torch.Tensor) and v.dim() != 3]
@@ -324,14 +326,15 @@ def run_ours(args, w):
     ev_in = [torch.cuda.Event() for _ in bounds]
     ev_done = [torch.cuda.Event() for _ in bounds]
     ev_out = [torch.cuda.Event() for _ in bounds]
+    ev_step = torch.cuda.Event()
     work_g = []
     for b0, b1 in bounds:
         need_g = ops.workspace_bytes(b1 - b0, w.dim, w.seqlen, w.dtype, w.dstate)
         work_g.append(torch.empty(need_g, dtype=torch.uint8, device=dev) if need_g > 0 else None)
 
     def e2e_step():
+        s_in.wait_event(ev_step)  # the previous step is complete, y included
         for i, (b0, b1) in enumerate(bounds):
-            s_in.wait_event(ev_done[i])  # the previous step's scan of these rows has read its inputs
             with torch.cuda.stream(s_in):
                 if i == 0:
                     for k in other_keys:
@@ -349,9 +352,9 @@ def run_ours(args, w):
             with torch.cuda.stream(s_out):
                 y_host[b0:b1].copy_(y[b0:b1], non_blocking=True)
             ev_out[i].record(s_out)
-        stream.wait_event(ev_out[-1])
-        for e in ev_out[:-1]:
-            stream.wait_event(e)
+        for e in ev_out:
+            stream.wait_event(e)  # the step ends when its y is on the host
+        ev_step.record(stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)
@@ -512,7 +515,9 @@ def run_decode(args, w):
     ms = total_ms / K
     value = ws * w.elements_per_step / (ms * 1e-3)
 
-    # e2e: each step's token inputs from pinned host memory, y back to the host
+    # e2e: each step's token inputs from pinned host memory, y back to the
+    # host, in order on the launch stream (a step's copies are a few MB: split
+    # over groups of sequences and three streams they measured slower)
     hx = [{k: v.cpu().pin_memory() for k, v in x.items()} for x in xs]
     y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in hx[0].values())
@@ -536,6 +541,7 @@ def run_decode(args, w):
     torch.cuda.synchronize(dev)
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / K2
+    ops.check_device_error(stream)
     if rank != 0:
         return 0
     peak, peak_kind = hbm_peak()
