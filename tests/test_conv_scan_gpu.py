@@ -62,3 +62,23 @@ def test_conv_scan_in_two_pieces():
     yy = torch.cat([y1, y2], dim=2).double().cpu().numpy().reshape(-1, L)
     assert max_rel_err(yy, y.double().cpu().numpy().reshape(-1, L)) <= 1e-5
     assert max_rel_err(h2.cpu().numpy().reshape(-1, 16), h.cpu().numpy().reshape(-1, 16)) <= 1e-5
+
+
+def test_conv_scan_full_size_sampled():
+    """The fused convolution at the 8 x 2048 x 4096 bf16 shape, every output of sampled channels.
+
+    The oracle computes u = silu(conv(x)) and the scan for the sampled
+    channels of each batch row only (their B and C are the batch row's)."""
+    w = syn.SCAN_WORKLOADS["scan_b8_d2048_l4096_bf16"]
+    x = syn.workload_inputs(w)
+    cw, cb, cs = conv_params(w.dim, w.seed + 3, w.batch, w.dtype, bias=True, state=True)
+    y, h = run(x, cw, cb, cs)
+    chans = np.array([0, 1, 15, 16, 1023, 2030, 2047])
+    for b in range(w.batch):
+        sel = lambda t: None if t is None else t[b:b + 1, chans].contiguous()
+        u = oracle.causal_conv_silu(sel(x["u"]), cw[chans], cb[chans], cs[b:b + 1, chans])
+        yr, hr = oracle.scan(u, sel(x["delta"]), x["A"][chans], x["B"][b:b + 1], x["C"][b:b + 1],
+                             x["D"][chans], sel(x["z"]), x["delta_bias"][chans], x["softplus"])
+        e = max_rel_err(y[b, chans].double().cpu().numpy(), yr)
+        assert e <= TOL["bfloat16"], f"batch row {b}: y {e:.3e}"
+        assert max_rel_err(h[b, chans].cpu().numpy(), hr) <= TOL["bfloat16"]
