@@ -58,6 +58,8 @@ def test_workspace_size_follows_the_plan():
     (1, 40, 3000, torch.float32, 8, False, True),
     (1, 16, 4096, torch.bfloat16, 32, True, True),
     (1, 8, 2100, torch.float32, 64, False, False),
+    (1, 8, 4096, torch.bfloat16, 64, True, True),     # bf16 conversion of the state-only pass at N = 64
+    (2, 24, 3001, torch.bfloat16, 32, False, False),  # ragged channels at 16 states a lane, plain loads
 ])
 def test_split_parity(batch, dim, L, dtype, dstate, zoh, h0):
     assert planned(batch, dim, L, dstate, dtype) > 0, "the case should take the split"
